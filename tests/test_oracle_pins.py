@@ -1,0 +1,298 @@
+"""Pins of the CPU oracle against things other than itself (no GPU).
+
+* a pure-Python brute force (tests/bruteforce.py) on the tiny paged case and
+  on 200 random tiny cases (bf16 and fp8 caches, paged and contiguous);
+* hand-derived golden values (tests/golden/*.json);
+* PyTorch's fp64 scaled_dot_product_attention with an explicit mask;
+* invariants: softmax rows sum to 1, masked weights are exactly 0, page
+  relabelling / layout changes / key permutations leave the output unchanged,
+  split-KV merge equals the unsplit result, the append touches only its slots;
+* special cases with closed forms (one key, constant keys, decode causal ==
+  non-causal, empty rows).
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests import bruteforce
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _expr(s):
+    s = str(s)
+    if s == "-inf":
+        return -math.inf
+    if "ln(" in s:
+        return float(eval(s.replace("ln(", "math.log("), {"math": math}))
+    return float(Fraction(s))
+
+
+# ---------------------------------------------------------------------------
+# golden hand cases
+# ---------------------------------------------------------------------------
+def _hand_cases():
+    with open(os.path.join(GOLDEN, "attention_hand_cases.json")) as f:
+        return json.load(f)
+
+
+@pytest.mark.parametrize("case", _hand_cases()["cases"], ids=lambda c: c["name"])
+def test_golden_hand_attention(case):
+    q = np.array([[[_expr(x) for x in hd] for hd in tok] for tok in case["q"]])
+    K = np.array(case["k"], dtype=np.float64)
+    V = np.array(case["v"], dtype=np.float64)
+    o, lse = oracle.attend(q, K, V, case["causal"], case["scale"])
+    exp_o = np.array([[[_expr(x) for x in hd] for hd in tok] for tok in case["o"]])
+    exp_l = np.array([[_expr(x) for x in row] for row in case["lse"]])
+    np.testing.assert_allclose(o, exp_o, rtol=0, atol=1e-13)
+    fin = np.isfinite(exp_l)
+    assert np.array_equal(np.isfinite(lse), fin)
+    np.testing.assert_allclose(lse[fin], exp_l[fin], rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("vc", _hand_cases()["visible_counts"], ids=lambda v: str(v["q_lens"]))
+def test_golden_visible_counts(vc):
+    counts = []
+    for lq, lc, ln in zip(vc["q_lens"], vc["cache_lens"], vc["new_lens"]):
+        counts += list(oracle.visible_mask(lq, lc + ln, True).sum(axis=1))
+    assert counts == vc["counts"]
+
+
+# ---------------------------------------------------------------------------
+# brute force
+# ---------------------------------------------------------------------------
+def _check_against_bruteforce(case, tol=1e-12):
+    ref = oracle.forward(case)
+    out, lse, kc, vc = bruteforce.run(case)
+    out = np.array(out, dtype=np.float64).reshape(ref["out"].shape)
+    lse = np.array(lse, dtype=np.float64).reshape(ref["lse"].shape)
+    np.testing.assert_allclose(ref["out"], out, rtol=0, atol=tol)
+    fin = np.isfinite(lse)
+    assert np.array_equal(np.isfinite(ref["lse"]), fin)
+    np.testing.assert_allclose(ref["lse"][fin], lse[fin], rtol=0, atol=tol)
+    # appended / cached contents, position by position
+    spec = case.spec
+    for (b, pos, hk), codes in kc.items():
+        idx = oracle.physical_slots(spec, case.block_table, b, np.array([pos]))
+        got = ref["k_cache"][idx][0, hk]
+        assert list(int(x) for x in got) == codes
+        got = ref["v_cache"][idx][0, hk]
+        assert list(int(x) for x in got) == vc[b, pos, hk]
+
+
+@pytest.mark.parametrize("sentinel", ["finite", "nan"])
+def test_bruteforce_config1(sentinel):
+    _check_against_bruteforce(synth.config1(sentinel=sentinel))
+
+
+@pytest.mark.parametrize("seed", range(200))
+def test_bruteforce_random(seed):
+    dtype = "fp8" if seed % 4 == 3 else "bf16"
+    case = synth.random_case(seed, cache_dtype=dtype, with_new=(seed % 5 != 0),
+                             q_equals_new=(seed % 7 != 0), sentinel="nan" if seed % 3 == 0 else "finite")
+    _check_against_bruteforce(case)
+
+
+# ---------------------------------------------------------------------------
+# library cross-check
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("seed", range(20))
+def test_sdpa_crosscheck(seed):
+    torch = pytest.importorskip("torch")
+    case = synth.random_case(1000 + seed, max_cache=64, max_new=12, allow_zero=False)
+    spec = case.spec
+    ref = oracle.forward(case)
+    cu = spec.cu_q
+    for b in range(spec.batch):
+        lq, lk = int(spec.q_lens[b]), int(spec.kv_lens[b])
+        K = oracle.gather_sequence(spec, ref["k_cache"], case.block_table, b, lk)
+        V = oracle.gather_sequence(spec, ref["v_cache"], case.block_table, b, lk)
+        q = oracle.bf16_to_f64(case.q[cu[b]:cu[b] + lq])
+        tq = torch.from_numpy(q).permute(1, 0, 2)                  # (Hq, lq, D)
+        tk = torch.from_numpy(K).permute(1, 0, 2).repeat_interleave(spec.g, 0)
+        tv = torch.from_numpy(V).permute(1, 0, 2).repeat_interleave(spec.g, 0)
+        i = torch.arange(lq)[:, None]
+        j = torch.arange(lk)[None, :]
+        mask = (j <= i + (lk - lq)) if spec.causal else torch.ones(lq, lk, dtype=torch.bool)
+        o = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask,
+                                                             scale=spec.softmax_scale)
+        got = ref["out"][cu[b]:cu[b] + lq]
+        np.testing.assert_allclose(got, o.permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# invariants and closed forms
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("seed", range(10))
+def test_softmax_rows(seed):
+    rng = np.random.default_rng(seed)
+    lq, lk, hq, hkv, d = 5, 17, 4, 2, 8
+    q = rng.standard_normal((lq, hq, d)) * 3
+    K = rng.standard_normal((lk, hkv, d))
+    V = rng.standard_normal((lk, hkv, d))
+    for causal in (True, False):
+        o, lse, w = oracle.attend(q, K, V, causal, 0.3, return_weights=True)
+        mask = oracle.visible_mask(lq, lk, causal)
+        np.testing.assert_allclose(w.sum(axis=2), 1.0, rtol=0, atol=1e-12)
+        assert np.all(w >= 0) and np.all(w <= 1)
+        assert np.all(w[:, ~mask] == 0.0)
+        # o is exactly the weights applied to V
+        for h in range(hq):
+            np.testing.assert_allclose(o[:, h], w[h] @ V[:, h // 2], atol=1e-12)
+
+
+def test_single_key_returns_value_row():
+    rng = np.random.default_rng(3)
+    q = rng.standard_normal((1, 4, 8))
+    K = rng.standard_normal((1, 2, 8))
+    V = rng.standard_normal((1, 2, 8))
+    o, lse = oracle.attend(q, K, V, True, 0.5)
+    for h in range(4):
+        assert np.array_equal(o[0, h], V[0, h // 2])
+        assert lse[h, 0] == pytest.approx(0.5 * q[0, h] @ K[0, h // 2], abs=1e-14)
+
+
+def test_constant_keys_give_mean_of_visible_values():
+    rng = np.random.default_rng(4)
+    lq, lk = 3, 9
+    q = rng.standard_normal((lq, 2, 4))
+    K = np.tile(rng.standard_normal((1, 1, 4)), (lk, 1, 1))
+    V = rng.standard_normal((lk, 1, 4))
+    o, lse = oracle.attend(q, K, V, True, 1.0)
+    for i in range(lq):
+        n = i + (lk - lq) + 1
+        np.testing.assert_allclose(o[i, 0], V[:n, 0].mean(axis=0), atol=1e-13)
+        np.testing.assert_allclose(lse[0, i], q[i, 0] @ K[0, 0] + math.log(n), atol=1e-12)
+
+
+def test_decode_causal_equals_noncausal():
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((1, 4, 8))
+    K = rng.standard_normal((30, 2, 8))
+    V = rng.standard_normal((30, 2, 8))
+    a = oracle.attend(q, K, V, True, 0.2)
+    b = oracle.attend(q, K, V, False, 0.2)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_prefill_from_empty_cache_is_lower_triangular():
+    m = oracle.visible_mask(7, 7, True)
+    assert np.array_equal(m, np.tril(np.ones((7, 7), dtype=bool)))
+    m = oracle.visible_mask(3, 8, True)   # bottom-right: last row sees everything
+    assert m[-1].all() and m[0].sum() == 6
+
+
+def test_empty_rows_are_zero_with_minus_inf_lse():
+    q = np.ones((3, 1, 2))
+    K = np.ones((1, 1, 2))
+    V = np.full((1, 1, 2), 5.0)
+    o, lse = oracle.attend(q, K, V, True, 1.0)
+    assert np.all(o[:2] == 0) and np.all(np.isneginf(lse[0, :2]))
+    assert np.all(o[2] == 5.0)
+    o, lse = oracle.attend(np.ones((2, 1, 2)), np.zeros((0, 1, 2)), np.zeros((0, 1, 2)), False, 1.0)
+    assert np.all(o == 0) and np.all(np.isneginf(lse))
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_noncausal_key_permutation_invariance(seed):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((4, 4, 8))
+    K = rng.standard_normal((23, 2, 8))
+    V = rng.standard_normal((23, 2, 8))
+    p = rng.permutation(23)
+    a = oracle.attend(q, K, V, False, 0.4)
+    b = oracle.attend(q, K[p], V[p], False, 0.4)
+    np.testing.assert_allclose(a[0], b[0], atol=1e-13)
+    np.testing.assert_allclose(a[1], b[1], atol=1e-13)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_page_relabel_and_contiguous_equivalence(seed):
+    case = synth.random_case(300 + seed, page_size=4, max_cache=30, max_new=6, allow_zero=False)
+    ref = oracle.forward(case)
+    rel = synth.relabel_pages(case, np.random.default_rng(seed))
+    r2 = oracle.forward(rel)
+    assert np.array_equal(ref["out"], r2["out"]) and np.array_equal(ref["lse"], r2["lse"])
+    con = synth.to_contiguous(case)
+    r3 = oracle.forward(con)
+    np.testing.assert_allclose(ref["out"], r3["out"], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(ref["lse"], r3["lse"], rtol=0, atol=1e-13)
+
+
+def test_config1_paged_equals_contiguous():
+    case = synth.config1()
+    ref = oracle.forward(case)
+    r3 = oracle.forward(synth.to_contiguous(case))
+    np.testing.assert_allclose(ref["out"], r3["out"], rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_split_merge_equals_unsplit(seed):
+    rng = np.random.default_rng(seed)
+    lq, lk = int(rng.integers(1, 6)), int(rng.integers(6, 60))
+    q = rng.standard_normal((lq, 4, 8)) * 2
+    K = rng.standard_normal((lk, 2, 8))
+    V = rng.standard_normal((lk, 2, 8))
+    cuts = sorted(set(rng.integers(1, lk, size=int(rng.integers(1, 5))).tolist()))
+    bounds = [0] + cuts + [lk]
+    for causal in (True, False):
+        o, lse = oracle.attend(q, K, V, causal, 0.35)
+        o2, lse2 = oracle.split_forward(q, K, V, causal, 0.35, bounds)
+        np.testing.assert_allclose(o2, o, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse2, lse, rtol=0, atol=1e-13)
+
+
+def test_split_merge_handles_empty_chunk():
+    # causal decode-like row where a later chunk is fully masked
+    q = np.ones((1, 1, 2))
+    K = np.arange(12, dtype=float).reshape(6, 1, 2) / 10
+    V = np.arange(12, dtype=float).reshape(6, 1, 2)
+    o, lse = oracle.attend(q[:, :, :], K, V, True, 1.0)
+    lq = 1
+    o2, l2 = oracle.split_forward(q, K, V, True, 1.0, [0, 3, 6])
+    np.testing.assert_allclose(o2, o, atol=1e-13)
+    o_parts = np.stack([o, np.zeros_like(o)])
+    l_parts = np.stack([lse.T, np.full_like(lse.T, -np.inf)])
+    o3, l3 = oracle.combine_partials(o_parts, l_parts)
+    np.testing.assert_allclose(o3, o, atol=1e-15)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_append_touches_only_its_slots(seed):
+    for dtype in ("bf16", "fp8"):
+        case = synth.random_case(500 + seed, cache_dtype=dtype, max_cache=30, max_new=9)
+        spec = case.spec
+        kc0, vc0 = oracle.prepare_prefix(case)
+        kc, vc = oracle.append_kv(spec, kc0, vc0, case.block_table, case.k_new, case.v_new,
+                                  case.k_scale, case.v_scale)
+        touched = np.zeros(kc.shape[:2], dtype=bool)
+        cu = spec.cu_new
+        for b in range(spec.batch):
+            for t in range(int(spec.new_lens[b])):
+                pos = int(spec.cache_lens[b]) + t
+                idx = oracle.physical_slots(spec, case.block_table, b, np.array([pos]))
+                touched[idx] = True
+                row_k = kc[idx][0]
+                want = case.k_new[cu[b] + t]
+                if dtype == "fp8":
+                    want = oracle.fp8_quantize(want, case.k_scale)
+                assert np.array_equal(row_k, want)
+        assert np.array_equal(kc[~touched], kc0[~touched])
+        assert np.array_equal(vc[~touched], vc0[~touched])
+
+
+def test_algorithmic_work_closed_forms():
+    case = synth.config3(causal=True)
+    w = oracle.algorithmic_work(case.spec)
+    assert w["pairs"] == 8 * (512 * 1536 + 512 * 513 // 2)
+    case = synth.config3(causal=False)
+    assert oracle.algorithmic_work(case.spec)["pairs"] == 8 * 512 * 2048
+    spec = synth.config2().spec
+    w = oracle.algorithmic_work(spec)
+    assert w["kv_bytes"] == int(spec.kv_lens.sum()) * 8 * 128 * 2 * 2
