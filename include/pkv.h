@@ -1,0 +1,222 @@
+/*
+ * pkv.h -- C ABI of the GB300 (sm_103a) library for forward attention over a
+ * batched, variable-length KV cache (paged or contiguous).
+ *
+ * What the library computes, per sequence b, query head h (kv head h / G,
+ * G = Hq / Hkv) and query row i:
+ *     out[i,h] = softmax_j( scale * q[i,h] . K_b[j] + mask(i,j) ) V_b[j]
+ * over the keys of the cache after the new tokens of this call are appended.
+ * Sources (the pages this library follows):
+ *  - flash-attention PR "Add flash_attn_varlen_func_with_kvcache", Usage:
+ *    packed q with cu_seqlens_q / max_seqlen_q, optional new k/v appended into
+ *    the cache in place, cache-only attention when k/v are absent, contiguous
+ *    cache (batch_size_cache, seqlen_cache, n_heads, head_dim); Minor Changes:
+ *    per-sequence cache lengths apart from cu_seqlens_knew; Limitation:
+ *    num_splits fixed to 1 hurts decode (this library splits the KV instead).
+ *  - TransformerEngine PR "Add KV cache for paged/non-paged attention",
+ *    backend table and notes: paged and non-paged bshd caches, one page table
+ *    for K and V, pure prefill / pure decode / mixed phases in one call.
+ *  - vLLM PR "[Kernel][Triton][FP8] Adding fp8 and variable length sequence
+ *    support to Triton FAv2 kernel", feature list: causal masking, GQA/MQA,
+ *    8-bit KV cache; review: block_table support and mixed prefill/decode.
+ *  - flashinfer PR "[Refactor] Uniform PoDAttention API with Horizontal Fusion
+ *    SMs Schedule", Key Changes 2 and Limitations: one persistent launch for
+ *    prefill and decode work, partitioned by KV load; a host classifier of
+ *    prefill vs decode by query length (pkv_plan below).
+ *
+ * Conventions
+ *  - Pointers are DEVICE pointers unless the name starts with h_.  Every
+ *    device buffer is owned by the caller; the library never allocates or frees
+ *    device memory.  The plan (pkv_plan_t) is a host object owned by the
+ *    library until pkv_plan_destroy.
+ *  - bf16 tensors: q, out, k_new, v_new, and a bf16 cache.  fp8 caches hold OCP
+ *    e4m3 ("fn") codes with per-tensor fp32 scales: value = code * scale.
+ *  - Strides are in ELEMENTS (of the tensor's own type).  The innermost
+ *    (head_dim) stride is 1.  All base pointers must be 16-byte aligned and all
+ *    strides multiples of 16 bytes.
+ *  - Causal masking is bottom-right aligned: query i of a sequence with Lq
+ *    queries and Lk keys sees keys j <= i + Lk - Lq.  A query row that sees no
+ *    key gets out = 0 and lse = -inf.
+ *  - Head mapping: query head h reads kv head h / (Hq / Hkv).
+ *  - stream arguments are cudaStream_t passed as void* (NULL = legacy stream).
+ *  - Errors: every entry point returns a pkv_status.  Problems detectable on
+ *    the host are reported before anything is launched.  Problems found on the
+ *    device (a block_table entry out of range, an append past the capacity, a
+ *    bounded wait that ran out, lengths that differ from the plan's) never trap:
+ *    the kernel skips the access, and records the first such code in a device
+ *    status word that pkv_get_status reads.  pkv_last_error() returns a
+ *    thread-local message for the last failing call.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,          /* bad pointer, shape, stride or length      */
+  PKV_ERR_UNSUPPORTED = 2,          /* valid but outside the supported set        */
+  PKV_ERR_WORKSPACE_TOO_SMALL = 3,  /* workspace smaller than the plan requires  */
+  PKV_ERR_CUDA = 4,                 /* a CUDA runtime/driver call failed          */
+  PKV_ERR_DEVICE_TIMEOUT = 5,       /* device: a bounded wait gave up             */
+  PKV_ERR_DEVICE_BOUNDS = 6,        /* device: block_table entry / slot out of range */
+  PKV_ERR_PLAN_MISMATCH = 7         /* device: cache_seqlens differ from the plan */
+} pkv_status;
+
+typedef enum { PKV_BF16 = 0, PKV_FP8_E4M3 = 1 } pkv_dtype;
+
+/* Problem shape shared by the plan, the append and the attention call. */
+typedef struct {
+  int32_t batch;          /* number of sequences B                                   */
+  int32_t num_heads_q;    /* Hq                                                      */
+  int32_t num_heads_kv;   /* Hkv; Hq % Hkv == 0 (MQA: Hkv = 1)                       */
+  int32_t head_dim;       /* D: 64 or 128 (fp8 cache: 128)                           */
+  int32_t page_size;      /* 0 = contiguous cache; else a multiple of 16, <= 256     */
+  int32_t cache_capacity; /* tokens one sequence can hold: contiguous seqlen_cache,
+                             paged max_pages_per_seq * page_size                     */
+  int32_t num_pages;      /* paged: pages in the pool; contiguous: batch_size_cache  */
+  int32_t cache_dtype;    /* pkv_dtype                                               */
+  int32_t causal;         /* 0 / 1                                                   */
+  float softmax_scale;    /* e.g. 1/sqrt(D)                                          */
+} pkv_problem;
+
+/* Device tensors of one call. */
+typedef struct {
+  const void* q;                 /* (total_q, Hq, D) bf16                            */
+  int64_t q_stride_tok, q_stride_head;
+  void* out;                     /* (total_q, Hq, D) bf16, written                   */
+  int64_t o_stride_tok, o_stride_head;
+  float* lse;                    /* nullable; (Hq, total_q) fp32 natural-log LSE     */
+  const int32_t* cu_seqlens_q;   /* [B+1] prefix sums of query lengths               */
+  int32_t max_seqlen_q;          /* upper bound of the query lengths                 */
+  const void* k_new;             /* nullable; (total_new, Hkv, D) bf16               */
+  const void* v_new;             /* nullable iff k_new is                            */
+  int64_t knew_stride_tok, knew_stride_head;
+  const int32_t* cu_seqlens_knew;/* [B+1]; required iff k_new is given               */
+  void* k_cache;                 /* paged (pages, P, Hkv, D) | contiguous (Bc, S, Hkv, D) */
+  void* v_cache;                 /* same shape and strides as k_cache                */
+  int64_t kc_stride_page;        /* paged: elements between pages; contiguous: between
+                                    batch rows                                       */
+  int64_t kc_stride_tok, kc_stride_head;
+  const int32_t* cache_seqlens;  /* [B] cache length BEFORE this call's append       */
+  const int32_t* block_table;    /* [B, block_table_stride]; NULL for contiguous     */
+  int32_t block_table_stride;
+  const float* k_scale;          /* fp8 cache only: device fp32 scalar               */
+  const float* v_scale;          /* fp8 cache only: device fp32 scalar               */
+} pkv_fwd_args;
+
+typedef struct pkv_plan_s* pkv_plan_t;
+
+/* Plan statistics (tests and benchmarks). */
+typedef struct {
+  int32_t num_items;         /* CTA work items (tiles)                      */
+  int32_t num_decode_items;  /* of which decode tiles                       */
+  int32_t num_prefill_items; /* of which prefill tiles                      */
+  int32_t num_split_units;   /* decode units cut into several KV chunks     */
+  int32_t num_ctas;          /* persistent grid size                        */
+  int32_t total_q;           /* sum of query lengths                        */
+  int32_t total_new;         /* sum of appended tokens                      */
+  int32_t max_items_per_cta;
+  double max_cta_cost;       /* LPT makespan, model units                   */
+  double mean_cta_cost;
+} pkv_plan_stats;
+
+/*
+ * pkv_plan -- host scheduling step (flashinfer PR "Uniform PoDAttention API",
+ * Key Changes 2: partition by KV-cache load; Limitations: classifier on the
+ * query length).  Validates the shape, classifies every (sequence, kv head)
+ * as decode work (Lq*G <= 16 rows) or prefill work (128-row query tiles),
+ * cuts long decode units into KV chunks (split-KV, flash-attention PR,
+ * Limitation), and assigns all tiles to num_sms persistent CTAs longest first.
+ * h_q_lens / h_cache_lens / h_new_lens: host int32 [B]; h_new_lens may be NULL
+ * when the call appends nothing.  Zero lengths are accepted.  On success
+ * *out_plan owns a host work list and *out_workspace_bytes is the device
+ * workspace size that pkv_plan_upload and pkv_attn_varlen_kvcache_fwd need.
+ * Pure host code: no CUDA call.
+ */
+pkv_status pkv_plan(const pkv_problem* problem, const int32_t* h_q_lens,
+                    const int32_t* h_cache_lens, const int32_t* h_new_lens,
+                    int32_t num_sms, pkv_plan_t* out_plan, size_t* out_workspace_bytes);
+
+/* Copies the plan's work list into the caller's device workspace on `stream`
+ * (asynchronously; the host copy stays valid until pkv_plan_destroy) and clears
+ * the device status word.  Must precede pkv_attn_varlen_kvcache_fwd with this
+ * workspace. */
+pkv_status pkv_plan_upload(pkv_plan_t plan, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/* Statistics of a plan (host only). */
+pkv_status pkv_plan_get_stats(pkv_plan_t plan, pkv_plan_stats* stats);
+
+/* One scheduled tile as the plan made it (diagnostics and tests).  Rows of a
+ * tile are (query token, head of the group) pairs, row = token * G + g. */
+typedef struct {
+  int32_t seq;          /* sequence b                                        */
+  int32_t kv_head;      /* kv head                                           */
+  int32_t q_row0;       /* packed-q index of the first query token           */
+  int32_t q_index0;     /* index of that token within the sequence           */
+  int32_t n_q;          /* query tokens in the tile                          */
+  int32_t q_len;        /* Lq of the sequence                                */
+  int32_t kv_len;       /* Lk = cache_len + new_len                          */
+  int32_t kv_begin;     /* keys [kv_begin, kv_end) handled by this tile      */
+  int32_t kv_end;
+  int32_t kind;         /* 0 decode tile, 1 prefill tile                     */
+  int32_t partial_slot; /* -1: writes the output; else split-KV partial slot */
+  int32_t cta;          /* persistent CTA that runs it                       */
+} pkv_work_item;
+
+/* Copies up to `capacity` tiles, in CTA order, into h_items (host memory);
+ * *count receives the number of tiles in the plan. */
+pkv_status pkv_plan_get_items(pkv_plan_t plan, pkv_work_item* h_items, int32_t capacity, int32_t* count);
+
+/*
+ * pkv_attn_varlen_kvcache_fwd -- the whole call (flash-attention PR "Add
+ * flash_attn_varlen_func_with_kvcache", Usage): if args->k_new is given, the
+ * new tokens are first written into the cache at positions cache_seqlens[b] ..
+ * cache_seqlens[b] + new_len[b] - 1 (as pkv_kv_append), then every query
+ * attends the first cache_seqlens[b] + new_len[b] keys of its sequence.
+ * cache_seqlens itself is NOT advanced (the caller does that).  Launches the
+ * append (if any), one persistent attention kernel and, when a unit was
+ * split, one combine kernel; no host synchronisation and no allocation.
+ * The plan must have been made from the same lengths and uploaded into
+ * `workspace`.
+ */
+pkv_status pkv_attn_varlen_kvcache_fwd(const pkv_problem* problem, const pkv_fwd_args* args,
+                                       pkv_plan_t plan, void* workspace,
+                                       size_t workspace_bytes, void* stream);
+
+/*
+ * pkv_kv_append -- in-place append alone (flash-attention PR, Usage: "kv cache
+ * will be updated in-place"; TE PR: paged / non-paged bshd caches).  Writes
+ * token t of sequence b (t < new_len[b], new_len from cu_seqlens_knew) to
+ * logical position cache_seqlens[b] + t: page block_table[b][pos / P], slot
+ * pos % P (or row pos of batch b for a contiguous cache).  bf16 caches get the
+ * bits unchanged; fp8 caches get e4m3_rn_satfinite(fp32(x) * fp32(1/scale)),
+ * bit-exact.  total_new = sum of new lengths (host int).  device_status:
+ * nullable device int32 that receives the first device error code.
+ */
+pkv_status pkv_kv_append(const pkv_problem* problem, const pkv_fwd_args* args,
+                         int32_t total_new, int32_t* device_status, void* stream);
+
+/* Synchronises `stream`, reads the device status word of `workspace` into
+ * *device_status (a pkv_status) and resets it to PKV_OK. */
+pkv_status pkv_get_status(void* workspace, void* stream, int32_t* device_status);
+
+void pkv_plan_destroy(pkv_plan_t plan);
+
+/* Thread-local message describing the last failing call ("" if none). */
+const char* pkv_last_error(void);
+
+/* Library version string. */
+const char* pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

@@ -1,0 +1,136 @@
+// KV append scatter and split-KV combine kernels.
+//
+// Append: flash-attention PR "Add flash_attn_varlen_func_with_kvcache", Usage
+// ("kv cache will be updated in-place"; new k/v packed with cu_seqlens_k) and
+// Minor Changes (cache lengths kept apart from cu_seqlens_knew);
+// TransformerEngine PR "Add KV cache for paged/non-paged attention" (paged and
+// non-paged bshd caches, one page table for K and V); vLLM PR "[Kernel][Triton]
+// [FP8] ..." (8-bit KV cache).
+//
+// Combine: merge of the normalised partial outputs of KV chunks of one decode
+// unit by their log-sum-exp (the split-KV decode named in the flash-attention
+// PR's Limitation and review).
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace pkv {
+
+// One warp per (new token, kv head) row; lane l moves elements [l*E, l*E+E).
+template <int D, bool FP8>
+__global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
+  constexpr int E = D / 32;  // elements per lane: 4 (D=128) or 2 (D=64)
+  const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= (int64_t)p.total_new * p.hkv) return;
+  const int t = (int)(row / p.hkv);
+  const int h = (int)(row % p.hkv);
+  // sequence of token t: the largest b with cu_knew[b] <= t
+  int lo = 0, hi = p.batch;
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (__ldg(p.cu_knew + mid) <= t) lo = mid; else hi = mid;
+  }
+  const int b = lo;
+  const int pos = __ldg(p.cache_seqlens + b) + (t - __ldg(p.cu_knew + b));
+  if (pos < 0 || pos >= p.capacity) {
+    if (lane == 0) record_status(p.status, PKV_ERR_DEVICE_BOUNDS, b, pos);
+    return;
+  }
+  int64_t dst;
+  if (p.page_size > 0) {
+    const int page = __ldg(p.block_table + (int64_t)b * p.bt_stride + pos / p.page_size);
+    if (page < 0 || page >= p.num_pages) {
+      if (lane == 0) record_status(p.status, PKV_ERR_DEVICE_BOUNDS, b, page);
+      return;
+    }
+    dst = (int64_t)page * p.c_stride_page + (int64_t)(pos % p.page_size) * p.c_stride_tok;
+  } else {
+    dst = (int64_t)b * p.c_stride_page + (int64_t)pos * p.c_stride_tok;
+  }
+  dst += (int64_t)h * p.c_stride_head + lane * E;
+  const int64_t src = (int64_t)t * p.n_stride_tok + (int64_t)h * p.n_stride_head + lane * E;
+  const __nv_bfloat16* kin = p.k_new + src;
+  const __nv_bfloat16* vin = p.v_new + src;
+  if constexpr (!FP8) {
+    __nv_bfloat16* kc = reinterpret_cast<__nv_bfloat16*>(p.k_cache) + dst;
+    __nv_bfloat16* vc = reinterpret_cast<__nv_bfloat16*>(p.v_cache) + dst;
+    if constexpr (E == 4) {
+      *reinterpret_cast<uint2*>(kc) = __ldg(reinterpret_cast<const uint2*>(kin));
+      *reinterpret_cast<uint2*>(vc) = __ldg(reinterpret_cast<const uint2*>(vin));
+    } else {
+      *reinterpret_cast<uint32_t*>(kc) = __ldg(reinterpret_cast<const uint32_t*>(kin));
+      *reinterpret_cast<uint32_t*>(vc) = __ldg(reinterpret_cast<const uint32_t*>(vin));
+    }
+  } else {
+    static_assert(E == 4, "fp8 cache rows are 128 elements");
+    // one IEEE reciprocal per call, then an RN multiply per element (no FMA)
+    const float inv_k = __frcp_rn(__ldg(p.k_scale));
+    const float inv_v = __frcp_rn(__ldg(p.v_scale));
+    const uint2 kr = __ldg(reinterpret_cast<const uint2*>(kin));
+    const uint2 vr = __ldg(reinterpret_cast<const uint2*>(vin));
+    auto lo_f = [](uint32_t w) { return __uint_as_float(w << 16); };
+    auto hi_f = [](uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); };
+    const uint32_t k01 = f32x2_to_e4m3x2(__fmul_rn(lo_f(kr.x), inv_k), __fmul_rn(hi_f(kr.x), inv_k));
+    const uint32_t k23 = f32x2_to_e4m3x2(__fmul_rn(lo_f(kr.y), inv_k), __fmul_rn(hi_f(kr.y), inv_k));
+    const uint32_t v01 = f32x2_to_e4m3x2(__fmul_rn(lo_f(vr.x), inv_v), __fmul_rn(hi_f(vr.x), inv_v));
+    const uint32_t v23 = f32x2_to_e4m3x2(__fmul_rn(lo_f(vr.y), inv_v), __fmul_rn(hi_f(vr.y), inv_v));
+    *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(p.k_cache) + dst) = k01 | (k23 << 16);
+    *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(p.v_cache) + dst) = v01 | (v23 << 16);
+  }
+}
+
+// One block per split unit; thread d owns column d of every row.
+// Partials are normalised outputs with log2-domain LSEs; the merge order over
+// chunks is fixed (deterministic).
+template <int D>
+__global__ void __launch_bounds__(D) combine_kernel(const CombineParams p) {
+  const CombineItem ci = p.items[blockIdx.x];
+  const int d = threadIdx.x;
+  const int rows = ci.n_q * p.G;
+  constexpr float kLn2 = 0.693147180559945309f;
+  for (int r = 0; r < rows; ++r) {
+    float m = -INFINITY;
+    for (int s = 0; s < ci.nsplit; ++s) m = fmaxf(m, p.partial_lse[(ci.slot0 + s) * kDecodeRows + r]);
+    const float m_use = m == -INFINITY ? 0.f : m;
+    float wsum = 0.f, acc = 0.f;
+    for (int s = 0; s < ci.nsplit; ++s) {
+      const float l = p.partial_lse[(ci.slot0 + s) * kDecodeRows + r];
+      const float w = ex2(l - m_use);
+      wsum += w;
+      acc += w * p.partial_o[((int64_t)(ci.slot0 + s) * kDecodeRows + r) * D + d];
+    }
+    const float o = wsum > 0.f ? acc / wsum : 0.f;
+    const int tok = ci.q_row0 + r / p.G;
+    const int head = ci.hk * p.G + r % p.G;
+    p.out[(int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head + d] = __float2bfloat16_rn(o);
+    if (p.lse != nullptr && d == 0)
+      p.lse[(int64_t)head * p.total_q + tok] = wsum > 0.f ? (m_use + __log2f(wsum)) * kLn2 : -INFINITY;
+  }
+}
+
+cudaError_t launch_kv_append(const AppendParams& p, int head_dim, bool fp8, cudaStream_t stream) {
+  const int64_t rows = (int64_t)p.total_new * p.hkv;
+  if (rows == 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t blocks = (rows * 32 + threads - 1) / threads;
+  if (blocks > INT32_MAX) return cudaErrorInvalidValue;
+  if (fp8) {
+    kv_append_kernel<128, true><<<(unsigned)blocks, threads, 0, stream>>>(p);
+  } else if (head_dim == 128) {
+    kv_append_kernel<128, false><<<(unsigned)blocks, threads, 0, stream>>>(p);
+  } else {
+    kv_append_kernel<64, false><<<(unsigned)blocks, threads, 0, stream>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const CombineParams& p, int num_items, int head_dim, cudaStream_t stream) {
+  if (num_items == 0) return cudaSuccess;
+  if (head_dim == 128) combine_kernel<128><<<num_items, 128, 0, stream>>>(p);
+  else combine_kernel<64><<<num_items, 64, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

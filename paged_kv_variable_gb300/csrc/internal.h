@@ -1,0 +1,82 @@
+// Internal layout shared by the host plan and the device kernels.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+constexpr int kKvTile = 128;        // keys per K/V tile (one pipeline stage)
+constexpr int kDecodeRows = 16;     // rows (query tokens x G) of a decode tile
+constexpr int kPrefillRows = 64;    // rows of a prefill tile (4 warps x 16)
+constexpr int kBoxRows = 16;        // cache rows per TMA box (divides every page size)
+
+enum ItemKind : int32_t { kDecode = 0, kPrefill = 1 };
+
+// One tile of work for one persistent CTA.  Rows of the tile are
+// (query token, head in group) pairs: row r = token * G + g.
+struct WorkItem {
+  int32_t b;         // sequence
+  int32_t hk;        // kv head
+  int32_t q_row0;    // packed-q index of the tile's first query token
+  int32_t q_i0;      // index of that token within its sequence
+  int32_t n_q;       // query tokens in the tile
+  int32_t lq;        // query length of the sequence
+  int32_t lk;        // attended keys of the sequence (cache + new)
+  int32_t kv_begin;  // key range of this item, kv_begin a multiple of kKvTile
+  int32_t kv_end;
+  int32_t kind;      // ItemKind
+  int32_t partial;   // -1: write the final output; else partial slot
+  int32_t cost;      // model cost (diagnostics)
+};
+static_assert(sizeof(WorkItem) == 48, "WorkItem layout");
+
+// A split decode unit merged by the combine kernel: slots slot0 .. slot0+nsplit-1.
+struct CombineItem {
+  int32_t q_row0;
+  int32_t n_q;
+  int32_t hk;
+  int32_t nsplit;
+  int32_t slot0;
+  int32_t pad[3];
+};
+static_assert(sizeof(CombineItem) == 32, "CombineItem layout");
+
+// Byte offsets of the sections of the caller's workspace.
+struct WorkspaceLayout {
+  size_t status;        // int32[4]: code, info0, info1, info2
+  size_t items;         // WorkItem[num_items], grouped by CTA
+  size_t cta_begin;     // int32[num_ctas + 1]
+  size_t combine;       // CombineItem[num_combine]
+  size_t plan_lc;       // int32[B] cache lengths the plan was made for
+  size_t partial_o;     // float[num_slots * kDecodeRows * D]
+  size_t partial_lse;   // float[num_slots * kDecodeRows] (log2 domain)
+  size_t total;
+};
+
+}  // namespace pkv
+
+// Host plan object (opaque to callers).
+struct pkv_plan_s {
+  pkv_problem problem;
+  int32_t num_ctas;
+  int32_t num_slots;
+  int32_t total_q;
+  int32_t total_new;
+  int32_t max_items_per_cta;
+  int32_t num_decode_items, num_prefill_items, num_split_units;
+  double max_cta_cost, mean_cta_cost;
+  pkv::WorkspaceLayout layout;
+  // host staging image of the workspace head (everything except partials)
+  unsigned char* image;
+  size_t image_bytes;
+  int32_t num_items;
+  int32_t num_combine;
+};
+
+namespace pkv {
+// thread-local error message helpers (api.cu)
+pkv_status fail(pkv_status st, const char* fmt, ...);
+}  // namespace pkv

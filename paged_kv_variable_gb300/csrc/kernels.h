@@ -1,0 +1,76 @@
+// Kernel parameter blocks and launchers (internal).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace pkv {
+
+struct AppendParams {
+  const __nv_bfloat16* k_new;
+  const __nv_bfloat16* v_new;
+  int64_t n_stride_tok, n_stride_head;
+  const int32_t* cu_knew;
+  const int32_t* cache_seqlens;
+  void* k_cache;
+  void* v_cache;
+  int64_t c_stride_page, c_stride_tok, c_stride_head;
+  const int32_t* block_table;
+  int32_t bt_stride;
+  int32_t page_size;
+  int32_t num_pages;
+  int32_t capacity;
+  int32_t batch;
+  int32_t hkv;
+  int32_t total_new;
+  const float* k_scale;
+  const float* v_scale;
+  int* status;
+};
+
+struct CombineParams {
+  const CombineItem* items;
+  const float* partial_o;
+  const float* partial_lse;
+  __nv_bfloat16* out;
+  int64_t o_stride_tok, o_stride_head;
+  float* lse;
+  int32_t total_q;
+  int32_t G;
+};
+
+struct AttnParams {
+  const __nv_bfloat16* q;
+  int64_t q_stride_tok, q_stride_head;
+  __nv_bfloat16* out;
+  int64_t o_stride_tok, o_stride_head;
+  float* lse;
+  int32_t total_q;
+  const int32_t* block_table;
+  int32_t bt_stride;
+  int32_t page_size;   // 0 = contiguous
+  int32_t num_pages;   // page pool size (contiguous: batch rows of the cache)
+  int32_t G;
+  int32_t causal;
+  float scale_log2;    // softmax_scale * log2(e)
+  const float* k_scale;
+  const float* v_scale;
+  const WorkItem* items;
+  const int32_t* cta_begin;
+  float* partial_o;
+  float* partial_lse;
+  int* status;
+  const int32_t* cache_seqlens;
+  const int32_t* plan_lc;
+  int32_t batch;
+};
+
+cudaError_t launch_kv_append(const AppendParams& p, int head_dim, bool fp8, cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams& p, int num_items, int head_dim, cudaStream_t stream);
+cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v, int num_ctas,
+                             int head_dim, bool fp8, cudaStream_t stream);
+
+}  // namespace pkv

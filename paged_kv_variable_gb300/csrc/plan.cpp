@@ -1,0 +1,317 @@
+// Host scheduling step: validation, prefill/decode classification, split-KV
+// chunking and longest-processing-time assignment of tiles to persistent CTAs.
+//
+// flashinfer PR "[Refactor] Uniform PoDAttention API with Horizontal Fusion SMs
+// Schedule": one persistent launch serves prefill and decode requests, the
+// partition of SMs follows the KV-cache load (Key Changes 2), requests are
+// classified by query length (Limitations: "qo_len > threshold"), and a zero
+// KV length must not be rejected (the review's failing test).  flash-attention
+// PR "Add flash_attn_varlen_func_with_kvcache", Limitation: a fixed
+// num_splits = 1 hurts decode, so decode units are cut into KV chunks here.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <functional>
+#include <new>
+#include <queue>
+#include <vector>
+
+#include "internal.h"
+
+namespace pkv {
+
+namespace {
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Tile {
+  WorkItem item;
+  double cost;
+};
+
+// Per-key model costs (relative units): a decode key streams 2*D*esize bytes
+// from HBM for one kv head; a prefill key costs one 128-row MMA step.
+double decode_cost(int keys, int d, int esize) { return 64.0 + keys * (2.0 * d * esize) / 512.0; }
+double prefill_cost(int keys, int rows, int d) { return 256.0 + keys * (rows * d * 4.0) / 65536.0 * 0.7; }
+
+}  // namespace
+
+pkv_status validate_problem(const pkv_problem* p) {
+  if (!p) return fail(PKV_ERR_INVALID_ARG, "problem is NULL");
+  if (p->batch < 0) return fail(PKV_ERR_INVALID_ARG, "batch < 0");
+  if (p->num_heads_q <= 0 || p->num_heads_kv <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "head counts must be positive");
+  if (p->num_heads_q % p->num_heads_kv != 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_heads_q (%d) %% num_heads_kv (%d) != 0", p->num_heads_q,
+                p->num_heads_kv);
+  int g = p->num_heads_q / p->num_heads_kv;
+  if (g > kDecodeRows)
+    return fail(PKV_ERR_UNSUPPORTED, "group size Hq/Hkv = %d > %d", g, kDecodeRows);
+  if (p->cache_dtype != PKV_BF16 && p->cache_dtype != PKV_FP8_E4M3)
+    return fail(PKV_ERR_INVALID_ARG, "cache_dtype %d unknown", p->cache_dtype);
+  if (p->head_dim != 64 && p->head_dim != 128)
+    return fail(PKV_ERR_UNSUPPORTED, "head_dim %d not in {64, 128}", p->head_dim);
+  if (p->cache_dtype == PKV_FP8_E4M3 && p->head_dim != 128)
+    return fail(PKV_ERR_UNSUPPORTED, "fp8 cache needs head_dim 128");
+  if (p->page_size < 0 || (p->page_size > 0 && (p->page_size % kBoxRows != 0 || p->page_size > 256)))
+    return fail(PKV_ERR_UNSUPPORTED, "page_size %d: 0 or a multiple of 16 up to 256", p->page_size);
+  if (p->cache_capacity <= 0) return fail(PKV_ERR_INVALID_ARG, "cache_capacity must be positive");
+  if (p->page_size > 0 && p->cache_capacity % p->page_size != 0)
+    return fail(PKV_ERR_INVALID_ARG, "cache_capacity must be a multiple of page_size");
+  if (p->num_pages <= 0) return fail(PKV_ERR_INVALID_ARG, "num_pages must be positive");
+  if (p->page_size == 0 && p->num_pages < p->batch)
+    return fail(PKV_ERR_INVALID_ARG, "contiguous cache: batch_size_cache (num_pages) < batch");
+  if (!std::isfinite(p->softmax_scale) || p->softmax_scale == 0.0f)
+    return fail(PKV_ERR_INVALID_ARG, "softmax_scale must be finite and non-zero");
+  return PKV_OK;
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" pkv_status pkv_plan(const pkv_problem* problem, const int32_t* h_q_lens,
+                               const int32_t* h_cache_lens, const int32_t* h_new_lens,
+                               int32_t num_sms, pkv_plan_t* out_plan, size_t* out_workspace_bytes) {
+  if (!out_plan || !out_workspace_bytes) return fail(PKV_ERR_INVALID_ARG, "output pointers are NULL");
+  *out_plan = nullptr;
+  *out_workspace_bytes = 0;
+  pkv_status st = validate_problem(problem);
+  if (st != PKV_OK) return st;
+  const pkv_problem& p = *problem;
+  const int B = p.batch;
+  if (B > 0 && (!h_q_lens || !h_cache_lens)) return fail(PKV_ERR_INVALID_ARG, "length arrays are NULL");
+  if (num_sms <= 0) return fail(PKV_ERR_INVALID_ARG, "num_sms must be positive");
+
+  const int G = p.num_heads_q / p.num_heads_kv;
+  const int D = p.head_dim;
+  const int esize = p.cache_dtype == PKV_BF16 ? 2 : 1;
+  const int tq_prefill = kPrefillRows / G;  // query tokens per prefill tile
+
+  int64_t total_q = 0, total_new = 0, total_decode_keys = 0;
+  for (int b = 0; b < B; ++b) {
+    int lq = h_q_lens[b], lc = h_cache_lens[b], ln = h_new_lens ? h_new_lens[b] : 0;
+    if (lq < 0 || lc < 0 || ln < 0) return fail(PKV_ERR_INVALID_ARG, "negative length at sequence %d", b);
+    if ((int64_t)lc + ln > p.cache_capacity)
+      return fail(PKV_ERR_INVALID_ARG, "sequence %d: cache_len %d + new_len %d > capacity %d", b, lc, ln,
+                  p.cache_capacity);
+    total_q += lq;
+    total_new += ln;
+    if (lq > 0 && (int64_t)lq * G <= kDecodeRows) total_decode_keys += (int64_t)(lc + ln) * p.num_heads_kv;
+  }
+  if (total_q > INT32_MAX / 2 || total_new > INT32_MAX / 2)
+    return fail(PKV_ERR_UNSUPPORTED, "total tokens too large");
+
+  // split-KV chunk for decode units: at least 4 decode items per CTA, chunks >= 512 keys
+  int64_t chunk = 1 << 30;
+  if (total_decode_keys > 0) {
+    int64_t target = 4LL * num_sms;
+    chunk = (total_decode_keys + target - 1) / target;
+    chunk = std::max<int64_t>(512, (chunk + kKvTile - 1) / kKvTile * kKvTile);
+  }
+
+  std::vector<Tile> tiles;
+  std::vector<CombineItem> combines;
+  int32_t num_slots = 0, n_dec = 0, n_pre = 0;
+  int64_t q_row = 0;
+  for (int b = 0; b < B; ++b) {
+    int lq = h_q_lens[b], lc = h_cache_lens[b], ln = h_new_lens ? h_new_lens[b] : 0;
+    int lk = lc + ln;
+    if (lq == 0) continue;
+    for (int hk = 0; hk < p.num_heads_kv; ++hk) {
+      if (lq * G <= kDecodeRows) {
+        int nchunks = lk <= chunk ? 1 : (int)((lk + chunk - 1) / chunk);
+        int slot0 = nchunks > 1 ? num_slots : -1;
+        for (int c = 0; c < nchunks; ++c) {
+          Tile t{};
+          t.item.b = b;
+          t.item.hk = hk;
+          t.item.q_row0 = (int32_t)q_row;
+          t.item.q_i0 = 0;
+          t.item.n_q = lq;
+          t.item.lq = lq;
+          t.item.lk = lk;
+          t.item.kv_begin = (int32_t)std::min<int64_t>((int64_t)c * chunk, lk);
+          t.item.kv_end = (int32_t)std::min<int64_t>((int64_t)(c + 1) * chunk, lk);
+          t.item.kind = kDecode;
+          t.item.partial = nchunks > 1 ? num_slots + c : -1;
+          t.cost = decode_cost(t.item.kv_end - t.item.kv_begin, D, esize);
+          t.item.cost = (int32_t)std::min(t.cost, 2.0e9);
+          tiles.push_back(t);
+          ++n_dec;
+        }
+        if (nchunks > 1) {
+          CombineItem ci{};
+          ci.q_row0 = (int32_t)q_row;
+          ci.n_q = lq;
+          ci.hk = hk;
+          ci.nsplit = nchunks;
+          ci.slot0 = slot0;
+          combines.push_back(ci);
+          num_slots += nchunks;
+        }
+      } else {
+        for (int i0 = 0; i0 < lq; i0 += tq_prefill) {
+          int n = std::min(tq_prefill, lq - i0);
+          int kv_end = lk;
+          if (p.causal) kv_end = std::max(0, std::min(lk, i0 + n + lk - lq));
+          Tile t{};
+          t.item.b = b;
+          t.item.hk = hk;
+          t.item.q_row0 = (int32_t)(q_row + i0);
+          t.item.q_i0 = i0;
+          t.item.n_q = n;
+          t.item.lq = lq;
+          t.item.lk = lk;
+          t.item.kv_begin = 0;
+          t.item.kv_end = kv_end;
+          t.item.kind = kPrefill;
+          t.item.partial = -1;
+          t.cost = prefill_cost(kv_end, kPrefillRows, D);
+          t.item.cost = (int32_t)std::min(t.cost, 2.0e9);
+          tiles.push_back(t);
+          ++n_pre;
+        }
+      }
+    }
+    q_row += lq;
+  }
+
+  // longest processing time first onto the least-loaded CTA
+  const int num_items = (int)tiles.size();
+  const int num_ctas = std::max(1, std::min(num_sms, num_items));
+  std::vector<int> order(num_items);
+  for (int i = 0; i < num_items; ++i) order[i] = i;
+  std::stable_sort(order.begin(), order.end(), [&](int a, int c) { return tiles[a].cost > tiles[c].cost; });
+  using Load = std::pair<double, int>;
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+  for (int c = 0; c < num_ctas; ++c) heap.push({0.0, c});
+  std::vector<std::vector<int>> per_cta(num_ctas);
+  for (int idx : order) {
+    Load l = heap.top();
+    heap.pop();
+    per_cta[l.second].push_back(idx);
+    l.first += tiles[idx].cost;
+    heap.push(l);
+  }
+  double max_cost = 0, sum_cost = 0;
+  int max_items = 0;
+  while (!heap.empty()) {
+    max_cost = std::max(max_cost, heap.top().first);
+    sum_cost += heap.top().first;
+    heap.pop();
+  }
+  for (auto& v : per_cta) max_items = std::max<int>(max_items, (int)v.size());
+
+  // workspace layout
+  WorkspaceLayout L{};
+  size_t off = 0;
+  L.status = off;
+  off = align_up(off + 16, 256);
+  L.items = off;
+  off = align_up(off + sizeof(WorkItem) * (size_t)std::max(1, num_items), 256);
+  L.cta_begin = off;
+  off = align_up(off + sizeof(int32_t) * (size_t)(num_ctas + 1), 256);
+  L.combine = off;
+  off = align_up(off + sizeof(CombineItem) * (size_t)std::max<size_t>(1, combines.size()), 256);
+  L.plan_lc = off;
+  off = align_up(off + sizeof(int32_t) * (size_t)std::max(1, B), 256);
+  size_t image_bytes = off;
+  L.partial_o = off;
+  off = align_up(off + sizeof(float) * (size_t)num_slots * kDecodeRows * D, 256);
+  L.partial_lse = off;
+  off = align_up(off + sizeof(float) * (size_t)num_slots * kDecodeRows, 256);
+  L.total = off;
+
+  pkv_plan_s* plan = new (std::nothrow) pkv_plan_s();
+  if (!plan) return fail(PKV_ERR_INVALID_ARG, "out of host memory");
+  plan->image = (unsigned char*)calloc(1, image_bytes);
+  if (!plan->image) {
+    delete plan;
+    return fail(PKV_ERR_INVALID_ARG, "out of host memory");
+  }
+  plan->problem = p;
+  plan->num_ctas = num_items > 0 ? num_ctas : 0;
+  plan->num_slots = num_slots;
+  plan->total_q = (int32_t)total_q;
+  plan->total_new = (int32_t)total_new;
+  plan->max_items_per_cta = max_items;
+  plan->num_decode_items = n_dec;
+  plan->num_prefill_items = n_pre;
+  plan->num_split_units = (int32_t)combines.size();
+  plan->max_cta_cost = max_cost;
+  plan->mean_cta_cost = num_ctas ? sum_cost / num_ctas : 0.0;
+  plan->layout = L;
+  plan->image_bytes = image_bytes;
+  plan->num_items = num_items;
+  plan->num_combine = (int32_t)combines.size();
+
+  WorkItem* items = (WorkItem*)(plan->image + L.items);
+  int32_t* cta_begin = (int32_t*)(plan->image + L.cta_begin);
+  int k = 0;
+  for (int c = 0; c < num_ctas; ++c) {
+    cta_begin[c] = k;
+    for (int idx : per_cta[c]) items[k++] = tiles[idx].item;
+  }
+  cta_begin[num_ctas] = k;
+  if (!combines.empty()) memcpy(plan->image + L.combine, combines.data(), combines.size() * sizeof(CombineItem));
+  int32_t* lc = (int32_t*)(plan->image + L.plan_lc);
+  for (int b = 0; b < B; ++b) lc[b] = h_cache_lens[b];
+
+  *out_plan = plan;
+  *out_workspace_bytes = L.total;
+  return PKV_OK;
+}
+
+extern "C" pkv_status pkv_plan_get_stats(pkv_plan_t plan, pkv_plan_stats* s) {
+  if (!plan || !s) return fail(PKV_ERR_INVALID_ARG, "NULL plan or stats");
+  s->num_items = plan->num_items;
+  s->num_decode_items = plan->num_decode_items;
+  s->num_prefill_items = plan->num_prefill_items;
+  s->num_split_units = plan->num_split_units;
+  s->num_ctas = plan->num_ctas;
+  s->total_q = plan->total_q;
+  s->total_new = plan->total_new;
+  s->max_items_per_cta = plan->max_items_per_cta;
+  s->max_cta_cost = plan->max_cta_cost;
+  s->mean_cta_cost = plan->mean_cta_cost;
+  return PKV_OK;
+}
+
+extern "C" pkv_status pkv_plan_get_items(pkv_plan_t plan, pkv_work_item* h_items, int32_t capacity,
+                                         int32_t* count) {
+  if (!plan || !count) return fail(PKV_ERR_INVALID_ARG, "NULL plan or count");
+  *count = plan->num_items;
+  if (!h_items || capacity <= 0) return PKV_OK;
+  const WorkItem* items = (const WorkItem*)(plan->image + plan->layout.items);
+  const int32_t* cta_begin = (const int32_t*)(plan->image + plan->layout.cta_begin);
+  int n = 0;
+  for (int c = 0; c < plan->num_ctas && n < capacity; ++c) {
+    for (int k = cta_begin[c]; k < cta_begin[c + 1] && n < capacity; ++k, ++n) {
+      const WorkItem& w = items[k];
+      pkv_work_item& o = h_items[n];
+      o.seq = w.b;
+      o.kv_head = w.hk;
+      o.q_row0 = w.q_row0;
+      o.q_index0 = w.q_i0;
+      o.n_q = w.n_q;
+      o.q_len = w.lq;
+      o.kv_len = w.lk;
+      o.kv_begin = w.kv_begin;
+      o.kv_end = w.kv_end;
+      o.kind = w.kind;
+      o.partial_slot = w.partial;
+      o.cta = c;
+    }
+  }
+  return PKV_OK;
+}
+
+extern "C" void pkv_plan_destroy(pkv_plan_t plan) {
+  if (!plan) return;
+  free(plan->image);
+  delete plan;
+}

@@ -168,7 +168,7 @@ def _fill_code(cache_dtype: str, sentinel: str):
 def make_case(spec: Spec, rng: np.random.Generator, *, block_table_width: Optional[int] = None,
               explicit_block_table: Optional[np.ndarray] = None, num_pages: Optional[int] = None,
               with_new: bool = True, sentinel: str = "finite", q_mult: float = 1.0,
-              page_perm: bool = True) -> Case:
+              page_perm: bool = True, draw_values: bool = True) -> Case:
     """Draw a case for ``spec`` (lengths already fixed in the spec).
 
     Paged pool: exactly the pages each sequence needs for ``cache_lens +
@@ -207,6 +207,9 @@ def make_case(spec: Spec, rng: np.random.Generator, *, block_table_width: Option
         npages = 0
         cache_shape = (B, spec.capacity, Hkv, D)
 
+    if not draw_values:   # lengths and page map only (host scheduling tests)
+        return Case(spec=spec, q=None, k_new=None, v_new=None, k_cache=None, v_cache=None,
+                    block_table=block_table, num_pages=npages, poison_page=poison, sentinel=sentinel)
     q = _normal_bf16(rng, (spec.total_q, Hq, D), q_mult)
     total_prefix = int(spec.cache_lens.sum())
     prefix_k = _normal_bf16(rng, (total_prefix, Hkv, D))
@@ -307,7 +310,7 @@ def config1(sentinel: str = "finite") -> Case:
     return make_case(spec, rng, explicit_block_table=bt, num_pages=8, sentinel=sentinel)
 
 
-def config2(sentinel: str = "finite") -> Case:
+def config2(sentinel: str = "finite", draw_values: bool = True) -> Case:
     """Decode: B=64, 1 query/new token each, Hq=32, Hkv=8, D=128, cache lens
     U[512,4096], paged P=16, block_table width 257."""
     rng = np.random.Generator(np.random.PCG64(1002))
@@ -317,10 +320,10 @@ def config2(sentinel: str = "finite") -> Case:
     spec = Spec(batch=B, hq=32, hkv=8, d=128, page_size=16, causal=True, softmax_scale=_scale(128),
                 cache_dtype="bf16", q_lens=ones, cache_lens=lc, new_lens=ones.copy(),
                 capacity=257 * 16, name="cfg2-decode-paged")
-    return make_case(spec, rng, block_table_width=257, sentinel=sentinel)
+    return make_case(spec, rng, block_table_width=257, sentinel=sentinel, draw_values=draw_values)
 
 
-def config3(causal: bool = True, sentinel: str = "finite") -> Case:
+def config3(causal: bool = True, sentinel: str = "finite", draw_values: bool = True) -> Case:
     """Prefill with a cached prefix, contiguous cache (8, 2048, 8, 128):
     B=8, 512 new q/k/v tokens on a 1536-token prefix, Hq=32, Hkv=8, D=128."""
     rng = np.random.Generator(np.random.PCG64(1003))
@@ -329,10 +332,10 @@ def config3(causal: bool = True, sentinel: str = "finite") -> Case:
     spec = Spec(batch=B, hq=32, hkv=8, d=128, page_size=0, causal=causal, softmax_scale=_scale(128),
                 cache_dtype="bf16", q_lens=n, cache_lens=np.full(B, 1536, np.int32), new_lens=n.copy(),
                 capacity=2048, name="cfg3-prefill-contig-" + ("causal" if causal else "noncausal"))
-    return make_case(spec, rng, sentinel=sentinel)
+    return make_case(spec, rng, sentinel=sentinel, draw_values=draw_values)
 
 
-def config4(sentinel: str = "finite") -> Case:
+def config4(sentinel: str = "finite", draw_values: bool = True) -> Case:
     """Mixed in-flight batch, paged P=16: 64 requests in seeded order = 60 decode
     (1 token, cache len U[1024,8192]) + 4 prefill (2048 tokens on a U[0,2048]
     prefix); Hq=32, Hkv=8, D=128, causal; block_table width 513."""
@@ -346,7 +349,7 @@ def config4(sentinel: str = "finite") -> Case:
     spec = Spec(batch=64, hq=32, hkv=8, d=128, page_size=16, causal=True, softmax_scale=_scale(128),
                 cache_dtype="bf16", q_lens=lq, cache_lens=lc, new_lens=lq.copy(),
                 capacity=513 * 16, name="cfg4-mixed-paged")
-    return make_case(spec, rng, block_table_width=513, sentinel=sentinel)
+    return make_case(spec, rng, block_table_width=513, sentinel=sentinel, draw_values=draw_values)
 
 
 def config5(sentinel: str = "finite", batch: int = 64, seqlen: int = 2048) -> tuple[Case, Case]:
@@ -433,3 +436,24 @@ def uniform_spec(name: str, batch: int, q_len: int, cache_len: int, *, hq=32, hk
                 softmax_scale=float(np.float32(1.0 / math.sqrt(d))), cache_dtype=cache_dtype,
                 q_lens=np.full(batch, q_len, np.int32), cache_lens=np.full(batch, cache_len, np.int32),
                 new_lens=np.full(batch, q_len, np.int32), capacity=cap, name=name)
+
+
+def subset_case(case: Case, seqs) -> Case:
+    """The same inputs restricted to sequences ``seqs`` (pure indexing): used
+    to check sampled sequences of a full-size workload against the oracle."""
+    spec = case.spec
+    seqs = [int(s) for s in seqs]
+    cu_q, cu_n, cu_p = spec.cu_q, spec.cu_new, case.cu_prefix
+    take = lambda arr, cu: (None if arr is None else
+                            np.concatenate([arr[cu[b]:cu[b + 1]] for b in seqs], axis=0))
+    sub = Spec(**{**spec.__dict__, "batch": len(seqs), "q_lens": spec.q_lens[seqs].copy(),
+                  "cache_lens": spec.cache_lens[seqs].copy(), "new_lens": spec.new_lens[seqs].copy(),
+                  "name": spec.name + "-subset"})
+    if spec.paged:
+        kc, vc, bt = case.k_cache, case.v_cache, case.block_table[seqs].copy()
+    else:
+        kc, vc, bt = case.k_cache[seqs].copy(), case.v_cache[seqs].copy(), None
+    return Case(spec=sub, q=take(case.q, cu_q), k_new=take(case.k_new, cu_n), v_new=take(case.v_new, cu_n),
+                k_cache=kc, v_cache=vc, block_table=bt, num_pages=case.num_pages, poison_page=case.poison_page,
+                prefix_k=take(case.prefix_k, cu_p), prefix_v=take(case.prefix_v, cu_p), k_scale=case.k_scale,
+                v_scale=case.v_scale, sentinel=case.sentinel)

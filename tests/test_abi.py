@@ -1,0 +1,209 @@
+"""Host-side tests of the C ABI (no GPU): the library loads and exports every
+symbol the header declares, host validation returns its status codes before
+anything is launched, and the plan's work list covers every query row and key
+exactly as the method requires."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    import paged_kv_variable_gb300 as m
+    from paged_kv_variable_gb300 import build as b
+    b.build()
+    m.lib()
+    return m
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(pkv):
+    names = _declared_symbols()
+    assert names, "no declarations found"
+    assert sorted(names) == sorted(pkv.EXPORTED)
+    for n in names:
+        assert hasattr(pkv.lib(), n), n
+    assert "sm_103a" in pkv.version()
+
+
+def _problem(pkv, **kw):
+    base = dict(batch=2, num_heads_q=4, num_heads_kv=2, head_dim=64, page_size=16, cache_capacity=64,
+                num_pages=8, cache_dtype="bf16", causal=True, softmax_scale=0.125)
+    base.update(kw)
+    return pkv.make_problem(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(num_heads_q=6, num_heads_kv=4), 1),
+    (dict(head_dim=96), 2),
+    (dict(page_size=8), 2),
+    (dict(page_size=512), 2),
+    (dict(cache_dtype="fp8", head_dim=64), 2),
+    (dict(num_heads_q=64, num_heads_kv=2), 2),
+    (dict(cache_capacity=0), 1),
+    (dict(cache_capacity=40), 1),   # not a multiple of the page size
+    (dict(softmax_scale=0.0), 1),
+    (dict(softmax_scale=float("nan")), 1),
+])
+def test_plan_rejects_bad_problems(pkv, kw, status):
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.plan(_problem(pkv, **kw), [1, 1], [3, 3], [1, 1], num_sms=4)
+    assert e.value.status == status
+    assert pkv.last_error()
+
+
+def test_plan_rejects_overflowing_lengths(pkv):
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.plan(_problem(pkv), [1, 1], [64, 3], [1, 1], num_sms=4)
+    assert e.value.status == 1 and "capacity" in pkv.last_error()
+    with pytest.raises(pkv.PkvError):
+        pkv.plan(_problem(pkv), [1, -1], [3, 3], [1, 1], num_sms=4)
+
+
+def _coverage(spec, items, num_sms):
+    """Every (seq, kv head, query token) is covered by exactly the tiles whose
+    key ranges tile [0, limit) of that row without overlap."""
+    G = spec.hq // spec.hkv
+    cov = {}
+    for it in items:
+        b, hk = it["seq"], it["kv_head"]
+        assert 0 <= it["cta"] < num_sms
+        assert it["kv_begin"] % 128 == 0 or it["kv_begin"] == it["kv_end"]
+        for t in range(it["n_q"]):
+            i = it["q_index0"] + t
+            cov.setdefault((b, hk, i), []).append((it["kv_begin"], it["kv_end"], it["partial_slot"]))
+        rows = it["n_q"] * G
+        if it["kind"] == 0:
+            assert rows <= 16
+    for b in range(spec.batch):
+        lq, lk = int(spec.q_lens[b]), int(spec.kv_lens[b])
+        for hk in range(spec.hkv):
+            for i in range(lq):
+                ranges = sorted(cov.pop((b, hk, i)))
+                # ranges are disjoint, start at 0 and reach at least the row's horizon
+                horizon = min(lk, i + lk - lq + 1) if spec.causal else lk
+                pos = 0
+                for a, z, _ in ranges:
+                    assert a == pos
+                    pos = z
+                assert pos >= max(0, horizon) and pos <= lk
+                if len(ranges) > 1:
+                    assert all(s >= 0 for _, _, s in ranges)
+                else:
+                    assert ranges[0][2] == -1
+    assert not cov
+
+
+@pytest.mark.parametrize("which", ["cfg1", "cfg2", "cfg3", "cfg4", "rand"])
+def test_plan_covers_every_row(pkv, which):
+    if which == "cfg1":
+        case = synth.config1()
+    elif which == "cfg2":
+        case = synth.config2(draw_values=False)
+    elif which == "cfg3":
+        case = synth.config3(draw_values=False)
+    elif which == "cfg4":
+        case = synth.config4(draw_values=False)
+    else:
+        case = synth.random_case(7, batch=5, hq=8, hkv=2, d=128, page_size=16, max_cache=900, max_new=70)
+    spec = case.spec
+    prob = pkv.make_problem(batch=spec.batch, num_heads_q=spec.hq, num_heads_kv=spec.hkv, head_dim=spec.d,
+                            page_size=spec.page_size, cache_capacity=spec.capacity,
+                            num_pages=max(1, case.num_pages if spec.paged else spec.batch),
+                            cache_dtype=spec.cache_dtype, causal=spec.causal, softmax_scale=spec.softmax_scale)
+    for sms in (1, 13, 152):
+        pl = pkv.plan(prob, spec.q_lens, spec.cache_lens, spec.new_lens, num_sms=sms)
+        items = pl.items()
+        st = pl.stats()
+        assert st["num_items"] == len(items)
+        assert st["total_q"] == spec.total_q and st["total_new"] == spec.total_new
+        _coverage(spec, items, sms)
+        if sms == 152 and which in ("cfg2", "cfg4"):
+            assert st["num_ctas"] == 152
+            assert st["max_cta_cost"] <= 1.15 * st["mean_cta_cost"]
+
+
+def test_plan_accepts_zero_lengths(pkv):
+    # zero kv length (a failure case reported for another scheduler) and zero query length
+    prob = _problem(pkv, batch=3)
+    pl = pkv.plan(prob, [2, 0, 1], [0, 5, 0], [0, 0, 1], num_sms=4)
+    items = pl.items()
+    assert sum(1 for it in items if it["seq"] == 1) == 0
+    zero = [it for it in items if it["seq"] == 0]
+    assert zero and all(it["kv_begin"] == it["kv_end"] == 0 for it in zero)
+
+
+def test_empty_batch(pkv):
+    pl = pkv.plan(_problem(pkv, batch=0), np.zeros(0, np.int32), np.zeros(0, np.int32), None, num_sms=4)
+    assert pl.stats()["num_items"] == 0
+
+
+class _FakeTensor:
+    def __init__(self, ptr, shape, strides=None, esize=2):
+        self._ptr, self.shape, self._esize = ptr, shape, esize
+        if strides is None:
+            strides, acc = [], 1
+            for s in reversed(shape):
+                strides.insert(0, acc)
+                acc *= s
+        self._strides = strides
+
+    def data_ptr(self):
+        return self._ptr
+
+    def stride(self, i):
+        return self._strides[i]
+
+    def numel(self):
+        return int(np.prod(self.shape))
+
+    def element_size(self):
+        return self._esize
+
+
+def test_fwd_validation_before_any_launch(pkv):
+    prob = _problem(pkv)
+    pl = pkv.plan(prob, [3, 1], [37, 5], [3, 1], num_sms=4)
+    ws = _FakeTensor(4096 * 256, (pl.workspace_bytes,), esize=1)
+    q = _FakeTensor(1 << 20, (4, 4, 64))
+    kc = _FakeTensor(1 << 24, (8, 16, 2, 64))
+    i32 = _FakeTensor(1 << 16, (3,), esize=4)
+    bt = _FakeTensor(1 << 17, (2, 4), esize=4)
+    good = dict(q=q, out=q, cu_seqlens_q=i32, max_seqlen_q=3, k_cache=kc, v_cache=kc, cache_seqlens=i32,
+                k_new=q, v_new=q, cu_seqlens_knew=i32, block_table=bt)
+
+    def call(**over):
+        kw = dict(good)
+        kw.update(over)
+        with pytest.raises(pkv.PkvError) as e:
+            pkv.attn_varlen_kvcache_fwd(prob, pkv.make_args(**kw), pl, ws, stream=0)
+        return e.value.status
+
+    assert call(block_table=None) == 1
+    assert call(k_cache=_FakeTensor((1 << 24) + 2, (8, 16, 2, 64))) == 1          # misaligned
+    assert call(k_new=None, v_new=None, cu_seqlens_knew=None) == 1                  # plan expects new tokens
+    assert call(q=_FakeTensor(1 << 20, (4, 4, 64), strides=[256, 66, 1])) == 1      # stride not 16 B multiple
+    small = _FakeTensor(4096 * 256, (pl.workspace_bytes - 256,), esize=1)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.attn_varlen_kvcache_fwd(prob, pkv.make_args(**good), pl, small, stream=0)
+    assert e.value.status == 3
+    other = _problem(pkv, causal=False)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.attn_varlen_kvcache_fwd(other, pkv.make_args(**good), pl, ws, stream=0)
+    assert e.value.status == 1
+    fp8 = _problem(pkv, cache_dtype="fp8", head_dim=128)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.kv_append(fp8, pkv.make_args(**good), 4, None, stream=0)   # no scales
+    assert e.value.status == 1

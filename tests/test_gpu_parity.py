@@ -1,0 +1,280 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Bar: cache appends bit-exact; outputs within max-abs 2e-2 / mean-abs 2e-3
+(bf16 cache) or max-abs 6e-2 (fp8 cache); LSE within 2e-3.  Small cases are
+compared element by element; the full-size workloads on sampled query rows
+(every head of the row) and on the whole post-append cache.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests import harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_variable_gb300 import build
+    build.build()
+
+
+def tol_for(case):
+    return H.FP8_TOL if case.spec.cache_dtype == "fp8" else H.BF16_TOL
+
+
+def run_full(case, num_sms=None, check_cache=True):
+    g = H.GpuCase(case, num_sms=num_sms)
+    g.write_prefix()
+    g.run()
+    assert g.status() == 0, g.pkv.last_error()
+    ref = oracle.forward(case)
+    H.compare_out(g.out, ref["out"], tol_for(case))
+    H.compare_lse(g.lse, ref["lse"])
+    if check_cache:
+        assert np.array_equal(H.to_numpy_bits(g.k_cache), ref["k_cache"]), "k cache differs"
+        assert np.array_equal(H.to_numpy_bits(g.v_cache), ref["v_cache"]), "v cache differs"
+    return g, ref
+
+
+@pytest.mark.parametrize("sentinel", ["finite", "nan"])
+def test_config1_tiny_paged(sentinel):
+    run_full(synth.config1(sentinel=sentinel))
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_bf16(seed):
+    run_full(H.gpu_random_case(seed, sentinel="nan" if seed % 3 == 0 else "finite"))
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_fp8(seed):
+    run_full(H.gpu_random_case(100 + seed, cache_dtype="fp8", sentinel="nan" if seed % 2 else "finite"))
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_cache_only_and_ragged_queries(seed):
+    # no new K/V (cache-only attention) and query lengths unrelated to new lengths
+    run_full(H.gpu_random_case(200 + seed, with_new=(seed % 2 == 0), q_equals_new=False))
+
+
+def test_zero_lengths_and_empty_rows():
+    spec = synth.Spec(batch=4, hq=8, hkv=2, d=128, page_size=16, causal=True, softmax_scale=0.0883883461356163,
+                      cache_dtype="bf16", q_lens=np.array([3, 0, 5, 2], np.int32),
+                      cache_lens=np.array([0, 7, 0, 1], np.int32), new_lens=np.array([0, 2, 5, 0], np.int32),
+                      capacity=32, name="zeros")
+    case = synth.make_case(spec, np.random.default_rng(5))
+    g, ref = run_full(case)
+    # sequence 0 sees no key at all: zeros and -inf
+    assert np.all(ref["out"][:3] == 0)
+
+
+@pytest.mark.parametrize("g_", [1, 2, 4, 8, 16])
+def test_group_sizes_decode_and_prefill(g_):
+    for seed, lq in ((300 + g_, 1), (310 + g_, 40)):
+        rng = np.random.default_rng(seed)
+        spec = synth.uniform_spec(f"g{g_}", 3, lq, int(rng.integers(100, 400)), hq=2 * g_, hkv=2, d=128)
+        run_full(synth.make_case(spec, rng))
+
+
+def test_long_decode_is_split_and_matches():
+    rng = np.random.default_rng(11)
+    spec = synth.uniform_spec("long", 2, 1, 9000, hq=8, hkv=2, d=128, page_size=64)
+    case = synth.make_case(spec, rng)
+    g, _ = run_full(case, num_sms=8)
+    assert g.plan.stats()["num_split_units"] > 0
+
+
+def test_split_counts_agree():
+    case = synth.random_case(21, batch=4, hq=8, hkv=2, d=128, page_size=32, causal=True, max_cache=3000,
+                             max_new=1, allow_zero=False)
+    outs = []
+    for sms in (1, 5, 37, 152):
+        g, _ = run_full(case, num_sms=sms)
+        outs.append(H.bf16_to_f64(g.out))
+    for o in outs[1:]:
+        assert np.max(np.abs(o - outs[0])) <= 1e-2
+
+
+def test_deterministic_and_poison_independent():
+    a = H.gpu_random_case(31, page_size=16, sentinel="finite")
+    b = H.gpu_random_case(31, page_size=16, sentinel="nan")
+    ga = H.GpuCase(a)
+    ga.run()
+    ga2 = H.GpuCase(a)
+    ga2.run()
+    gb = H.GpuCase(b)
+    gb.run()
+    first = H.to_numpy_bits(ga.out)
+    assert np.array_equal(first, H.to_numpy_bits(ga2.out))
+    assert np.array_equal(first, H.to_numpy_bits(gb.out))
+
+
+def test_paged_equals_contiguous_and_relabel():
+    case = synth.random_case(41, batch=3, hq=8, hkv=2, d=128, page_size=16, causal=True, max_cache=500,
+                             max_new=40, allow_zero=False)
+    ga = H.GpuCase(case)
+    ga.run()
+    gc = H.GpuCase(synth.to_contiguous(case))
+    gc.run()
+    gr = H.GpuCase(synth.relabel_pages(case, np.random.default_rng(3)))
+    gr.run()
+    base = H.to_numpy_bits(ga.out)
+    assert np.array_equal(base, H.to_numpy_bits(gc.out))
+    assert np.array_equal(base, H.to_numpy_bits(gr.out))
+
+
+def test_fused_append_equals_append_then_attend():
+    import torch
+    case = H.gpu_random_case(51, page_size=32)
+    fused = H.GpuCase(case)
+    fused.run()
+    sep = H.GpuCase(case)
+    spec = case.spec
+    sep.pkv.kv_append(sep.problem, sep.args(), spec.total_new, sep.workspace)
+    # the attention alone over the advanced cache lengths
+    adv = synth.Spec(**{**spec.__dict__, "cache_lens": spec.kv_lens, "new_lens": np.zeros_like(spec.new_lens)})
+    import paged_kv_variable_gb300 as pkv
+    pl = pkv.plan(sep.problem, adv.q_lens, adv.cache_lens, None)
+    ws = pkv.workspace_tensor(pl.workspace_bytes)
+    pl.upload(ws)
+    a = pkv.make_args(q=sep.q, out=sep.out, lse=sep.lse, cu_seqlens_q=sep.cu_q, max_seqlen_q=int(spec.q_lens.max()),
+                      k_cache=sep.k_cache, v_cache=sep.v_cache, cache_seqlens=H.i32(adv.cache_lens),
+                      block_table=sep.block_table)
+    pkv.attn_varlen_kvcache_fwd(sep.problem, a, pl, ws)
+    assert pkv.get_status(ws) == 0
+    assert np.array_equal(H.to_numpy_bits(fused.out), H.to_numpy_bits(sep.out))
+    assert torch.equal(fused.k_cache, sep.k_cache)
+
+
+def test_device_status_on_bad_block_table_entry():
+    # an out-of-range page number is never dereferenced: the append skips the
+    # row, the gather reads zeros, and the status word reports it
+    case = synth.config1()
+    g = H.GpuCase(case)
+    bt = g.block_table.clone()
+    bt[0, 1] = 10_000
+    g.block_table = bt
+    g.run()
+    assert g.status() == 6
+
+
+def test_device_status_on_plan_mismatch():
+    case = synth.config1()
+    g = H.GpuCase(case)
+    g.cache_lens[1] += 1
+    g.run()
+    assert g.status() == 7
+
+
+# ------------------------------------------------------------------ full-size workloads
+def _sample_rows(spec, n, seed):
+    rng = np.random.default_rng(seed)
+    rows = []
+    seqs = [b for b in range(spec.batch) if spec.q_lens[b] > 0]
+    for _ in range(n):
+        b = int(rng.choice(seqs))
+        i = int(rng.integers(0, int(spec.q_lens[b])))
+        rows.append((b, i))
+    # always include the first and last query of the longest sequence
+    bl = int(np.argmax(spec.q_lens))
+    rows += [(bl, 0), (bl, int(spec.q_lens[bl]) - 1)]
+    return rows
+
+
+def check_sampled(case, g, n_rows=48, seed=0, full_cache=True):
+    """bf16 caches: the whole post-append cache bit-exact, then sampled rows
+    from the oracle's own post-append cache.  fp8 (full_cache=False): the
+    oracle writes and attends only the sampled sequences."""
+    spec = case.spec
+    rows = _sample_rows(spec, n_rows, seed)
+    tol = tol_for(case)
+    out = g.out.float().cpu().double().numpy()
+    lse = g.lse.cpu().double().numpy()
+    cu = spec.cu_q
+    if full_cache:
+        kc0, vc0 = oracle.prepare_prefix(case)
+        kc, vc = oracle.append_kv(spec, kc0, vc0, case.block_table, case.k_new, case.v_new, case.k_scale,
+                                  case.v_scale)
+        assert np.array_equal(H.to_numpy_bits(g.k_cache), kc), "k cache differs"
+        assert np.array_equal(H.to_numpy_bits(g.v_cache), vc), "v cache differs"
+        o, l = oracle.forward_rows(case, kc, vc, rows)
+        idx = [cu[b] + i for b, i in rows]
+        err = np.abs(out[idx] - o)
+        assert err.max() <= tol["max_abs"], float(err.max())
+        assert err.mean() <= tol["mean_abs"], float(err.mean())
+        assert np.max(np.abs(lse[:, idx] - l)) <= H.LSE_TOL
+        return
+    by_seq = {}
+    for b, i in rows:
+        by_seq.setdefault(b, []).append(i)
+    for b, idx in by_seq.items():
+        sub = synth.subset_case(case, [b])
+        kc0, vc0 = oracle.prepare_prefix(sub)
+        kc, vc = oracle.append_kv(sub.spec, kc0, vc0, sub.block_table, sub.k_new, sub.v_new, sub.k_scale,
+                                  sub.v_scale)
+        o, l = oracle.forward_rows(sub, kc, vc, [(0, i) for i in idx])
+        got = out[[cu[b] + i for i in idx]]
+        err = np.abs(got - o)
+        assert err.max() <= tol["max_abs"], (b, float(err.max()))
+        assert err.mean() <= tol["mean_abs"], (b, float(err.mean()))
+        gl = lse[:, [cu[b] + i for i in idx]]
+        assert np.max(np.abs(gl - l)) <= H.LSE_TOL
+
+
+@pytest.mark.slow
+def test_config2_decode_full():
+    case = synth.config2()
+    g = H.GpuCase(case)
+    g.run()
+    assert g.status() == 0
+    check_sampled(case, g, n_rows=64)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("causal", [True, False])
+def test_config3_prefill_full(causal):
+    case = synth.config3(causal=causal)
+    g = H.GpuCase(case)
+    g.run()
+    assert g.status() == 0
+    check_sampled(case, g, n_rows=48)
+
+
+@pytest.mark.slow
+def test_config4_mixed_full():
+    case = synth.config4()
+    g = H.GpuCase(case)
+    g.run()
+    assert g.status() == 0
+    check_sampled(case, g, n_rows=64)
+
+
+@pytest.mark.slow
+def test_config5_fp8_prefill_then_decode():
+    pre, dec = synth.config5()
+    g = H.GpuCase(pre)
+    g.run()
+    assert g.status() == 0
+    check_sampled(pre, g, n_rows=24, full_cache=False)
+    # fp8 append bit-exact on sampled sequences
+    spec = pre.spec
+    for b in (0, 17, 63):
+        sub = synth.subset_case(pre, [b])
+        kc, vc = oracle.append_kv(sub.spec, sub.k_cache, sub.v_cache, sub.block_table, sub.k_new, sub.v_new,
+                                  sub.k_scale, sub.v_scale)
+        pages = pre.block_table[b]
+        assert np.array_equal(H.to_numpy_bits(g.k_cache[pages.tolist()]), kc[pages])
+        assert np.array_equal(H.to_numpy_bits(g.v_cache[pages.tolist()]), vc[pages])
+    # decode step on the cache the prefill left (token 2049)
+    gd = H.GpuCase(dec)
+    gd.k_cache.copy_(g.k_cache)
+    gd.v_cache.copy_(g.v_cache)
+    gd.run()
+    assert gd.status() == 0
+    check_sampled(dec, gd, n_rows=32, full_cache=False)
