@@ -1,0 +1,396 @@
+"""Benchmark of the attention-over-KV-cache hot path on GB300.
+
+Headline workload (one "step"): the decode batch -- 64 sequences, 1 query and
+1 appended token each, Hq=32, Hkv=8, D=128, bf16 paged cache (page 16,
+seeded page permutation), cache lengths U[512, 4096].  One step = one
+pkv_attn_varlen_kvcache_fwd call: KV append + persistent attention kernel +
+split-KV combine.  value = algorithmic bytes of the step / device time, GB/s.
+
+The other workloads (prefill with a cached prefix, the mixed batch, the fp8
+cache) are measured the same way and reported under "workloads".
+
+Timing: W warm-up steps, then K steps each timed with CUDA events on the
+launching stream; L2 is flushed (256 MB write) before every timed step,
+outside the timed events.  --impl reference times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+# the oracle leg runs single-threaded BLAS so that "cores" is exact
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "decode KV GB/s & prefill attn TFLOP/s on 1 GB300, % of roofline"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "src": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
+
+
+# --------------------------------------------------------------------------- algorithmic work
+def step_work(spec, with_new=True):
+    """Bytes and flops one call must move / compute (valid tokens, unmasked pairs)."""
+    es = 2 if spec.cache_dtype == "bf16" else 1
+    lk = spec.kv_lens.astype(np.int64)
+    lq = spec.q_lens.astype(np.int64)
+    kv = int(lk.sum()) * spec.hkv * spec.d * 2 * es
+    qo = int(lq.sum()) * spec.hq * spec.d * 2 * 2
+    bt = int(sum((int(n) + spec.page_size - 1) // spec.page_size for n in lk)) * 4 if spec.page_size else 0
+    new = int(spec.new_lens.sum()) * spec.hkv * spec.d * 2 * (2 + es) if with_new else 0
+    pairs = 0
+    for a, k in zip(lq, lk):
+        a, k = int(a), int(k)
+        if spec.causal:
+            i = np.arange(a)
+            pairs += int(np.clip(i + 1 + k - a, 0, k).sum())
+        else:
+            pairs += a * k
+    return {"attn_bytes": kv + qo + bt, "append_bytes": new, "bytes": kv + qo + bt + new,
+            "flops": 4 * spec.d * spec.hq * pairs}
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self._stop = threading.Event()
+        self._t = None
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                r = subprocess.run(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                    "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=5)
+                if r.returncode == 0 and r.stdout.strip():
+                    self.samples.append([x.strip() for x in r.stdout.strip().split(",")])
+            except Exception:
+                return
+            self._stop.wait(0.2)
+
+    def __enter__(self):
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._t:
+            self._t.join(timeout=10)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        mx = [float(s[2]) for s in self.samples if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for s in self.samples for k in range(4) if len(s) > 5 + k and
+                          s[5 + k].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+# --------------------------------------------------------------------------- GPU arm
+class Workload:
+    """A case resident on the device, runnable as one library call per step."""
+
+    def __init__(self, name, case, device):
+        import torch
+        sys.path.insert(0, os.path.join(ROOT, "tests"))
+        from tests import harness as H
+        self.name, self.case = name, case
+        self.g = H.GpuCase(case, device=device)
+        self.g.write_prefix()
+        self.work = step_work(case.spec, with_new=case.k_new is not None)
+        self.torch = torch
+        self.nsplit = self.g.plan.stats()["num_split_units"]
+
+    def launches_per_step(self):
+        return (1 if self.case.k_new is not None else 0) + 1 + (1 if self.nsplit else 0)
+
+    def step(self):
+        self.g.run()
+
+
+def time_workload(wl, steps, warmup, flush, stream):
+    import torch
+    import paged_kv_variable_gb300 as pkv
+    for _ in range(warmup):
+        wl.step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for s0, s1, k0, k1 in ev:
+        flush.zero_()
+        s0.record(stream)
+        pkv.set_profile_events(k0, k1)
+        wl.step()
+        s1.record(stream)
+    pkv.set_profile_events(None, None)
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b, _, _ in ev]
+    kern_ms = [a.elapsed_time(b) for _, _, a, b in ev]
+    assert wl.g.status() == 0, wl.g.pkv.last_error()
+    return step_ms, kern_ms
+
+
+def e2e_decode(case, steps, warmup, device):
+    """The same step through the public API from HOST buffers: plan on the host,
+    pinned-host -> device copies of the step's inputs, the call, and the
+    device -> host copy of the output, all inside the timed region."""
+    import torch
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from tests import harness as H
+    import paged_kv_variable_gb300 as pkv
+    g = H.GpuCase(case, device=device)
+    spec = case.spec
+    host = {
+        "q": torch.from_numpy(case.q.view(np.int16)).view(torch.bfloat16).pin_memory(),
+        "k_new": torch.from_numpy(case.k_new.view(np.int16)).view(torch.bfloat16).pin_memory(),
+        "v_new": torch.from_numpy(case.v_new.view(np.int16)).view(torch.bfloat16).pin_memory(),
+        "cu_q": torch.from_numpy(spec.cu_q).pin_memory(),
+        "cu_new": torch.from_numpy(spec.cu_new).pin_memory(),
+        "lens": torch.from_numpy(spec.cache_lens).pin_memory(),
+    }
+    out_h = torch.empty(g.out.shape, dtype=torch.bfloat16).pin_memory()
+    dev = {"q": g.q, "k_new": g.k_new, "v_new": g.v_new, "cu_q": g.cu_q, "cu_new": g.cu_new, "lens": g.cache_lens}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    nsms = torch.cuda.get_device_properties(device).multi_processor_count
+    stream = torch.cuda.current_stream()
+
+    def one():
+        pl = pkv.plan(g.problem, spec.q_lens, spec.cache_lens, spec.new_lens, nsms)
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        pl.upload(g.workspace)
+        pkv.attn_varlen_kvcache_fwd(g.problem, g.args(), pl, g.workspace)
+        out_h.copy_(g.out, non_blocking=True)
+        stream.synchronize()
+        return pl
+
+    for _ in range(warmup):
+        one()
+    ts = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        pl = one()
+        ts.append(time.perf_counter() - t0)
+        del pl
+    return statistics.median(ts) * 1e3, h2d + int(g.plan.stats()["upload_bytes"]), d2h
+
+
+def cpu_oracle_leg(case, budget_s=12.0):
+    """The oracle as it stands on a bounded sample of the workload."""
+    import oracle
+    spec = case.spec
+    work = step_work(spec)
+    t0 = time.perf_counter()
+    n = 0
+    seqs_done = 0
+    # whole steps if they fit the budget, else a prefix of the sequences
+    while time.perf_counter() - t0 < budget_s:
+        sub = synth.subset_case(case, [seqs_done % spec.batch])
+        oracle.forward(sub)
+        seqs_done += 1
+        n += 1
+    dt = time.perf_counter() - t0
+    frac = seqs_done / spec.batch
+    value = work["bytes"] * frac / dt / 1e9
+    return {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{seqs_done} sequences of the decode batch ({frac:.2f} steps) in {dt:.1f} s, fp64 NumPy, 1 thread"}
+
+
+def gpu_arm(args):
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    peaks = _peaks()
+
+    decode_case = synth.config2()
+    cpu_base = cpu_oracle_leg(decode_case, 12.0 if args.cpu_leg else 1.0) if rank == 0 else None
+
+    from paged_kv_variable_gb300 import build
+    build.build()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    if args.workload == "decode-small":
+        # 16 sequences of the decode batch (about 150 MB of KV, above L2): profiler captures
+        main = Workload("decode-small", synth.subset_case(decode_case, list(range(16))), device)
+    else:
+        main = Workload("decode", decode_case, device)
+    with ClockSampler(local) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter()
+        step_ms, kern_ms = time_workload(main, args.steps, args.warmup, flush, stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        t_wall = time.perf_counter() - t_wall
+    clocks = clk.summary()
+    t_step = sum(step_ms) / len(step_ms)
+    if world > 1:
+        t = torch.tensor([t_step], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_step = float(t.item())
+    t_kern = sum(kern_ms) / len(kern_ms)
+    value = main.work["bytes"] * world / (t_step * 1e-3) / 1e9
+    achieved = main.work["attn_bytes"] / (t_kern * 1e-3) / 1e9
+
+    e2e_ms, h2d, d2h = e2e_decode(main.case, max(3, args.steps // 2), 3, device)
+    e2e_val = main.work["bytes"] * world / (e2e_ms * 1e-3) / 1e9
+
+    extra = {}
+    if args.secondary and rank == 0:
+        secondary = [("prefill_cached_prefix_causal", lambda: synth.config3(True), "tensor"),
+                     ("prefill_cached_prefix_noncausal", lambda: synth.config3(False), "tensor"),
+                     ("mixed_prefill_decode", synth.config4, "mixed"),
+                     ("fp8_prefill", lambda: synth.config5()[0], "tensor"),
+                     ("fp8_decode", lambda: synth.config5()[1], "hbm")]
+        for name, mk, bound in secondary:
+            case = mk()
+            wl = Workload(name, case, device)
+            if name == "fp8_decode":
+                pre = Workload("fp8_prefill_for_decode", synth.config5()[0], device)
+                pre.step()
+                wl.g.k_cache.copy_(pre.g.k_cache)
+                wl.g.v_cache.copy_(pre.g.v_cache)
+                del pre
+            sm, km = time_workload(wl, max(3, args.steps // 4), 3, flush, stream)
+            ts, tk = sum(sm) / len(sm), sum(km) / len(km)
+            ent = {"ms_per_call": round(ts, 4), "attn_kernel_ms": round(tk, 4),
+                   "tflops": round(wl.work["flops"] / (ts * 1e-3) / 1e12, 1),
+                   "gbs": round(wl.work["bytes"] / (ts * 1e-3) / 1e9, 1)}
+            if bound == "tensor":
+                ent["attn_tflops"] = round(wl.work["flops"] / (tk * 1e-3) / 1e12, 1)
+                ent["frac_of_bf16_peak"] = round(ent["attn_tflops"] / peaks["bf16_tflops"], 3)
+            elif bound == "hbm":
+                ent["attn_gbs"] = round(wl.work["attn_bytes"] / (tk * 1e-3) / 1e9, 1)
+                ent["frac_of_hbm_peak"] = round(ent["attn_gbs"] / peaks["hbm_gbs"], 3)
+            else:
+                t_dec = wl.work["attn_bytes"] / (peaks["hbm_gbs"] * 1e9)
+                t_pre = wl.work["flops"] / (peaks["bf16_tflops"] * 1e12)
+                ent["bound_ms_serial"] = round((t_dec + t_pre) * 1e3, 4)
+                ent["bound_ms_overlap"] = round(max(t_dec, t_pre) * 1e3, 4)
+            extra[name] = ent
+            del wl
+            torch.cuda.empty_cache()
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(t_step, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "decode: B=64, 1 query + 1 appended token each, Hq=32, Hkv=8, D=128, bf16 "
+                                   "paged cache page 16 (seeded permutation), cache lens U[512,4096]",
+                       "step": "kv append + persistent attention + split-KV combine (one library call)",
+                       "l2": "flushed before every timed step (256 MB write, outside the timed events)",
+                       "parallelism": f"replicas x{world}", "split_units": main.nsplit},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                         "kernel": "attn_kernel (persistent attention)", "peak_src": peaks["src"],
+                         "attn_kernel_ms": round(t_kern, 5)},
+            "cpu_baseline": cpu_base,
+            "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": main.launches_per_step() * args.steps,
+            "clocks": clocks,
+            "wall_s_timed_region": round(t_wall, 4),
+            "workloads": extra,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def reference_arm(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    case = synth.config2()
+    work = step_work(case.spec)
+    import oracle
+    per = []
+    for i in range(args.warmup + args.steps):
+        # each step: the oracle on a bounded sample (4 sequences) of the decode batch
+        seqs = [(4 * i + k) % case.spec.batch for k in range(4)]
+        sub = synth.subset_case(case, seqs)
+        t0 = time.perf_counter()
+        oracle.forward(sub)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            per.append((dt, step_work(sub.spec)["bytes"]))
+    tot_t = sum(t for t, _ in per)
+    tot_b = sum(b for _, b in per)
+    value = tot_b / tot_t / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_t / len(per) * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "decode: B=64, 1 query + 1 appended token each, Hq=32, Hkv=8, D=128, bf16 "
+                                   "paged cache page 16, cache lens U[512,4096]",
+                       "sample": "4 sequences of the batch per step"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "4 sequences of the decode batch per step, fp64 NumPy, 1 thread"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "work_bytes_full_step": work["bytes"]}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-secondary", dest="secondary", action="store_false")
+    ap.add_argument("--workload", default="decode", choices=["decode", "decode-small"])
+    ap.add_argument("--no-cpu-leg", dest="cpu_leg", action="store_false")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

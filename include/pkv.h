@@ -124,6 +124,8 @@ typedef struct {
   int32_t max_items_per_cta;
   double max_cta_cost;       /* LPT makespan, model units                   */
   double mean_cta_cost;
+  int64_t upload_bytes;      /* bytes pkv_plan_upload copies to the device  */
+  int64_t workspace_bytes;   /* device workspace the plan needs             */
 } pkv_plan_stats;
 
 /*
@@ -211,6 +213,13 @@ void pkv_plan_destroy(pkv_plan_t plan);
 
 /* Thread-local message describing the last failing call ("" if none). */
 const char* pkv_last_error(void);
+
+/* Timing hook for benchmarks: when start/stop are non-NULL (cudaEvent_t
+ * passed as void*), every later pkv_attn_varlen_kvcache_fwd on this host
+ * thread records `start` immediately before and `stop` immediately after the
+ * persistent attention kernel, on the call's stream.  NULL, NULL turns it off.
+ * The events stay owned by the caller. */
+pkv_status pkv_set_profile_events(void* start_event, void* stop_event);
 
 /* Library version string. */
 const char* pkv_version(void);

@@ -25,7 +25,7 @@ STATUS_NAMES = {
 
 # every symbol the header declares
 EXPORTED = ["pkv_plan", "pkv_plan_upload", "pkv_plan_get_stats", "pkv_plan_get_items", "pkv_attn_varlen_kvcache_fwd", "pkv_kv_append",
-            "pkv_get_status", "pkv_plan_destroy", "pkv_last_error", "pkv_version"]
+            "pkv_get_status", "pkv_plan_destroy", "pkv_last_error", "pkv_version", "pkv_set_profile_events"]
 
 
 class PkvError(RuntimeError):
@@ -63,7 +63,8 @@ class PlanStats(ctypes.Structure):
                 ("num_prefill_items", ctypes.c_int32), ("num_split_units", ctypes.c_int32),
                 ("num_ctas", ctypes.c_int32), ("total_q", ctypes.c_int32), ("total_new", ctypes.c_int32),
                 ("max_items_per_cta", ctypes.c_int32), ("max_cta_cost", ctypes.c_double),
-                ("mean_cta_cost", ctypes.c_double)]
+                ("mean_cta_cost", ctypes.c_double), ("upload_bytes", ctypes.c_int64),
+                ("workspace_bytes", ctypes.c_int64)]
 
 
 _lib = None
@@ -84,12 +85,13 @@ def lib() -> ctypes.CDLL:
         L.pkv_attn_varlen_kvcache_fwd.argtypes = [ctypes.POINTER(Problem), ctypes.POINTER(FwdArgs), vp, vp, sz, vp]
         L.pkv_kv_append.argtypes = [ctypes.POINTER(Problem), ctypes.POINTER(FwdArgs), i32, vp, vp]
         L.pkv_get_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
+        L.pkv_set_profile_events.argtypes = [vp, vp]
         L.pkv_plan_destroy.argtypes = [vp]
         L.pkv_plan_destroy.restype = None
         L.pkv_last_error.restype = ctypes.c_char_p
         L.pkv_version.restype = ctypes.c_char_p
         for name in ("pkv_plan", "pkv_plan_upload", "pkv_plan_get_stats", "pkv_plan_get_items", "pkv_attn_varlen_kvcache_fwd",
-                     "pkv_kv_append", "pkv_get_status"):
+                     "pkv_kv_append", "pkv_get_status", "pkv_set_profile_events"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -219,6 +221,19 @@ def get_status(workspace, stream=None) -> int:
     st = ctypes.c_int32()
     _check(lib().pkv_get_status(workspace.data_ptr(), _stream_handle(stream), ctypes.byref(st)))
     return int(st.value)
+
+
+def set_profile_events(start=None, stop=None) -> None:
+    """Record torch.cuda.Event objects around the attention kernel of later calls.
+
+    torch creates the CUDA event lazily, on its first record(); record both once
+    here so that the handles passed to the library exist."""
+    if start is not None:
+        start.record()
+        stop.record()
+        assert start.cuda_event and stop.cuda_event
+    _check(lib().pkv_set_profile_events(None if start is None else start.cuda_event,
+                                        None if stop is None else stop.cuda_event))
 
 
 def workspace_tensor(nbytes: int, device="cuda"):

@@ -13,6 +13,8 @@ namespace pkv {
 
 namespace {
 thread_local char g_err[512] = "";
+thread_local cudaEvent_t g_ev_start = nullptr;
+thread_local cudaEvent_t g_ev_stop = nullptr;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -70,6 +72,23 @@ pkv_status make_cache_map(CUtensorMap* map, const pkv_problem& pr, const pkv_fwd
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return PKV_OK;
+}
+
+// 3-D map over q (D, Hq, total_q): a box of G heads x 128/G tokens is the
+// 128-row Q tile of one kv head's prefill item (row = token * G + g).
+pkv_status make_q_map(CUtensorMap* map, const pkv_problem& pr, const pkv_fwd_args& a, int total_q) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const int g = pr.num_heads_q / pr.num_heads_kv;
+  cuuint64_t dims[3] = {(cuuint64_t)pr.head_dim, (cuuint64_t)pr.num_heads_q, (cuuint64_t)(total_q > 0 ? total_q : 1)};
+  cuuint64_t strides[2] = {(cuuint64_t)a.q_stride_head * 2, (cuuint64_t)a.q_stride_tok * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)g, (cuuint32_t)(kPrefillRowsTc / g)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled (q) failed (%d)", (int)r);
   return PKV_OK;
 }
 
@@ -220,11 +239,16 @@ extern "C" pkv_status pkv_attn_varlen_kvcache_fwd(const pkv_problem* problem, co
   }
   if (plan->num_items == 0) return PKV_OK;
 
-  CUtensorMap tk, tv;
+  CUtensorMap tk, tv, tq;
   st = make_cache_map(&tk, pr, *args, args->k_cache);
   if (st != PKV_OK) return st;
   st = make_cache_map(&tv, pr, *args, args->v_cache);
   if (st != PKV_OK) return st;
+  memset(&tq, 0, sizeof(tq));
+  if (pr.cache_dtype == PKV_BF16 && plan->num_prefill_items > 0) {
+    st = make_q_map(&tq, pr, *args, plan->total_q);
+    if (st != PKV_OK) return st;
+  }
 
   AttnParams p{};
   p.q = static_cast<const __nv_bfloat16*>(args->q);
@@ -252,8 +276,11 @@ extern "C" pkv_status pkv_attn_varlen_kvcache_fwd(const pkv_problem* problem, co
   p.cache_seqlens = args->cache_seqlens;
   p.plan_lc = reinterpret_cast<const int32_t*>(ws + plan->layout.plan_lc);
   p.batch = pr.batch;
-  cudaError_t e = launch_attention(p, tk, tv, plan->num_ctas, pr.head_dim, pr.cache_dtype == PKV_FP8_E4M3, s);
+  cudaError_t e;
+  if (g_ev_start && (e = cudaEventRecord(g_ev_start, s)) != cudaSuccess) return cuda_fail(e, "profile event");
+  e = launch_attention(p, tk, tv, tq, plan->num_ctas, pr.head_dim, pr.cache_dtype == PKV_FP8_E4M3, s);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  if (g_ev_stop && (e = cudaEventRecord(g_ev_stop, s)) != cudaSuccess) return cuda_fail(e, "profile event");
 
   if (plan->num_combine > 0) {
     CombineParams cp{};
@@ -269,6 +296,14 @@ extern "C" pkv_status pkv_attn_varlen_kvcache_fwd(const pkv_problem* problem, co
     e = launch_combine(cp, plan->num_combine, pr.head_dim, s);
     if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   }
+  return PKV_OK;
+}
+
+extern "C" pkv_status pkv_set_profile_events(void* start_event, void* stop_event) {
+  if ((start_event == nullptr) != (stop_event == nullptr))
+    return fail(PKV_ERR_INVALID_ARG, "give both events or neither");
+  g_ev_start = static_cast<cudaEvent_t>(start_event);
+  g_ev_stop = static_cast<cudaEvent_t>(stop_event);
   return PKV_OK;
 }
 

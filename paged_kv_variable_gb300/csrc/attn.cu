@@ -2,52 +2,81 @@
 //
 // One CTA per SM walks its host-assigned list of work items (flashinfer PR
 // "[Refactor] Uniform PoDAttention API with Horizontal Fusion SMs Schedule",
-// Key Changes 2: prefill and decode work share one persistent launch).  Warp 0
-// gathers K/V tiles of 128 keys with TMA: one 16-row box per (page, 128-byte
-// column chunk), page numbers read from block_table (vLLM PR "[Kernel][Triton]
-// [FP8] ...", review: block_table support; TransformerEngine PR "Add KV cache
-// for paged/non-paged attention": one table for K and V, bshd pages), into a
-// ring of shared-memory stages guarded by mbarriers (the prefetch of cached KV
-// of the cutlass-sycl PR "Extend FlashAttention Prefill with KV cache").
-// Warps 1..4 compute S = Q K^T, the masked online softmax and O += P V on the
-// tensor cores and write either the final output or a split-KV partial.
+// Key Changes 2: prefill and decode work share one persistent launch).
 //
-// Tile kinds:
-//   decode  -- up to 16 rows (query tokens x group heads); the 4 warps split
-//              the 128 keys of each tile and merge at the end of the item.
-//   prefill -- 64 rows; each warp owns 16 rows and all 128 keys of a tile.
+// Warp roles (192 threads):
+//   warp 0      TMA producer: K/V tiles of 128 keys, one 16-row box per
+//               (page, 128-byte column chunk), page numbers read from
+//               block_table (vLLM PR "[Kernel][Triton][FP8] ...", review:
+//               block_table support; TransformerEngine PR "Add KV cache for
+//               paged/non-paged attention": one table for K and V, bshd pages)
+//               into a ring of shared-memory stages (the cached-KV prefetch of
+//               the cutlass-sycl PR "Extend FlashAttention Prefill with KV
+//               cache"); plus the 128-row Q tile of a prefill item.
+//   warp 1      owns tensor memory and issues the tcgen05 MMAs of prefill
+//               tiles: S = Q K^T into TMEM (two buffers), O += P V into TMEM.
+//   warps 2..5  consumers.  Prefill tile: one query row per thread, masked
+//               online softmax on S read from TMEM, P written to shared memory
+//               for the next MMA, O rescaled in TMEM, epilogue.  Decode tile
+//               (<= 16 rows): warp-level MMAs, the four warps split the keys
+//               of each tile and merge at the end of the item.
+//
 // fp8 caches (vLLM PR, 8-bit KV cache) are converted to bf16 in shared memory
 // (exact), with k_scale folded into the logit scale and v_scale applied to the
-// normalised output.
+// normalised output; their prefill tiles use the warp-level MMA path (64 rows).
 #include <cuda_bf16.h>
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "tcgen05.cuh"
 
 namespace pkv {
 
 namespace {
 
 constexpr int kConsumerWarps = 4;
-constexpr int kThreads = 32 * (1 + kConsumerWarps);
+constexpr int kThreads = 32 * (2 + kConsumerWarps);
+constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr float kLn2 = 0.693147180559945309f;
+constexpr uint32_t kTmemCols = 512;   // S0 [0,128), S1 [128,256), O [256, 256+D)
+constexpr uint32_t kTmemO = 256;
 
 template <int D, bool FP8>
 struct Layout {
+  static constexpr bool kTc = !FP8;                        // tensor-core (tcgen05) prefill tiles
   static constexpr int kEsize = FP8 ? 1 : 2;
-  static constexpr int kStages = 3;
+  static constexpr int kStagesK = (FP8 || D == 128) ? 3 : 4;  // K ring (released after S = Q K^T)
+  static constexpr int kStagesV = (FP8 || D == 128) ? (FP8 ? 3 : 2) : 4;  // V ring (released after O += P V)
   static constexpr int kTileBytes = kKvTile * D * kEsize;   // one raw K (or V) tile
   static constexpr int kChunks = D * kEsize / 128;            // 128-byte column chunks per cache row
   static constexpr int kBf16Tile = kKvTile * D * 2;
-  static constexpr int kStageOff = 0;                         // [stage][K, V]
-  static constexpr int kDeqOff = kStages * 2 * kTileBytes;    // fp8: bf16 copies of K and V
-  static constexpr int kMergeOff = kDeqOff + (FP8 ? 2 * kBf16Tile : 0);
+  static constexpr int kKOff = 0;                             // K ring
+  static constexpr int kVOff = kStagesK * kTileBytes;         // V ring
+  static constexpr int kQOff = kVOff + kStagesV * kTileBytes; // tcgen05 path: Q tile (128 x D bf16)
+  static constexpr int kDeqOff = kQOff + (kTc ? kKvTile * D * 2 : 0);  // fp8: bf16 copies of K and V
+  static constexpr int kPOff = kDeqOff + (FP8 ? 2 * kBf16Tile : 0);    // P (128 x 128 bf16) / decode merge
   static constexpr int kMergeBytes = kConsumerWarps * kDecodeRows * D * 4;
-  static constexpr int kMlOff = kMergeOff + kMergeBytes;      // float[4][16][2]: (m, l)
+  static constexpr int kPBytes = kTc ? (kMergeBytes > 32768 ? kMergeBytes : 32768) : kMergeBytes;
+  static constexpr int kMlOff = kPOff + kPBytes;              // float[4][16][2]: (m, l)
   static constexpr int kBarOff = kMlOff + kConsumerWarps * kDecodeRows * 2 * 4;
-  static constexpr int kAbortOff = kBarOff + 3 * kStages * 8;
-  static constexpr int kBytes = kAbortOff + 16;
+  static constexpr int kNumBars = 2 * kStagesK + 2 * kStagesV + 9;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;     // tmem base, abort flag
+  static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes + 1024;                // room to align the base to 1024
+};
+
+struct Bars {
+  uint64_t* full_k;
+  uint64_t* empty_k;
+  uint64_t* full_v;
+  uint64_t* empty_v;
+  uint64_t* q_full;
+  uint64_t* q_empty;
+  uint64_t* s_full;   // [2]
+  uint64_t* s_free;   // [2]
+  uint64_t* p_full;
+  uint64_t* o_done;
+  uint64_t* drain;    // MMA completion before tensor memory is freed after an abort
 };
 
 // Byte offset of 16-byte chunk c of row r in a bf16 tile stored as
@@ -60,11 +89,15 @@ __device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16* p) {
   return __ldg(reinterpret_cast<const unsigned int*>(p));
 }
 
+__device__ __forceinline__ int num_tiles(const WorkItem& w) {
+  return w.kv_end > w.kv_begin ? (w.kv_end - w.kv_begin + kKvTile - 1) / kKvTile : 0;
+}
+
 // fp8 K or V tile (128 rows x 128 codes, swizzled) -> bf16 tile in the layout above.
 __device__ __forceinline__ void dequant_tile(const uint8_t* raw, uint8_t* dst, int ctid) {
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    const int u = ctid + 128 * k;
+    const int u = ctid + kConsumerThreads * k;
     const int r = u >> 3, c = u & 7;
     const uint4 w = *reinterpret_cast<const uint4*>(raw + r * 128 + (((c ^ (r & 7))) << 4));
     uint4 lo, hi;
@@ -85,94 +118,333 @@ struct Ring {
   int stage = 0;
   uint32_t phase = 0;
   template <int NS>
-  __device__ __forceinline__ void advance() {
-    if (++stage == NS) {
-      stage = 0;
-      phase ^= 1;
+  __device__ __forceinline__ void advance(int n = 1) {
+    for (int i = 0; i < n; ++i) {
+      if (++stage == NS) {
+        stage = 0;
+        phase ^= 1;
+      }
     }
   }
 };
 
 // ------------------------------------------------------------------ producer
+// Issues K of tile j+1 before V of tile j, so that S = Q K^T of the next tile
+// never waits behind the V ring.
+struct TileRef {
+  int b, hk, t0, kv_end;
+};
+
 template <int D, bool FP8>
-__device__ void producer(const AttnParams& p, const CUtensorMap* tm_k, const CUtensorMap* tm_v, uint8_t* smem,
-                         uint64_t* full_k, uint64_t* full_v, uint64_t* empty, volatile int* abort_flag, int it0,
+__device__ __forceinline__ void load_tile(const AttnParams& p, const CUtensorMap* tm, uint8_t* dst, uint64_t* bar,
+                                          const TileRef& t) {
+  using L = Layout<D, FP8>;
+  const int32_t* bt = p.block_table + (int64_t)t.b * p.bt_stride;
+  mbar_arrive_expect_tx(bar, L::kTileBytes);
+#pragma unroll 1
+  for (int g = 0; g < kKvTile / kBoxRows; ++g) {
+    const int j0 = t.t0 + g * kBoxRows;
+    int page = p.num_pages, slot = 0;  // out of range: the copy fills zeros
+    if (j0 < t.kv_end) {
+      if (p.page_size > 0) {
+        page = __ldg(bt + j0 / p.page_size);
+        slot = j0 % p.page_size;
+        if (page < 0 || page >= p.num_pages) {
+          record_status(p.status, PKV_ERR_DEVICE_BOUNDS, t.b, page);
+          page = p.num_pages;
+          slot = 0;
+        }
+      } else {
+        page = t.b;
+        slot = j0;
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < L::kChunks; ++c)
+      tma_load_4d(dst + c * (kKvTile * 128) + g * (kBoxRows * 128), tm, bar, c * (128 / L::kEsize), t.hk, slot,
+                  page);
+  }
+}
+
+template <int D, bool FP8>
+__device__ void producer(const AttnParams& p, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                         const CUtensorMap* tm_q, uint8_t* smem, const Bars& B, volatile int* abort_flag, int it0,
                          int it1) {
   using L = Layout<D, FP8>;
   tma_prefetch_desc(tm_k);
   tma_prefetch_desc(tm_v);
-  Ring ring;
-  int issued = 0;
-  bool ok = true;
+  Ring rk, rv;
+  int issued_k = 0, issued_v = 0;
+  uint32_t pi = 0;  // prefill items with at least one tile
+  bool ok = true, pending = false;
+  TileRef pend{};
+  auto issue_v = [&](const TileRef& t) -> bool {
+    if (!mbar_wait(&B.empty_v[rv.stage], rv.phase ^ 1, abort_flag)) return false;
+    load_tile<D, FP8>(p, tm_v, smem + L::kVOff + rv.stage * L::kTileBytes, &B.full_v[rv.stage], t);
+    ++issued_v;
+    rv.advance<L::kStagesV>();
+    return true;
+  };
   for (int it = it0; it < it1 && ok; ++it) {
     const WorkItem w = p.items[it];
-    const int32_t* bt = p.block_table + (int64_t)w.b * p.bt_stride;
-    for (int t0 = w.kv_begin; t0 < w.kv_end; t0 += kKvTile) {
-      if (!mbar_wait(&empty[ring.stage], ring.phase ^ 1, abort_flag)) {
+    if (L::kTc && w.kind == kPrefill && num_tiles(w) > 0) {
+      if (!mbar_wait(B.q_empty, (pi & 1) ^ 1, abort_flag)) {
         ok = false;
         break;
       }
-      uint8_t* kdst = smem + L::kStageOff + ring.stage * 2 * L::kTileBytes;
-      uint8_t* vdst = kdst + L::kTileBytes;
-      mbar_arrive_expect_tx(&full_k[ring.stage], L::kTileBytes);
-      mbar_arrive_expect_tx(&full_v[ring.stage], L::kTileBytes);
-#pragma unroll 1
-      for (int g = 0; g < kKvTile / kBoxRows; ++g) {
-        const int j0 = t0 + g * kBoxRows;
-        int page = p.num_pages, slot = 0;  // out of range: the copy fills zeros
-        if (j0 < w.kv_end) {
-          if (p.page_size > 0) {
-            page = __ldg(bt + j0 / p.page_size);
-            slot = j0 % p.page_size;
-            if (page < 0 || page >= p.num_pages) {
-              record_status(p.status, PKV_ERR_DEVICE_BOUNDS, w.b, page);
-              page = p.num_pages;
-              slot = 0;
-            }
-          } else {
-            page = w.b;
-            slot = j0;
-          }
-        }
+      const int tq = kPrefillRowsTc / p.G;
+      mbar_arrive_expect_tx(B.q_full, (uint32_t)((D / 64) * p.G * tq * 128));
 #pragma unroll
-        for (int c = 0; c < L::kChunks; ++c) {
-          const int off = c * (kKvTile * 128) + g * (kBoxRows * 128);
-          tma_load_4d(kdst + off, tm_k, &full_k[ring.stage], c * (128 / L::kEsize), w.hk, slot, page);
-          tma_load_4d(vdst + off, tm_v, &full_v[ring.stage], c * (128 / L::kEsize), w.hk, slot, page);
-        }
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_3d(smem + L::kQOff + c * (kKvTile * 128), tm_q, B.q_full, c * 64, w.hk * p.G, w.q_row0);
+      ++pi;
+    }
+    for (int t0 = w.kv_begin; t0 < w.kv_end; t0 += kKvTile) {
+      const TileRef cur{w.b, w.hk, t0, w.kv_end};
+      if (!mbar_wait(&B.empty_k[rk.stage], rk.phase ^ 1, abort_flag)) {
+        ok = false;
+        break;
       }
-      ++issued;
-      ring.advance<L::kStages>();
+      load_tile<D, FP8>(p, tm_k, smem + L::kKOff + rk.stage * L::kTileBytes, &B.full_k[rk.stage], cur);
+      ++issued_k;
+      rk.advance<L::kStagesK>();
+      if (pending && !issue_v(pend)) {
+        ok = false;
+        break;
+      }
+      pend = cur;
+      pending = true;
     }
   }
+  if (ok && pending) ok = issue_v(pend);
   if (!ok) {
     record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, 0);
     *abort_flag = 1;
     // let the copies already issued land before the CTA can exit (bounded)
     int zero = 0;
-    const int n = issued < L::kStages ? issued : L::kStages;
-    for (int k = issued - n; k < issued; ++k) {
-      const int s = k % L::kStages;
-      const uint32_t ph = (uint32_t)((k / L::kStages) & 1);
-      mbar_wait(&full_k[s], ph, &zero);
-      mbar_wait(&full_v[s], ph, &zero);
-    }
+    const int nk = issued_k < L::kStagesK ? issued_k : L::kStagesK;
+    for (int k = issued_k - nk; k < issued_k; ++k)
+      mbar_wait(&B.full_k[k % L::kStagesK], (uint32_t)((k / L::kStagesK) & 1), &zero);
+    const int nv = issued_v < L::kStagesV ? issued_v : L::kStagesV;
+    for (int k = issued_v - nv; k < issued_v; ++k)
+      mbar_wait(&B.full_v[k % L::kStagesV], (uint32_t)((k / L::kStagesV) & 1), &zero);
   }
 }
 
-// ------------------------------------------------------------------ consumers
+// ------------------------------------------------------------------ MMA issuer (prefill tiles)
+template <int D>
+__device__ bool mma_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, volatile int* abort_flag,
+                           uint32_t tmem, int it0, int it1) {
+  using L = Layout<D, false>;
+  constexpr uint32_t kIdescQK = idesc_f16(1, 0, 128, 128);
+  constexpr uint32_t kIdescPV = idesc_f16(1, 1, 128, D);
+  const uint32_t q_base = smem_u32(smem + L::kQOff);
+  const uint32_t p_base = smem_u32(smem + L::kPOff);
+  Ring rk, rv;
+  uint32_t pt = 0, pi = 0;
+
+  auto do_pv = [&](uint32_t T, bool first) -> bool {
+    if (!mbar_wait(B.p_full, T & 1, abort_flag)) return false;
+    if (!mbar_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
+    tc_fence_after();
+    const uint32_t v_base = smem_u32(smem + L::kVOff + rv.stage * L::kTileBytes);
+#pragma unroll
+    for (int k = 0; k < kKvTile / 16; ++k) {
+      const uint64_t a = sdesc_sw128(p_base + (k >> 2) * (kKvTile * 128) + (k & 3) * 32, 16, 1024);
+      const uint64_t b = sdesc_sw128(v_base + k * 16 * 128, kKvTile * 128, 1024);
+      umma_ss(tmem + kTmemO, a, b, kIdescPV, (first && k == 0) ? 0u : 1u);
+    }
+    umma_commit(B.o_done);
+#pragma unroll
+    for (int i = 0; i < kConsumerWarps; ++i) umma_commit(&B.empty_v[rv.stage]);
+    rv.advance<L::kStagesV>();
+    return true;
+  };
+
+  for (int it = it0; it < it1; ++it) {
+    const WorkItem w = p.items[it];
+    const int n = num_tiles(w);
+    if (w.kind != kPrefill) {
+      rk.advance<L::kStagesK>(n);
+      rv.advance<L::kStagesV>(n);
+      continue;
+    }
+    if (n == 0) continue;
+    if (!mbar_wait(B.q_full, pi & 1, abort_flag)) return false;
+    for (int j = 0; j < n; ++j) {
+      const uint32_t T = pt + j;
+      if (!mbar_wait(&B.full_k[rk.stage], rk.phase, abort_flag)) return false;
+      if (T >= 2 && !mbar_wait(&B.s_free[T & 1], ((T >> 1) & 1) ^ 1, abort_flag)) return false;
+      tc_fence_after();
+      const uint32_t k_base = smem_u32(smem + L::kKOff + rk.stage * L::kTileBytes);
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = (k >> 2) * (kKvTile * 128) + (k & 3) * 32;
+        umma_ss(tmem + (T & 1) * 128, sdesc_sw128(q_base + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024),
+                kIdescQK, k > 0 ? 1u : 0u);
+      }
+      umma_commit(&B.s_full[T & 1]);
+#pragma unroll
+      for (int i = 0; i < kConsumerWarps; ++i) umma_commit(&B.empty_k[rk.stage]);
+      if (j == n - 1) umma_commit(B.q_empty);
+      rk.advance<L::kStagesK>();
+      if (j >= 1 && !do_pv(T - 1, j == 1)) return false;
+    }
+    if (!do_pv(pt + n - 1, n == 1)) return false;
+    pt += n;
+    ++pi;
+  }
+  return true;
+}
+
+// ------------------------------------------------------------------ prefill tile softmax (tcgen05 path)
+template <int D>
+__device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, const Bars& B,
+                             volatile int* abort_flag, uint32_t tmem, Ring& rk, Ring& rv, uint32_t& pt, float sl2) {
+  using L = Layout<D, false>;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qw = warp & 3;                   // TMEM lane quarter this warp may access
+  const int r = qw * 32 + lane;              // tile row == TMEM lane
+  const uint32_t t_lane = tmem + ((uint32_t)(qw * 32) << 16);
+  const int R = w.n_q * p.G;
+  const bool valid = r < R;
+  const int tok = w.q_row0 + r / p.G;
+  const int head = w.hk * p.G + r % p.G;
+  int lim = 0;
+  if (valid) {
+    lim = w.kv_end;
+    if (p.causal) lim = min(lim, w.q_i0 + r / p.G + w.lk - w.lq + 1);
+  }
+  const int n = num_tiles(w);
+  float m = -INFINITY, l = 0.f;
+  uint8_t* pbuf = smem + L::kPOff;
+
+  for (int j = 0; j < n; ++j) {
+    const uint32_t T = pt + j;
+    const int t0 = w.kv_begin + j * kKvTile;
+    if (!mbar_wait(&B.s_full[T & 1], (T >> 1) & 1, abort_flag)) return false;
+    tc_fence_after();
+    uint32_t s[128];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tmem_ld32(t_lane + (T & 1) * 128 + c * 32, s + c * 32);
+    tmem_wait_ld();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&B.s_free[T & 1]);
+
+    // mask by select (rows past the sequence see nothing), row max
+    const bool need_mask = t0 + kKvTile > lim;
+    float mx = -INFINITY;
+    if (__any_sync(0xffffffffu, need_mask)) {
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        const float v = (t0 + c < lim) ? __uint_as_float(s[c]) : -INFINITY;
+        s[c] = __float_as_uint(v);
+        mx = fmaxf(mx, v);
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+    }
+    const float m_new = fmaxf(m, mx * sl2);
+    const float mu = m_new == -INFINITY ? 0.f : m_new;
+    const float alpha = ex2(m - mu);
+    float sum = 0.f;
+    uint32_t pk[64];
+#pragma unroll
+    for (int c = 0; c < 64; ++c) {
+      const float p0 = ex2(fmaf(__uint_as_float(s[2 * c]), sl2, -mu));
+      const float p1 = ex2(fmaf(__uint_as_float(s[2 * c + 1]), sl2, -mu));
+      sum += p0 + p1;
+      pk[c] = pack_bf16(p0, p1);
+    }
+    l = l * alpha + sum;
+    m = m_new;
+
+    // P buffer and O are free once the previous tile's P V has completed
+    if (j > 0 && !mbar_wait(B.o_done, (T - 1) & 1, abort_flag)) return false;
+    tc_fence_after();
+    if (t0 + kKvTile > w.lk) {
+      // rows past the sequence may hold anything (even NaN): zero them in V
+      if (!mbar_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
+      if (t0 + r >= w.lk) {
+        uint8_t* vrow = smem + L::kVOff + rv.stage * L::kTileBytes + r * 128;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+#pragma unroll
+          for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(vrow + c * (kKvTile * 128) + q * 16) = make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+      *reinterpret_cast<uint4*>(pbuf + tile_off(r, c)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+    if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(t_lane + kTmemO + c * 32, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+        tmem_st32(t_lane + kTmemO + c * 32, o);
+      }
+      tmem_wait_st();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(B.p_full);
+    rk.advance<L::kStagesK>();
+    rv.advance<L::kStagesV>();
+  }
+
+  // epilogue: O / l -> bf16 rows, natural-log LSE
+  __nv_bfloat16* dst = p.out + (int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head;
+  if (n > 0) {
+    if (!mbar_wait(B.o_done, (pt + n - 1) & 1, abort_flag)) return false;
+    tc_fence_after();
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      tmem_ld32(t_lane + kTmemO + c * 32, o);
+      tmem_wait_ld();
+      if (valid) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 v;
+          v.x = pack_bf16(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+          v.y = pack_bf16(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+          v.z = pack_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+          v.w = pack_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+          *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) = v;
+        }
+      }
+    }
+    tc_fence_before();
+  } else if (valid) {
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) *reinterpret_cast<uint4*>(dst + c * 8) = make_uint4(0, 0, 0, 0);
+  }
+  if (valid && p.lse != nullptr)
+    p.lse[(int64_t)head * p.total_q + tok] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+  pt += n;
+  return true;
+}
+
+// ------------------------------------------------------------------ warp-MMA tiles (decode; fp8 prefill)
 // KPW = keys of each 128-key tile handled by one warp: 32 (decode), 128 (prefill).
 template <int D, bool FP8, int KPW>
-__device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, uint64_t* full_k, uint64_t* full_v,
-                         uint64_t* empty, volatile int* abort_flag, Ring& ring, float sl2, float vscale) {
+__device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, const Bars& B,
+                         volatile int* abort_flag, Ring& rk, Ring& rv, float sl2, float vscale) {
   using L = Layout<D, FP8>;
   constexpr int NT = KPW / 8;       // S column tiles per warp
   constexpr int KS = D / 16;        // k-steps of Q K^T
   constexpr int NO = D / 8;         // O column tiles
   constexpr bool kDecodeTile = (KPW != kKvTile);
   const int lane = threadIdx.x & 31;
-  const int cw = (threadIdx.x >> 5) - 1;  // consumer warp 0..3
-  const int ctid = threadIdx.x - 32;
+  const int cw = (threadIdx.x >> 5) - 2;  // consumer warp 0..3
+  const int ctid = threadIdx.x - 64;
   const int g = lane >> 2, t = lane & 3;
   const int row_blk = kDecodeTile ? 0 : cw;
   const int kw0 = kDecodeTile ? cw * KPW : 0;
@@ -212,19 +484,21 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
   for (int t0 = w.kv_begin; t0 < w.kv_end; t0 += kKvTile) {
-    if (!mbar_wait(&full_k[ring.stage], ring.phase, abort_flag)) return false;
-    uint8_t* stage_k = smem + L::kStageOff + ring.stage * 2 * L::kTileBytes;
-    uint8_t* stage_v = stage_k + L::kTileBytes;
+    if (!mbar_wait(&B.full_k[rk.stage], rk.phase, abort_flag)) return false;
+    uint8_t* stage_k = smem + L::kKOff + rk.stage * L::kTileBytes;
+    uint8_t* stage_v = smem + L::kVOff + rv.stage * L::kTileBytes;
     uint32_t kb, vb;
     if constexpr (FP8) {
       uint8_t* dk = smem + L::kDeqOff;
       uint8_t* dv = dk + L::kBf16Tile;
       dequant_tile(stage_k, dk, ctid);
-      if (!mbar_wait(&full_v[ring.stage], ring.phase, abort_flag)) return false;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B.empty_k[rk.stage]);
+      if (!mbar_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
       dequant_tile(stage_v, dv, ctid);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[ring.stage]);
-      named_bar_sync(1, 32 * kConsumerWarps);
+      if (lane == 0) mbar_arrive(&B.empty_v[rv.stage]);
+      named_bar_sync(1, kConsumerThreads);
       kb = smem_u32(dk);
       vb = smem_u32(dv);
     } else {
@@ -247,6 +521,11 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
         mma_bf16(s[2 * np], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
         mma_bf16(s[2 * np + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
       }
+    }
+
+    if constexpr (!FP8) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B.empty_k[rk.stage]);
     }
 
     // mask (select, never add) + online softmax in the log2 domain
@@ -295,7 +574,7 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
 
     // O += P V
     if constexpr (!FP8) {
-      if (!mbar_wait(&full_v[ring.stage], ring.phase, abort_flag)) return false;
+      if (!mbar_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
     }
     const bool vmask = t0 + kKvTile > w.lk;  // rows past the sequence may hold anything: zero them
 #pragma unroll
@@ -325,11 +604,12 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
     }
     if constexpr (!FP8) {
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[ring.stage]);
+      if (lane == 0) mbar_arrive(&B.empty_v[rv.stage]);
     } else {
-      named_bar_sync(1, 32 * kConsumerWarps);  // bf16 copies free for the next tile
+      named_bar_sync(1, kConsumerThreads);  // bf16 copies free for the next tile
     }
-    ring.advance<L::kStages>();
+    rk.advance<L::kStagesK>();
+    rv.advance<L::kStagesV>();
   }
 
   // ---------------------------------------------------------------- epilogue
@@ -340,14 +620,14 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
 
   if constexpr (kDecodeTile) {
     float* ml = reinterpret_cast<float*>(smem + L::kMlOff);
-    float* mo = reinterpret_cast<float*>(smem + L::kMergeOff);
+    float* mo = reinterpret_cast<float*>(smem + L::kPOff);
     if (t == 0) {
       ml[(cw * 16 + g) * 2 + 0] = m0;
       ml[(cw * 16 + g) * 2 + 1] = l0;
       ml[(cw * 16 + g + 8) * 2 + 0] = m1;
       ml[(cw * 16 + g + 8) * 2 + 1] = l1;
     }
-    named_bar_sync(1, 32 * kConsumerWarps);
+    named_bar_sync(1, kConsumerThreads);
     float M0 = -INFINITY, M1 = -INFINITY;
 #pragma unroll
     for (int ww = 0; ww < kConsumerWarps; ++ww) {
@@ -362,8 +642,8 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
       *reinterpret_cast<float2*>(mo + (cw * 16 + g + 8) * D + n * 8 + 2 * t) =
           make_float2(o[n][2] * f1, o[n][3] * f1);
     }
-    named_bar_sync(1, 32 * kConsumerWarps);
-    for (int idx = ctid; idx < R * D; idx += 32 * kConsumerWarps) {
+    named_bar_sync(1, kConsumerThreads);
+    for (int idx = ctid; idx < R * D; idx += kConsumerThreads) {
       const int row = idx / D, d = idx % D;
       float M = -INFINITY;
 #pragma unroll
@@ -387,7 +667,7 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
         if (d == 0 && p.lse != nullptr) p.lse[(int64_t)head * p.total_q + tok] = lse2 * kLn2;
       }
     }
-    named_bar_sync(1, 32 * kConsumerWarps);
+    named_bar_sync(1, kConsumerThreads);
   } else {
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
@@ -412,75 +692,139 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
 }
 
 template <int D, bool FP8>
-__global__ void __launch_bounds__(kThreads, 1)
-    attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v) {
+__device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, volatile int* abort_flag, uint32_t tmem,
+                         int it0, int it1) {
   using L = Layout<D, FP8>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  uint64_t* full_k = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
-  uint64_t* full_v = full_k + L::kStages;
-  uint64_t* empty = full_v + L::kStages;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbortOff);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < L::kStages; ++s) {
-      mbar_init(&full_k[s], 1);
-      mbar_init(&full_v[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
-    }
-    *abort_flag = 0;
-    fence_mbarrier_init();
-  }
-  __syncthreads();
-  const int it0 = p.cta_begin[blockIdx.x], it1 = p.cta_begin[blockIdx.x + 1];
-  if (warp == 0) {
-    if (lane == 0) producer<D, FP8>(p, &tm_k, &tm_v, smem, full_k, full_v, empty, abort_flag, it0, it1);
-    return;
-  }
-  const int ctid = threadIdx.x - 32;
+  const int ctid = threadIdx.x - 64;
   if (blockIdx.x == 0) {
-    for (int b = ctid; b < p.batch; b += 32 * kConsumerWarps)
+    for (int b = ctid; b < p.batch; b += kConsumerThreads)
       if (__ldg(p.cache_seqlens + b) != __ldg(p.plan_lc + b))
         record_status(p.status, PKV_ERR_PLAN_MISMATCH, b, __ldg(p.cache_seqlens + b));
   }
   const float kscale = FP8 ? __ldg(p.k_scale) : 1.f;
   const float vscale = FP8 ? __ldg(p.v_scale) : 1.f;
   const float sl2 = p.scale_log2 * kscale;
-  Ring ring;
+  Ring rk, rv;
+  uint32_t pt = 0;
   for (int it = it0; it < it1; ++it) {
     const WorkItem w = p.items[it];
     bool ok;
-    if (w.kind == kDecode)
-      ok = run_item<D, FP8, kKvTile / kConsumerWarps>(p, w, smem, full_k, full_v, empty, abort_flag, ring, sl2, vscale);
-    else
-      ok = run_item<D, FP8, kKvTile>(p, w, smem, full_k, full_v, empty, abort_flag, ring, sl2, vscale);
+    if (w.kind == kDecode) {
+      ok = run_item<D, FP8, kKvTile / kConsumerWarps>(p, w, smem, B, abort_flag, rk, rv, sl2, vscale);
+    } else if constexpr (L::kTc) {
+      ok = softmax_item<D>(p, w, smem, B, abort_flag, tmem, rk, rv, pt, sl2);
+    } else {
+      ok = run_item<D, FP8, kKvTile>(p, w, smem, B, abort_flag, rk, rv, sl2, vscale);
+    }
     if (!ok) {
       record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, it);
       *abort_flag = 1;
-      return;
+      return false;
     }
   }
+  return true;
 }
 
 template <int D, bool FP8>
-cudaError_t launch_t(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int num_ctas, cudaStream_t s) {
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q) {
+  using L = Layout<D, FP8>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  Bars B;
+  B.full_k = bars;
+  B.empty_k = bars + L::kStagesK;
+  B.full_v = bars + 2 * L::kStagesK;
+  B.empty_v = bars + 2 * L::kStagesK + L::kStagesV;
+  B.q_full = bars + 2 * L::kStagesK + 2 * L::kStagesV;
+  B.q_empty = B.q_full + 1;
+  B.s_full = B.q_full + 2;
+  B.s_free = B.q_full + 4;
+  B.p_full = B.q_full + 6;
+  B.o_done = B.q_full + 7;
+  B.drain = B.q_full + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < L::kStagesK; ++s) {
+      mbar_init(&B.full_k[s], 1);
+      mbar_init(&B.empty_k[s], kConsumerWarps);
+    }
+    for (int s = 0; s < L::kStagesV; ++s) {
+      mbar_init(&B.full_v[s], 1);
+      mbar_init(&B.empty_v[s], kConsumerWarps);
+    }
+    mbar_init(B.q_full, 1);
+    mbar_init(B.q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&B.s_full[i], 1);
+      mbar_init(&B.s_free[i], kConsumerWarps);
+    }
+    mbar_init(B.p_full, kConsumerWarps);
+    mbar_init(B.o_done, 1);
+    mbar_init(B.drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (L::kTc && warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = L::kTc ? *tmem_slot : 0u;
+  const int it0 = p.cta_begin[blockIdx.x], it1 = p.cta_begin[blockIdx.x + 1];
+  if (warp == 0) {
+    if (lane == 0) producer<D, FP8>(p, &tm_k, &tm_v, &tm_q, smem, B, abort_flag, it0, it1);
+    return;
+  }
+  if (warp == 1) {
+    if constexpr (L::kTc) {
+      if (lane == 0) {
+        if (!mma_issuer<D>(p, smem, B, abort_flag, tmem, it0, it1)) {
+          record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, -1);
+          *abort_flag = 1;
+          // wait (bounded) for the MMAs already issued before the memory is freed
+          int zero = 0;
+          umma_commit(B.drain);
+          mbar_wait(B.drain, 0, &zero);
+        }
+      }
+      __syncwarp();
+    }
+  } else {
+    consumer<D, FP8>(p, smem, B, abort_flag, tmem, it0, it1);
+  }
+  // warps 1..5: every tensor-memory access is done before warp 1 frees it
+  tc_fence_before();
+  named_bar_sync(2, 32 * (1 + kConsumerWarps));
+  tc_fence_after();
+  if (L::kTc && warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int D, bool FP8>
+cudaError_t launch_t(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
+                     int num_ctas, cudaStream_t s) {
   using L = Layout<D, FP8>;
   static_assert(L::kAlloc <= 232448, "shared memory budget");
   cudaError_t e = cudaFuncSetAttribute(attn_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
-  attn_kernel<D, FP8><<<num_ctas, kThreads, L::kAlloc, s>>>(p, tk, tv);
+  attn_kernel<D, FP8><<<num_ctas, kThreads, L::kAlloc, s>>>(p, tk, tv, tq);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v, int num_ctas,
-                             int head_dim, bool fp8, cudaStream_t stream) {
+cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                             const CUtensorMap& tm_q, int num_ctas, int head_dim, bool fp8, cudaStream_t stream) {
   if (num_ctas == 0) return cudaSuccess;
-  if (fp8) return launch_t<128, true>(p, tm_k, tm_v, num_ctas, stream);
-  if (head_dim == 128) return launch_t<128, false>(p, tm_k, tm_v, num_ctas, stream);
-  return launch_t<64, false>(p, tm_k, tm_v, num_ctas, stream);
+  if (fp8) return launch_t<128, true>(p, tm_k, tm_v, tm_q, num_ctas, stream);
+  if (head_dim == 128) return launch_t<128, false>(p, tm_k, tm_v, tm_q, num_ctas, stream);
+  return launch_t<64, false>(p, tm_k, tm_v, tm_q, num_ctas, stream);
 }
 
 }  // namespace pkv

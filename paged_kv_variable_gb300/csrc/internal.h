@@ -10,7 +10,8 @@ namespace pkv {
 
 constexpr int kKvTile = 128;        // keys per K/V tile (one pipeline stage)
 constexpr int kDecodeRows = 16;     // rows (query tokens x G) of a decode tile
-constexpr int kPrefillRows = 64;    // rows of a prefill tile (4 warps x 16)
+constexpr int kPrefillRowsTc = 128;  // rows of a bf16 prefill tile (tcgen05, one TMEM lane per row)
+constexpr int kPrefillRowsWarp = 64; // rows of an fp8-cache prefill tile (4 warps x 16, warp MMA)
 constexpr int kBoxRows = 16;        // cache rows per TMA box (divides every page size)
 
 enum ItemKind : int32_t { kDecode = 0, kPrefill = 1 };

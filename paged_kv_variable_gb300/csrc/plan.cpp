@@ -64,8 +64,8 @@ pkv_status validate_problem(const pkv_problem* p) {
   if (p->num_pages <= 0) return fail(PKV_ERR_INVALID_ARG, "num_pages must be positive");
   if (p->page_size == 0 && p->num_pages < p->batch)
     return fail(PKV_ERR_INVALID_ARG, "contiguous cache: batch_size_cache (num_pages) < batch");
-  if (!std::isfinite(p->softmax_scale) || p->softmax_scale == 0.0f)
-    return fail(PKV_ERR_INVALID_ARG, "softmax_scale must be finite and non-zero");
+  if (!std::isfinite(p->softmax_scale) || !(p->softmax_scale > 0.0f))
+    return fail(PKV_ERR_INVALID_ARG, "softmax_scale must be finite and positive");
   return PKV_OK;
 }
 
@@ -89,7 +89,8 @@ extern "C" pkv_status pkv_plan(const pkv_problem* problem, const int32_t* h_q_le
   const int G = p.num_heads_q / p.num_heads_kv;
   const int D = p.head_dim;
   const int esize = p.cache_dtype == PKV_BF16 ? 2 : 1;
-  const int tq_prefill = kPrefillRows / G;  // query tokens per prefill tile
+  const int prefill_rows = p.cache_dtype == PKV_BF16 ? kPrefillRowsTc : kPrefillRowsWarp;
+  const int tq_prefill = prefill_rows / G;  // query tokens per prefill tile
 
   int64_t total_q = 0, total_new = 0, total_decode_keys = 0;
   for (int b = 0; b < B; ++b) {
@@ -170,7 +171,7 @@ extern "C" pkv_status pkv_plan(const pkv_problem* problem, const int32_t* h_q_le
           t.item.kv_end = kv_end;
           t.item.kind = kPrefill;
           t.item.partial = -1;
-          t.cost = prefill_cost(kv_end, kPrefillRows, D);
+          t.cost = prefill_cost(kv_end, prefill_rows, D);
           t.item.cost = (int32_t)std::min(t.cost, 2.0e9);
           tiles.push_back(t);
           ++n_pre;
@@ -278,6 +279,8 @@ extern "C" pkv_status pkv_plan_get_stats(pkv_plan_t plan, pkv_plan_stats* s) {
   s->max_items_per_cta = plan->max_items_per_cta;
   s->max_cta_cost = plan->max_cta_cost;
   s->mean_cta_cost = plan->mean_cta_cost;
+  s->upload_bytes = (int64_t)plan->image_bytes;
+  s->workspace_bytes = (int64_t)plan->layout.total;
   return PKV_OK;
 }
 

@@ -36,11 +36,19 @@ SENTINEL_VALUE = 1.0e4          # finite sentinel written into unused bf16 slots
 # ---------------------------------------------------------------------------
 # bf16 bit helpers (input construction only)
 # ---------------------------------------------------------------------------
-def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+def f32_to_bf16_bits(x: np.ndarray, check_nan: bool = True) -> np.ndarray:
     """Round float32 values to the nearest bf16 (ties to even); return bits."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    rounding = ((u >> 16) & 1) + 0x7FFF
-    out = ((u + rounding) >> 16).astype(np.uint16)
+    # finite and infinite inputs cannot overflow 32 bits here; NaNs are patched below
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    t = u >> 16
+    t &= 1
+    t += np.uint32(0x7FFF)
+    t += u
+    t >>= 16
+    out = t.astype(np.uint16)
+    del t
+    if not check_nan:
+        return out
     nan = np.isnan(np.asarray(x, dtype=np.float32))
     if nan.any():
         out = out.copy()
@@ -144,8 +152,8 @@ class Case:
 def _normal_bf16(rng: np.random.Generator, shape, mult: float = 1.0) -> np.ndarray:
     x = rng.standard_normal(size=shape, dtype=np.float32)
     if mult != 1.0:
-        x = x * np.float32(mult)
-    return f32_to_bf16_bits(x)
+        x *= np.float32(mult)
+    return f32_to_bf16_bits(x, check_nan=False)   # N(0,1) draws are never NaN
 
 
 def _amax_scale(*bits: np.ndarray) -> float:
@@ -449,11 +457,18 @@ def subset_case(case: Case, seqs) -> Case:
     sub = Spec(**{**spec.__dict__, "batch": len(seqs), "q_lens": spec.q_lens[seqs].copy(),
                   "cache_lens": spec.cache_lens[seqs].copy(), "new_lens": spec.new_lens[seqs].copy(),
                   "name": spec.name + "-subset"})
+    num_pages, poison = case.num_pages, case.poison_page
     if spec.paged:
-        kc, vc, bt = case.k_cache, case.v_cache, case.block_table[seqs].copy()
+        # keep only the pages these sequences reference, renumbered in order
+        rows = case.block_table[seqs]
+        used = np.unique(rows)
+        kc, vc = case.k_cache[used], case.v_cache[used]
+        bt = np.searchsorted(used, rows).astype(np.int32)
+        num_pages = int(used.size)
+        poison = int(np.searchsorted(used, poison)) if poison in used else -1
     else:
         kc, vc, bt = case.k_cache[seqs].copy(), case.v_cache[seqs].copy(), None
     return Case(spec=sub, q=take(case.q, cu_q), k_new=take(case.k_new, cu_n), v_new=take(case.v_new, cu_n),
-                k_cache=kc, v_cache=vc, block_table=bt, num_pages=case.num_pages, poison_page=case.poison_page,
+                k_cache=kc, v_cache=vc, block_table=bt, num_pages=num_pages, poison_page=poison,
                 prefix_k=take(case.prefix_k, cu_p), prefix_v=take(case.prefix_v, cu_p), k_scale=case.k_scale,
                 v_scale=case.v_scale, sentinel=case.sentinel)
