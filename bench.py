@@ -252,6 +252,9 @@ def gpu_arm(args):
     if args.workload == "decode-small":
         # 16 sequences of the decode batch (about 150 MB of KV, above L2): profiler captures
         main = Workload("decode-small", synth.subset_case(decode_case, list(range(16))), device)
+    elif args.workload == "prefill":
+        # the contiguous-cache causal prefill (profiler captures of the tensor-core tile)
+        main = Workload("prefill", synth.config3(True), device)
     else:
         main = Workload("decode", decode_case, device)
     with ClockSampler(local) as clk:
@@ -381,7 +384,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-secondary", dest="secondary", action="store_false")
-    ap.add_argument("--workload", default="decode", choices=["decode", "decode-small"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "decode-small", "prefill"])
     ap.add_argument("--no-cpu-leg", dest="cpu_leg", action="store_false")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -81,33 +81,42 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
   }
 }
 
-// One block per split unit; thread d owns column d of every row.
-// Partials are normalised outputs with log2-domain LSEs; the merge order over
-// chunks is fixed (deterministic).
+// One block per split unit; thread t owns row t / (D/8) and 8 consecutive
+// columns.  Partials are normalised outputs with log2-domain LSEs; the merge
+// order over chunks is fixed (deterministic).
 template <int D>
-__global__ void __launch_bounds__(D) combine_kernel(const CombineParams p) {
+__global__ void __launch_bounds__(kDecodeRows * D / 8) combine_kernel(const CombineParams p) {
   const CombineItem ci = p.items[blockIdx.x];
-  const int d = threadIdx.x;
-  const int rows = ci.n_q * p.G;
+  const int row = threadIdx.x / (D / 8);
+  const int d0 = (threadIdx.x % (D / 8)) * 8;
+  if (row >= ci.n_q * p.G) return;
   constexpr float kLn2 = 0.693147180559945309f;
-  for (int r = 0; r < rows; ++r) {
-    float m = -INFINITY;
-    for (int s = 0; s < ci.nsplit; ++s) m = fmaxf(m, p.partial_lse[(ci.slot0 + s) * kDecodeRows + r]);
-    const float m_use = m == -INFINITY ? 0.f : m;
-    float wsum = 0.f, acc = 0.f;
-    for (int s = 0; s < ci.nsplit; ++s) {
-      const float l = p.partial_lse[(ci.slot0 + s) * kDecodeRows + r];
-      const float w = ex2(l - m_use);
-      wsum += w;
-      acc += w * p.partial_o[((int64_t)(ci.slot0 + s) * kDecodeRows + r) * D + d];
-    }
-    const float o = wsum > 0.f ? acc / wsum : 0.f;
-    const int tok = ci.q_row0 + r / p.G;
-    const int head = ci.hk * p.G + r % p.G;
-    p.out[(int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head + d] = __float2bfloat16_rn(o);
-    if (p.lse != nullptr && d == 0)
-      p.lse[(int64_t)head * p.total_q + tok] = wsum > 0.f ? (m_use + __log2f(wsum)) * kLn2 : -INFINITY;
+  const float* lse = p.partial_lse + (int64_t)ci.slot0 * kDecodeRows + row;
+  float m = -INFINITY;
+  for (int s = 0; s < ci.nsplit; ++s) m = fmaxf(m, __ldg(lse + s * kDecodeRows));
+  const float m_use = m == -INFINITY ? 0.f : m;
+  float wsum = 0.f;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const float* po = p.partial_o + ((int64_t)ci.slot0 * kDecodeRows + row) * D + d0;
+  for (int s = 0; s < ci.nsplit; ++s) {
+    const float w = ex2(__ldg(lse + s * kDecodeRows) - m_use);
+    const float4 a = __ldg(reinterpret_cast<const float4*>(po + (int64_t)s * kDecodeRows * D));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(po + (int64_t)s * kDecodeRows * D + 4));
+    wsum += w;
+    acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
+    acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
   }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  const int tok = ci.q_row0 + row / p.G;
+  const int head = ci.hk * p.G + row % p.G;
+  uint4 v;
+  v.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+  v.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+  v.z = pack_bf16(acc[4] * inv, acc[5] * inv);
+  v.w = pack_bf16(acc[6] * inv, acc[7] * inv);
+  *reinterpret_cast<uint4*>(p.out + (int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head + d0) = v;
+  if (p.lse != nullptr && d0 == 0)
+    p.lse[(int64_t)head * p.total_q + tok] = wsum > 0.f ? (m_use + __log2f(wsum)) * kLn2 : -INFINITY;
 }
 
 cudaError_t launch_kv_append(const AppendParams& p, int head_dim, bool fp8, cudaStream_t stream) {
@@ -128,8 +137,8 @@ cudaError_t launch_kv_append(const AppendParams& p, int head_dim, bool fp8, cuda
 
 cudaError_t launch_combine(const CombineParams& p, int num_items, int head_dim, cudaStream_t stream) {
   if (num_items == 0) return cudaSuccess;
-  if (head_dim == 128) combine_kernel<128><<<num_items, 128, 0, stream>>>(p);
-  else combine_kernel<64><<<num_items, 64, 0, stream>>>(p);
+  if (head_dim == 128) combine_kernel<128><<<num_items, kDecodeRows * 128 / 8, 0, stream>>>(p);
+  else combine_kernel<64><<<num_items, kDecodeRows * 64 / 8, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -129,105 +129,118 @@ struct Ring {
 };
 
 // ------------------------------------------------------------------ producer
-// Issues K of tile j+1 before V of tile j, so that S = Q K^T of the next tile
-// never waits behind the V ring.
-struct TileRef {
-  int b, hk, t0, kv_end;
-};
-
-template <int D, bool FP8>
-__device__ __forceinline__ void load_tile(const AttnParams& p, const CUtensorMap* tm, uint8_t* dst, uint64_t* bar,
-                                          const TileRef& t) {
-  using L = Layout<D, FP8>;
-  const int32_t* bt = p.block_table + (int64_t)t.b * p.bt_stride;
-  mbar_arrive_expect_tx(bar, L::kTileBytes);
-#pragma unroll 1
-  for (int g = 0; g < kKvTile / kBoxRows; ++g) {
-    const int j0 = t.t0 + g * kBoxRows;
-    int page = p.num_pages, slot = 0;  // out of range: the copy fills zeros
-    if (j0 < t.kv_end) {
-      if (p.page_size > 0) {
-        page = __ldg(bt + j0 / p.page_size);
-        slot = j0 % p.page_size;
-        if (page < 0 || page >= p.num_pages) {
-          record_status(p.status, PKV_ERR_DEVICE_BOUNDS, t.b, page);
-          page = p.num_pages;
-          slot = 0;
-        }
-      } else {
-        page = t.b;
-        slot = j0;
-      }
-    }
-#pragma unroll
-    for (int c = 0; c < L::kChunks; ++c)
-      tma_load_4d(dst + c * (kKvTile * 128) + g * (kBoxRows * 128), tm, bar, c * (128 / L::kEsize), t.hk, slot,
-                  page);
-  }
-}
-
+// The whole warp issues: lane l owns the 16-row box of group (l % 8) and
+// 128-byte column chunk (l / 8) of every tile, so the 8 block_table reads of a
+// tile are one coalesced load instead of 8 dependent ones.  K of tile j+1 is
+// issued before V of tile j, so that S = Q K^T of the next tile never waits
+// behind the V ring.
 template <int D, bool FP8>
 __device__ void producer(const AttnParams& p, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                          const CUtensorMap* tm_q, uint8_t* smem, const Bars& B, volatile int* abort_flag, int it0,
                          int it1) {
   using L = Layout<D, FP8>;
-  tma_prefetch_desc(tm_k);
-  tma_prefetch_desc(tm_v);
+  constexpr int kGroups = kKvTile / kBoxRows;
+  const int lane = threadIdx.x & 31;
+  const int grp = lane % kGroups, chunk = lane / kGroups;
+  const bool active = chunk < L::kChunks;
+  if (lane == 0) {
+    tma_prefetch_desc(tm_k);
+    tma_prefetch_desc(tm_v);
+  }
   Ring rk, rv;
   int issued_k = 0, issued_v = 0;
   uint32_t pi = 0;  // prefill items with at least one tile
   bool ok = true, pending = false;
-  TileRef pend{};
-  auto issue_v = [&](const TileRef& t) -> bool {
-    if (!mbar_wait(&B.empty_v[rv.stage], rv.phase ^ 1, abort_flag)) return false;
-    load_tile<D, FP8>(p, tm_v, smem + L::kVOff + rv.stage * L::kTileBytes, &B.full_v[rv.stage], t);
+  int pend_page = 0, pend_slot = 0, pend_hk = 0;
+
+  // this lane's box of a tile: page and slot (an out-of-range page fills zeros)
+  auto locate = [&](const WorkItem& w, int t0, int& page, int& slot) {
+    const int j0 = t0 + grp * kBoxRows;
+    page = p.num_pages;
+    slot = 0;
+    if (j0 < w.kv_end) {
+      if (p.page_size > 0) {
+        const int pg = __ldg(p.block_table + (int64_t)w.b * p.bt_stride + j0 / p.page_size);
+        if (pg < 0 || pg >= p.num_pages) {
+          if (active) record_status(p.status, PKV_ERR_DEVICE_BOUNDS, w.b, pg);
+        } else {
+          page = pg;
+          slot = j0 % p.page_size;
+        }
+      } else {
+        page = w.b;
+        slot = j0;
+      }
+    }
+  };
+  auto issue_v = [&]() -> bool {
+    if (!warp_wait(&B.empty_v[rv.stage], rv.phase ^ 1, abort_flag)) return false;
+    if (lane == 0) mbar_arrive_expect_tx(&B.full_v[rv.stage], L::kTileBytes);
+    __syncwarp();
+    if (active)
+      tma_load_4d(smem + L::kVOff + rv.stage * L::kTileBytes + chunk * (kKvTile * 128) + grp * (kBoxRows * 128),
+                  tm_v, &B.full_v[rv.stage], chunk * (128 / L::kEsize), pend_hk, pend_slot, pend_page);
     ++issued_v;
     rv.advance<L::kStagesV>();
     return true;
   };
+
   for (int it = it0; it < it1 && ok; ++it) {
     const WorkItem w = p.items[it];
     if (L::kTc && w.kind == kPrefill && num_tiles(w) > 0) {
-      if (!mbar_wait(B.q_empty, (pi & 1) ^ 1, abort_flag)) {
+      if (!warp_wait(B.q_empty, (pi & 1) ^ 1, abort_flag)) {
         ok = false;
         break;
       }
-      const int tq = kPrefillRowsTc / p.G;
-      mbar_arrive_expect_tx(B.q_full, (uint32_t)((D / 64) * p.G * tq * 128));
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_3d(smem + L::kQOff + c * (kKvTile * 128), tm_q, B.q_full, c * 64, w.hk * p.G, w.q_row0);
+      if (lane == 0) {
+        if (pi == 0) tma_prefetch_desc(tm_q);
+        const int tq = kPrefillRowsTc / p.G;
+        mbar_arrive_expect_tx(B.q_full, (uint32_t)((D / 64) * p.G * tq * 128));
+      }
+      __syncwarp();
+      if (lane < D / 64)
+        tma_load_3d(smem + L::kQOff + lane * (kKvTile * 128), tm_q, B.q_full, lane * 64, w.hk * p.G, w.q_row0);
       ++pi;
     }
     for (int t0 = w.kv_begin; t0 < w.kv_end; t0 += kKvTile) {
-      const TileRef cur{w.b, w.hk, t0, w.kv_end};
-      if (!mbar_wait(&B.empty_k[rk.stage], rk.phase ^ 1, abort_flag)) {
+      int page, slot;
+      locate(w, t0, page, slot);  // block_table read overlaps the wait below
+      if (!warp_wait(&B.empty_k[rk.stage], rk.phase ^ 1, abort_flag)) {
         ok = false;
         break;
       }
-      load_tile<D, FP8>(p, tm_k, smem + L::kKOff + rk.stage * L::kTileBytes, &B.full_k[rk.stage], cur);
+      if (lane == 0) mbar_arrive_expect_tx(&B.full_k[rk.stage], L::kTileBytes);
+      __syncwarp();
+      if (active)
+        tma_load_4d(smem + L::kKOff + rk.stage * L::kTileBytes + chunk * (kKvTile * 128) + grp * (kBoxRows * 128),
+                    tm_k, &B.full_k[rk.stage], chunk * (128 / L::kEsize), w.hk, slot, page);
       ++issued_k;
       rk.advance<L::kStagesK>();
-      if (pending && !issue_v(pend)) {
+      if (pending && !issue_v()) {
         ok = false;
         break;
       }
-      pend = cur;
+      pend_page = page;
+      pend_slot = slot;
+      pend_hk = w.hk;
       pending = true;
     }
   }
-  if (ok && pending) ok = issue_v(pend);
+  if (ok && pending) ok = issue_v();
   if (!ok) {
-    record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, 0);
+    if (lane == 0) record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, 0);
     *abort_flag = 1;
     // let the copies already issued land before the CTA can exit (bounded)
-    int zero = 0;
-    const int nk = issued_k < L::kStagesK ? issued_k : L::kStagesK;
-    for (int k = issued_k - nk; k < issued_k; ++k)
-      mbar_wait(&B.full_k[k % L::kStagesK], (uint32_t)((k / L::kStagesK) & 1), &zero);
-    const int nv = issued_v < L::kStagesV ? issued_v : L::kStagesV;
-    for (int k = issued_v - nv; k < issued_v; ++k)
-      mbar_wait(&B.full_v[k % L::kStagesV], (uint32_t)((k / L::kStagesV) & 1), &zero);
+    if (lane == 0) {
+      int zero = 0;
+      const int nk = issued_k < L::kStagesK ? issued_k : L::kStagesK;
+      for (int k = issued_k - nk; k < issued_k; ++k)
+        mbar_wait(&B.full_k[k % L::kStagesK], (uint32_t)((k / L::kStagesK) & 1), &zero);
+      const int nv = issued_v < L::kStagesV ? issued_v : L::kStagesV;
+      for (int k = issued_v - nv; k < issued_v; ++k)
+        mbar_wait(&B.full_v[k % L::kStagesV], (uint32_t)((k / L::kStagesV) & 1), &zero);
+    }
+    __syncwarp();
   }
 }
 
@@ -322,7 +335,7 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
   for (int j = 0; j < n; ++j) {
     const uint32_t T = pt + j;
     const int t0 = w.kv_begin + j * kKvTile;
-    if (!mbar_wait(&B.s_full[T & 1], (T >> 1) & 1, abort_flag)) return false;
+    if (!warp_wait(&B.s_full[T & 1], (T >> 1) & 1, abort_flag)) return false;
     tc_fence_after();
     uint32_t s[128];
 #pragma unroll
@@ -362,11 +375,11 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
     m = m_new;
 
     // P buffer and O are free once the previous tile's P V has completed
-    if (j > 0 && !mbar_wait(B.o_done, (T - 1) & 1, abort_flag)) return false;
+    if (j > 0 && !warp_wait(B.o_done, (T - 1) & 1, abort_flag)) return false;
     tc_fence_after();
     if (t0 + kKvTile > w.lk) {
       // rows past the sequence may hold anything (even NaN): zero them in V
-      if (!mbar_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
+      if (!warp_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
       if (t0 + r >= w.lk) {
         uint8_t* vrow = smem + L::kVOff + rv.stage * L::kTileBytes + r * 128;
 #pragma unroll
@@ -401,7 +414,7 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
   // epilogue: O / l -> bf16 rows, natural-log LSE
   __nv_bfloat16* dst = p.out + (int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head;
   if (n > 0) {
-    if (!mbar_wait(B.o_done, (pt + n - 1) & 1, abort_flag)) return false;
+    if (!warp_wait(B.o_done, (pt + n - 1) & 1, abort_flag)) return false;
     tc_fence_after();
     const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
@@ -484,7 +497,7 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
   for (int t0 = w.kv_begin; t0 < w.kv_end; t0 += kKvTile) {
-    if (!mbar_wait(&B.full_k[rk.stage], rk.phase, abort_flag)) return false;
+    if (!warp_wait(&B.full_k[rk.stage], rk.phase, abort_flag)) return false;
     uint8_t* stage_k = smem + L::kKOff + rk.stage * L::kTileBytes;
     uint8_t* stage_v = smem + L::kVOff + rv.stage * L::kTileBytes;
     uint32_t kb, vb;
@@ -494,7 +507,7 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
       dequant_tile(stage_k, dk, ctid);
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.empty_k[rk.stage]);
-      if (!mbar_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
+      if (!warp_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
       dequant_tile(stage_v, dv, ctid);
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.empty_v[rv.stage]);
@@ -574,7 +587,7 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
 
     // O += P V
     if constexpr (!FP8) {
-      if (!mbar_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
+      if (!warp_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
     }
     const bool vmask = t0 + kKvTile > w.lk;  // rows past the sequence may hold anything: zero them
 #pragma unroll
@@ -779,7 +792,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = L::kTc ? *tmem_slot : 0u;
   const int it0 = p.cta_begin[blockIdx.x], it1 = p.cta_begin[blockIdx.x + 1];
   if (warp == 0) {
-    if (lane == 0) producer<D, FP8>(p, &tm_k, &tm_v, &tm_q, smem, B, abort_flag, it0, it1);
+    producer<D, FP8>(p, &tm_k, &tm_v, &tm_q, smem, B, abort_flag, it0, it1);
     return;
   }
   if (warp == 1) {
