@@ -193,6 +193,30 @@ pkv_status pkv_attn_varlen_kvcache_fwd(const pkv_problem* problem, const pkv_fwd
                                        size_t workspace_bytes, void* stream);
 
 /*
+ * pkv_attn_varlen_kvcache_fwd_noalloc -- the same call as
+ * pkv_attn_varlen_kvcache_fwd for callers that cannot provide a device
+ * workspace: hosts whose device memory is owned by their own pool and may not
+ * be allocated from, latency-critical loops that must not call cudaMalloc
+ * (it synchronises the device), or bindings without an allocator.  (The pages
+ * have no counterpart; this is an interface convenience of this library.)
+ * The work list, split-KV partials and status word live in a fixed 32 MiB
+ * device array that every GPU loading the library reserves until the process
+ * exits; the entry point allocates nothing and frees nothing.  It uploads the
+ * plan into that array and then runs the call on `stream`.
+ *  - The first call on a device resolves the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - A plan needing more than 32 MiB of workspace is rejected with
+ *    PKV_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ *  - Every call on a device shares the one array: calls that overlap on the
+ *    GPU (other streams, other host threads) race and must be serialised by
+ *    the caller.  Each call rewrites what it reads, including the status word.
+ *  - The device status word of these calls is not readable by pkv_get_status.
+ */
+pkv_status pkv_attn_varlen_kvcache_fwd_noalloc(const pkv_problem* problem, const pkv_fwd_args* args,
+                                               pkv_plan_t plan, void* stream);
+
+/*
  * pkv_kv_append -- in-place append alone (flash-attention PR, Usage: "kv cache
  * will be updated in-place"; TE PR: paged / non-paged bshd caches).  Writes
  * token t of sequence b (t < new_len[b], new_len from cu_seqlens_knew) to

@@ -25,7 +25,8 @@ STATUS_NAMES = {
 
 # every symbol the header declares
 EXPORTED = ["pkv_plan", "pkv_plan_upload", "pkv_plan_get_stats", "pkv_plan_get_items", "pkv_attn_varlen_kvcache_fwd", "pkv_kv_append",
-            "pkv_get_status", "pkv_plan_destroy", "pkv_last_error", "pkv_version", "pkv_set_profile_events"]
+            "pkv_get_status", "pkv_plan_destroy", "pkv_last_error", "pkv_version", "pkv_set_profile_events",
+            "pkv_attn_varlen_kvcache_fwd_noalloc"]
 
 
 class PkvError(RuntimeError):
@@ -86,12 +87,14 @@ def lib() -> ctypes.CDLL:
         L.pkv_kv_append.argtypes = [ctypes.POINTER(Problem), ctypes.POINTER(FwdArgs), i32, vp, vp]
         L.pkv_get_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
         L.pkv_set_profile_events.argtypes = [vp, vp]
+        L.pkv_attn_varlen_kvcache_fwd_noalloc.argtypes = [ctypes.POINTER(Problem), ctypes.POINTER(FwdArgs), vp, vp]
         L.pkv_plan_destroy.argtypes = [vp]
         L.pkv_plan_destroy.restype = None
         L.pkv_last_error.restype = ctypes.c_char_p
         L.pkv_version.restype = ctypes.c_char_p
         for name in ("pkv_plan", "pkv_plan_upload", "pkv_plan_get_stats", "pkv_plan_get_items", "pkv_attn_varlen_kvcache_fwd",
-                     "pkv_kv_append", "pkv_get_status", "pkv_set_profile_events"):
+                     "pkv_kv_append", "pkv_get_status", "pkv_set_profile_events",
+                     "pkv_attn_varlen_kvcache_fwd_noalloc"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -210,6 +213,13 @@ def attn_varlen_kvcache_fwd(problem: Problem, args: FwdArgs, plan_: Plan, worksp
     _check(lib().pkv_attn_varlen_kvcache_fwd(ctypes.byref(problem), ctypes.byref(args), plan_.handle,
                                              workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                              _stream_handle(stream)))
+
+
+def attn_varlen_kvcache_fwd_noalloc(problem: Problem, args: FwdArgs, plan_: Plan, stream=None) -> None:
+    """The attention call without a caller workspace (for callers that cannot
+    allocate device memory); uses the library's fixed 32 MiB device scratch."""
+    _check(lib().pkv_attn_varlen_kvcache_fwd_noalloc(ctypes.byref(problem), ctypes.byref(args), plan_.handle,
+                                                     _stream_handle(stream)))
 
 
 def kv_append(problem: Problem, args: FwdArgs, total_new: int, device_status=None, stream=None) -> None:
