@@ -54,8 +54,9 @@ pkv_status cuda_fail(cudaError_t e, const char* what) {
   return fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-// 4-D map over a cache (D, Hkv, rows-per-page-or-seq, pages-or-batch), box of 16
-// rows and one 128-byte column chunk, 128-byte swizzle, zero fill outside.
+// 4-D map over a cache (D, Hkv, rows-per-page-or-seq, pages-or-batch); a box
+// is cache_box_rows() rows of one 128-byte column chunk, 128-byte swizzle, zero
+// fill outside the tensor.
 pkv_status make_cache_map(CUtensorMap* map, const pkv_problem& pr, const pkv_fwd_args& a, void* base) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
@@ -65,7 +66,7 @@ pkv_status make_cache_map(CUtensorMap* map, const pkv_problem& pr, const pkv_fwd
   cuuint64_t dims[4] = {(cuuint64_t)pr.head_dim, (cuuint64_t)pr.num_heads_kv, rows, (cuuint64_t)pr.num_pages};
   cuuint64_t strides[3] = {(cuuint64_t)a.kc_stride_head * es, (cuuint64_t)a.kc_stride_tok * es,
                            (cuuint64_t)a.kc_stride_page * es};
-  cuuint32_t box[4] = {(cuuint32_t)(128 / es), 1, (cuuint32_t)kBoxRows, 1};
+  cuuint32_t box[4] = {(cuuint32_t)(128 / es), 1, (cuuint32_t)cache_box_rows(pr.page_size, pr.cache_capacity), 1};
   if (pr.head_dim * es < 128) box[0] = (cuuint32_t)pr.head_dim;
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides,
@@ -262,6 +263,7 @@ extern "C" pkv_status pkv_attn_varlen_kvcache_fwd(const pkv_problem* problem, co
   p.block_table = args->block_table;
   p.bt_stride = args->block_table_stride;
   p.page_size = pr.page_size;
+  p.box_rows = cache_box_rows(pr.page_size, pr.cache_capacity);
   p.num_pages = pr.num_pages;
   p.G = pr.num_heads_q / pr.num_heads_kv;
   p.causal = pr.causal;

@@ -4,9 +4,9 @@
 // "[Refactor] Uniform PoDAttention API with Horizontal Fusion SMs Schedule",
 // Key Changes 2: prefill and decode work share one persistent launch).
 //
-// Warp roles (192 threads):
-//   warp 0      TMA producer: K/V tiles of 128 keys, one 16-row box per
-//               (page, 128-byte column chunk), page numbers read from
+// Warp roles (224 threads):
+//   warps 0, 6  TMA producers (K and Q; V): tiles of 128 keys, boxes of up to
+//               128 rows per (page, 128-byte column chunk), page numbers read from
 //               block_table (vLLM PR "[Kernel][Triton][FP8] ...", review:
 //               block_table support; TransformerEngine PR "Add KV cache for
 //               paged/non-paged attention": one table for K and V, bshd pages)
@@ -34,35 +34,41 @@ namespace pkv {
 
 namespace {
 
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = 32 * (2 + kConsumerWarps);
+constexpr int kConsumerWarps = 4;                  // warp-MMA consumers (decode, fp8 prefill): warps 2..5
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr float kLn2 = 0.693147180559945309f;
-constexpr uint32_t kTmemCols = 512;   // S0 [0,128), S1 [128,256), O [256, 256+D)
+// Tensor memory: S buffers [0,128) and [128,256) (fp32), O [256, 256+D) (fp32),
+// P buffers [384,448) and [448,512) (bf16 pairs: 128 keys in 64 columns).
+constexpr uint32_t kTmemCols = 512;
+constexpr int kSBufs = 2;             // S = Q K^T of tile j+2 is issued before P V of tile j
 constexpr uint32_t kTmemO = 256;
+constexpr uint32_t kTmemP = 384;
 
 template <int D, bool FP8>
 struct Layout {
   static constexpr bool kTc = !FP8;                        // tensor-core (tcgen05) prefill tiles
+  // softmax warps of a tensor-core prefill tile: one per TMEM lane quarter (warps 2..5)
+  static constexpr int kSoftmaxWarps = kConsumerWarps;
+  static constexpr int kVProducerWarp = 2 + kSoftmaxWarps;   // after the consumer warps
+  static constexpr int kThreads = 32 * (3 + kSoftmaxWarps);
   static constexpr int kEsize = FP8 ? 1 : 2;
-  static constexpr int kStagesK = (FP8 || D == 128) ? 3 : 4;  // K ring (released after S = Q K^T)
-  static constexpr int kStagesV = (FP8 || D == 128) ? (FP8 ? 3 : 2) : 4;  // V ring (released after O += P V)
+  static constexpr int kStagesK = FP8 ? 4 : (D == 128 ? 3 : 4);  // K ring (released after S = Q K^T)
+  static constexpr int kStagesV = FP8 ? 4 : (D == 128 ? 3 : 4);  // V ring (released after O += P V)
   static constexpr int kTileBytes = kKvTile * D * kEsize;   // one raw K (or V) tile
   static constexpr int kChunks = D * kEsize / 128;            // 128-byte column chunks per cache row
-  static constexpr int kBf16Tile = kKvTile * D * 2;
   static constexpr int kKOff = 0;                             // K ring
   static constexpr int kVOff = kStagesK * kTileBytes;         // V ring
   static constexpr int kQOff = kVOff + kStagesV * kTileBytes; // tcgen05 path: Q tile (128 x D bf16)
-  static constexpr int kDeqOff = kQOff + (kTc ? kKvTile * D * 2 : 0);  // fp8: bf16 copies of K and V
-  static constexpr int kPOff = kDeqOff + (FP8 ? 2 * kBf16Tile : 0);    // P (128 x 128 bf16) / decode merge
+  // decode merge scratch: the fp8 layout has its own; the bf16 layout borrows
+  // the item's last V stage (as large as the scratch) before releasing it
   static constexpr int kMergeBytes = kConsumerWarps * kDecodeRows * D * 4;
-  static constexpr int kPBytes = kTc ? (kMergeBytes > 32768 ? kMergeBytes : 32768) : kMergeBytes;
-  static constexpr int kMlOff = kPOff + kPBytes;              // float[4][16][2]: (m, l)
+  static constexpr int kMergeOff = kQOff + (kTc ? kKvTile * D * 2 : 0);
+  static constexpr int kMlOff = kMergeOff + (FP8 ? kMergeBytes : 0);  // float[4][16][2]: (m, l)
   static constexpr int kBarOff = kMlOff + kConsumerWarps * kDecodeRows * 2 * 4;
-  static constexpr int kNumBars = 2 * kStagesK + 2 * kStagesV + 9;
+  static constexpr int kNumBars = 2 * kStagesK + 2 * kStagesV + 3 + 2 * kSBufs + 4;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;     // tmem base, abort flag
   static constexpr int kBytes = kMiscOff + 16;
-  static constexpr int kAlloc = kBytes + 1024;                // room to align the base to 1024
+  static constexpr int kAlloc = kBytes;                       // base is 1024-aligned (checked in the kernel)
 };
 
 struct Bars {
@@ -72,10 +78,10 @@ struct Bars {
   uint64_t* empty_v;
   uint64_t* q_full;
   uint64_t* q_empty;
-  uint64_t* s_full;   // [2]
-  uint64_t* s_free;   // [2]
-  uint64_t* p_full;
-  uint64_t* o_done;
+  uint64_t* s_full;   // [kSBufs] S of a tile is in TMEM
+  uint64_t* s_free;   // [kSBufs] the softmax has read it
+  uint64_t* p_full;   // [2] P of a tile is in shared memory (and O rescaled)
+  uint64_t* o_done;   // [2] P V of a tile has completed
   uint64_t* drain;    // MMA completion before tensor memory is freed after an abort
 };
 
@@ -93,27 +99,6 @@ __device__ __forceinline__ int num_tiles(const WorkItem& w) {
   return w.kv_end > w.kv_begin ? (w.kv_end - w.kv_begin + kKvTile - 1) / kKvTile : 0;
 }
 
-// fp8 K or V tile (128 rows x 128 codes, swizzled) -> bf16 tile in the layout above.
-__device__ __forceinline__ void dequant_tile(const uint8_t* raw, uint8_t* dst, int ctid) {
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int u = ctid + kConsumerThreads * k;
-    const int r = u >> 3, c = u & 7;
-    const uint4 w = *reinterpret_cast<const uint4*>(raw + r * 128 + (((c ^ (r & 7))) << 4));
-    uint4 lo, hi;
-    lo.x = e4m3x2_to_bf16x2((uint16_t)(w.x & 0xFFFF));
-    lo.y = e4m3x2_to_bf16x2((uint16_t)(w.x >> 16));
-    lo.z = e4m3x2_to_bf16x2((uint16_t)(w.y & 0xFFFF));
-    lo.w = e4m3x2_to_bf16x2((uint16_t)(w.y >> 16));
-    hi.x = e4m3x2_to_bf16x2((uint16_t)(w.z & 0xFFFF));
-    hi.y = e4m3x2_to_bf16x2((uint16_t)(w.z >> 16));
-    hi.z = e4m3x2_to_bf16x2((uint16_t)(w.w & 0xFFFF));
-    hi.w = e4m3x2_to_bf16x2((uint16_t)(w.w >> 16));
-    *reinterpret_cast<uint4*>(dst + tile_off(r, 2 * c)) = lo;
-    *reinterpret_cast<uint4*>(dst + tile_off(r, 2 * c + 1)) = hi;
-  }
-}
-
 struct Ring {
   int stage = 0;
   uint32_t phase = 0;
@@ -128,66 +113,36 @@ struct Ring {
   }
 };
 
-// ------------------------------------------------------------------ producer
-// The whole warp issues: lane l owns the 16-row box of group (l % 8) and
-// 128-byte column chunk (l / 8) of every tile, so the 8 block_table reads of a
-// tile are one coalesced load instead of 8 dependent ones.  K of tile j+1 is
-// issued before V of tile j, so that S = Q K^T of the next tile never waits
-// behind the V ring.
-template <int D, bool FP8>
-__device__ void producer(const AttnParams& p, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
-                         const CUtensorMap* tm_q, uint8_t* smem, const Bars& B, volatile int* abort_flag, int it0,
-                         int it1) {
+// ------------------------------------------------------------------ producers
+// Two producer warps, one per ring: warp 0 loads Q tiles and K tiles, the last
+// warp loads V tiles, each as soon as a stage of its own ring is free.  The
+// whole warp issues: lane l owns box (l % boxes) of 128-byte column chunk
+// (l / boxes) of every tile, where a tile of 128 keys is `boxes` boxes of
+// box_rows cache rows (128 for a contiguous cache, the largest power of two
+// dividing the page size for a paged one), so the block_table reads of a tile
+// are one coalesced load.
+template <int D, bool FP8, bool kIsV>
+__device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CUtensorMap* tm_q, uint8_t* smem,
+                         const Bars& B, volatile int* abort_flag, int it0, int it1) {
   using L = Layout<D, FP8>;
-  constexpr int kGroups = kKvTile / kBoxRows;
+  constexpr int kStages = kIsV ? L::kStagesV : L::kStagesK;
+  uint64_t* full = kIsV ? B.full_v : B.full_k;
+  uint64_t* empty = kIsV ? B.empty_v : B.empty_k;
+  uint8_t* ring_base = smem + (kIsV ? L::kVOff : L::kKOff);
   const int lane = threadIdx.x & 31;
-  const int grp = lane % kGroups, chunk = lane / kGroups;
+  const int boxes = kKvTile / p.box_rows;
+  const int grp = lane % boxes, chunk = lane / boxes;
   const bool active = chunk < L::kChunks;
-  if (lane == 0) {
-    tma_prefetch_desc(tm_k);
-    tma_prefetch_desc(tm_v);
-  }
-  Ring rk, rv;
-  int issued_k = 0, issued_v = 0;
+  const int box_off = chunk * (kKvTile * 128) + grp * (p.box_rows * 128);
+  if (lane == 0) tma_prefetch_desc(tm_kv);
+  Ring ring;
+  int issued = 0;
   uint32_t pi = 0;  // prefill items with at least one tile
-  bool ok = true, pending = false;
-  int pend_page = 0, pend_slot = 0, pend_hk = 0;
-
-  // this lane's box of a tile: page and slot (an out-of-range page fills zeros)
-  auto locate = [&](const WorkItem& w, int t0, int& page, int& slot) {
-    const int j0 = t0 + grp * kBoxRows;
-    page = p.num_pages;
-    slot = 0;
-    if (j0 < w.kv_end) {
-      if (p.page_size > 0) {
-        const int pg = __ldg(p.block_table + (int64_t)w.b * p.bt_stride + j0 / p.page_size);
-        if (pg < 0 || pg >= p.num_pages) {
-          if (active) record_status(p.status, PKV_ERR_DEVICE_BOUNDS, w.b, pg);
-        } else {
-          page = pg;
-          slot = j0 % p.page_size;
-        }
-      } else {
-        page = w.b;
-        slot = j0;
-      }
-    }
-  };
-  auto issue_v = [&]() -> bool {
-    if (!warp_wait(&B.empty_v[rv.stage], rv.phase ^ 1, abort_flag)) return false;
-    if (lane == 0) mbar_arrive_expect_tx(&B.full_v[rv.stage], L::kTileBytes);
-    __syncwarp();
-    if (active)
-      tma_load_4d(smem + L::kVOff + rv.stage * L::kTileBytes + chunk * (kKvTile * 128) + grp * (kBoxRows * 128),
-                  tm_v, &B.full_v[rv.stage], chunk * (128 / L::kEsize), pend_hk, pend_slot, pend_page);
-    ++issued_v;
-    rv.advance<L::kStagesV>();
-    return true;
-  };
+  bool ok = true;
 
   for (int it = it0; it < it1 && ok; ++it) {
     const WorkItem w = p.items[it];
-    if (L::kTc && w.kind == kPrefill && num_tiles(w) > 0) {
+    if (!kIsV && L::kTc && w.kind == kPrefill && num_tiles(w) > 0) {
       if (!warp_wait(B.q_empty, (pi & 1) ^ 1, abort_flag)) {
         ok = false;
         break;
@@ -203,48 +158,54 @@ __device__ void producer(const AttnParams& p, const CUtensorMap* tm_k, const CUt
       ++pi;
     }
     for (int t0 = w.kv_begin; t0 < w.kv_end; t0 += kKvTile) {
-      int page, slot;
-      locate(w, t0, page, slot);  // block_table read overlaps the wait below
-      if (!warp_wait(&B.empty_k[rk.stage], rk.phase ^ 1, abort_flag)) {
+      // this lane's box: page and slot (an out-of-range page fills zeros); the
+      // block_table read overlaps the wait below
+      const int j0 = t0 + grp * p.box_rows;
+      int page = p.num_pages, slot = 0;
+      if (j0 < w.kv_end) {
+        if (p.page_size > 0) {
+          const int pg = __ldg(p.block_table + (int64_t)w.b * p.bt_stride + j0 / p.page_size);
+          if (pg < 0 || pg >= p.num_pages) {
+            if (active && !kIsV) record_status(p.status, PKV_ERR_DEVICE_BOUNDS, w.b, pg);
+          } else {
+            page = pg;
+            slot = j0 % p.page_size;
+          }
+        } else {
+          page = w.b;
+          slot = j0;
+        }
+      }
+      if (!warp_wait(&empty[ring.stage], ring.phase ^ 1, abort_flag)) {
         ok = false;
         break;
       }
-      if (lane == 0) mbar_arrive_expect_tx(&B.full_k[rk.stage], L::kTileBytes);
+      if (lane == 0) mbar_arrive_expect_tx(&full[ring.stage], L::kTileBytes);
       __syncwarp();
       if (active)
-        tma_load_4d(smem + L::kKOff + rk.stage * L::kTileBytes + chunk * (kKvTile * 128) + grp * (kBoxRows * 128),
-                    tm_k, &B.full_k[rk.stage], chunk * (128 / L::kEsize), w.hk, slot, page);
-      ++issued_k;
-      rk.advance<L::kStagesK>();
-      if (pending && !issue_v()) {
-        ok = false;
-        break;
-      }
-      pend_page = page;
-      pend_slot = slot;
-      pend_hk = w.hk;
-      pending = true;
+        tma_load_4d(ring_base + ring.stage * L::kTileBytes + box_off, tm_kv, &full[ring.stage],
+                    chunk * (128 / L::kEsize), w.hk, slot, page);
+      ++issued;
+      ring.advance<kStages>();
     }
   }
-  if (ok && pending) ok = issue_v();
   if (!ok) {
-    if (lane == 0) record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, 0);
+    if (lane == 0) record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, kIsV ? 2 : 1);
     *abort_flag = 1;
     // let the copies already issued land before the CTA can exit (bounded)
     if (lane == 0) {
       int zero = 0;
-      const int nk = issued_k < L::kStagesK ? issued_k : L::kStagesK;
-      for (int k = issued_k - nk; k < issued_k; ++k)
-        mbar_wait(&B.full_k[k % L::kStagesK], (uint32_t)((k / L::kStagesK) & 1), &zero);
-      const int nv = issued_v < L::kStagesV ? issued_v : L::kStagesV;
-      for (int k = issued_v - nv; k < issued_v; ++k)
-        mbar_wait(&B.full_v[k % L::kStagesV], (uint32_t)((k / L::kStagesV) & 1), &zero);
+      const int n = issued < kStages ? issued : kStages;
+      for (int k = issued - n; k < issued; ++k) mbar_wait(&full[k % kStages], (uint32_t)((k / kStages) & 1), &zero);
     }
     __syncwarp();
   }
 }
 
 // ------------------------------------------------------------------ MMA issuer (prefill tiles)
+// Order per item with n tiles: S_0, S_1, then for each j: S_{j+2}, P_j V_j.
+// S_{j+2} needs S buffer j % 2 read by the softmax of tile j; P_j V_j needs
+// P_j (tensor-memory buffer j % 2, written by the softmax) and V_j.
 template <int D>
 __device__ bool mma_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, volatile int* abort_flag,
                            uint32_t tmem, int it0, int it1) {
@@ -252,22 +213,39 @@ __device__ bool mma_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, vo
   constexpr uint32_t kIdescQK = idesc_f16(1, 0, 128, 128);
   constexpr uint32_t kIdescPV = idesc_f16(1, 1, 128, D);
   const uint32_t q_base = smem_u32(smem + L::kQOff);
-  const uint32_t p_base = smem_u32(smem + L::kPOff);
   Ring rk, rv;
   uint32_t pt = 0, pi = 0;
 
-  auto do_pv = [&](uint32_t T, bool first) -> bool {
-    if (!mbar_wait(B.p_full, T & 1, abort_flag)) return false;
+  auto issue_s = [&](uint32_t T) -> bool {
+    const uint32_t b = T % kSBufs, use = T / kSBufs;
+    if (!mbar_wait(&B.full_k[rk.stage], rk.phase, abort_flag)) return false;
+    if (use >= 1 && !mbar_wait(&B.s_free[b], (use - 1) & 1, abort_flag)) return false;
+    tc_fence_after();
+    const uint32_t k_base = smem_u32(smem + L::kKOff + rk.stage * L::kTileBytes);
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+      const uint32_t off = (k >> 2) * (kKvTile * 128) + (k & 3) * 32;
+      umma_ss(tmem + b * 128, sdesc_sw128(q_base + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024), kIdescQK,
+              k > 0 ? 1u : 0u);
+    }
+    umma_commit(&B.s_full[b]);
+#pragma unroll
+    for (int i = 0; i < kConsumerWarps; ++i) umma_commit(&B.empty_k[rk.stage]);
+    rk.advance<L::kStagesK>();
+    return true;
+  };
+  auto issue_pv = [&](uint32_t T, bool first) -> bool {
+    if (!mbar_wait(&B.p_full[T & 1], (T >> 1) & 1, abort_flag)) return false;
     if (!mbar_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
     tc_fence_after();
+    const uint32_t p_tmem = tmem + kTmemP + (T & 1) * 64;
     const uint32_t v_base = smem_u32(smem + L::kVOff + rv.stage * L::kTileBytes);
 #pragma unroll
     for (int k = 0; k < kKvTile / 16; ++k) {
-      const uint64_t a = sdesc_sw128(p_base + (k >> 2) * (kKvTile * 128) + (k & 3) * 32, 16, 1024);
-      const uint64_t b = sdesc_sw128(v_base + k * 16 * 128, kKvTile * 128, 1024);
-      umma_ss(tmem + kTmemO, a, b, kIdescPV, (first && k == 0) ? 0u : 1u);
+      const uint64_t bd = sdesc_sw128(v_base + k * 16 * 128, kKvTile * 128, 1024);
+      umma_ts(tmem + kTmemO, p_tmem + k * 8, bd, kIdescPV, (first && k == 0) ? 0u : 1u);
     }
-    umma_commit(B.o_done);
+    umma_commit(&B.o_done[T & 1]);
 #pragma unroll
     for (int i = 0; i < kConsumerWarps; ++i) umma_commit(&B.empty_v[rv.stage]);
     rv.advance<L::kStagesV>();
@@ -284,26 +262,17 @@ __device__ bool mma_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, vo
     }
     if (n == 0) continue;
     if (!mbar_wait(B.q_full, pi & 1, abort_flag)) return false;
+    const int ahead = n < 2 ? n : 2;
+    for (int j = 0; j < ahead; ++j)
+      if (!issue_s(pt + j)) return false;
+    if (ahead == n) umma_commit(B.q_empty);
     for (int j = 0; j < n; ++j) {
-      const uint32_t T = pt + j;
-      if (!mbar_wait(&B.full_k[rk.stage], rk.phase, abort_flag)) return false;
-      if (T >= 2 && !mbar_wait(&B.s_free[T & 1], ((T >> 1) & 1) ^ 1, abort_flag)) return false;
-      tc_fence_after();
-      const uint32_t k_base = smem_u32(smem + L::kKOff + rk.stage * L::kTileBytes);
-#pragma unroll
-      for (int k = 0; k < D / 16; ++k) {
-        const uint32_t off = (k >> 2) * (kKvTile * 128) + (k & 3) * 32;
-        umma_ss(tmem + (T & 1) * 128, sdesc_sw128(q_base + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024),
-                kIdescQK, k > 0 ? 1u : 0u);
+      if (j + 2 < n) {
+        if (!issue_s(pt + j + 2)) return false;
+        if (j + 2 == n - 1) umma_commit(B.q_empty);
       }
-      umma_commit(&B.s_full[T & 1]);
-#pragma unroll
-      for (int i = 0; i < kConsumerWarps; ++i) umma_commit(&B.empty_k[rk.stage]);
-      if (j == n - 1) umma_commit(B.q_empty);
-      rk.advance<L::kStagesK>();
-      if (j >= 1 && !do_pv(T - 1, j == 1)) return false;
+      if (!issue_pv(pt + j, j == 0)) return false;
     }
-    if (!do_pv(pt + n - 1, n == 1)) return false;
     pt += n;
     ++pi;
   }
@@ -311,6 +280,10 @@ __device__ bool mma_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, vo
 }
 
 // ------------------------------------------------------------------ prefill tile softmax (tcgen05 path)
+// Four warps, one query row per thread (TMEM lane), all 128 keys of a tile.
+// P of tile T goes to tensor-memory buffer T % 2, so it only waits for P V of
+// tile T-2; O is rescaled (which needs P V of tile T-1 done) only when a row's
+// running max moves.
 template <int D>
 __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, const Bars& B,
                              volatile int* abort_flag, uint32_t tmem, Ring& rk, Ring& rv, uint32_t& pt, float sl2) {
@@ -330,52 +303,61 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
   }
   const int n = num_tiles(w);
   float m = -INFINITY, l = 0.f;
-  uint8_t* pbuf = smem + L::kPOff;
 
   for (int j = 0; j < n; ++j) {
     const uint32_t T = pt + j;
     const int t0 = w.kv_begin + j * kKvTile;
-    if (!warp_wait(&B.s_full[T & 1], (T >> 1) & 1, abort_flag)) return false;
+    const uint32_t sb = T % kSBufs;
+    if (!warp_wait(&B.s_full[sb], (T / kSBufs) & 1, abort_flag)) return false;
     tc_fence_after();
     uint32_t s[128];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) tmem_ld32(t_lane + (T & 1) * 128 + c * 32, s + c * 32);
+    for (int c = 0; c < 4; ++c) tmem_ld32(t_lane + sb * 128 + c * 32, s + c * 32);
     tmem_wait_ld();
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&B.s_free[T & 1]);
+    if (lane == 0) mbar_arrive(&B.s_free[sb]);
 
-    // mask by select (rows past the sequence see nothing), row max
+    // mask by select (rows past the sequence see nothing), row max as a tree
     const bool need_mask = t0 + kKvTile > lim;
-    float mx = -INFINITY;
+    float mx8[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
     if (__any_sync(0xffffffffu, need_mask)) {
 #pragma unroll
       for (int c = 0; c < 128; ++c) {
         const float v = (t0 + c < lim) ? __uint_as_float(s[c]) : -INFINITY;
         s[c] = __float_as_uint(v);
-        mx = fmaxf(mx, v);
+        mx8[c & 7] = fmaxf(mx8[c & 7], v);
       }
     } else {
 #pragma unroll
-      for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+      for (int c = 0; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(s[c]));
     }
-    const float m_new = fmaxf(m, mx * sl2);
+    const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                           fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+    // The running max m only moves when the tile's max exceeds it by more than
+    // 2^8: probabilities then stay below 256, and l and O, both accumulated
+    // against the same m, still give the exact O / l and LSE = m + log2 l.
+    const float mx2 = mx * sl2;
+    const bool bump = mx2 > m + 8.f;
+    const float m_new = bump ? mx2 : m;
     const float mu = m_new == -INFINITY ? 0.f : m_new;
-    const float alpha = ex2(m - mu);
-    float sum = 0.f;
+    const float alpha = bump ? ex2(m - mu) : 1.f;
+    float sum4[4] = {0.f, 0.f, 0.f, 0.f};
     uint32_t pk[64];
 #pragma unroll
     for (int c = 0; c < 64; ++c) {
       const float p0 = ex2(fmaf(__uint_as_float(s[2 * c]), sl2, -mu));
       const float p1 = ex2(fmaf(__uint_as_float(s[2 * c + 1]), sl2, -mu));
-      sum += p0 + p1;
+      sum4[c & 3] += p0 + p1;
       pk[c] = pack_bf16(p0, p1);
     }
-    l = l * alpha + sum;
+    l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
     m = m_new;
 
-    // P buffer and O are free once the previous tile's P V has completed
-    if (j > 0 && !warp_wait(B.o_done, (T - 1) & 1, abort_flag)) return false;
+    // P buffer T % 2 is free once P V of tile T-2 has completed
+    if (j >= 2 && !warp_wait(&B.o_done[T & 1], ((T - 2) >> 1) & 1, abort_flag)) return false;
     tc_fence_after();
     if (t0 + kKvTile > w.lk) {
       // rows past the sequence may hold anything (even NaN): zero them in V
@@ -388,10 +370,12 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
           for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(vrow + c * (kKvTile * 128) + q * 16) = make_uint4(0, 0, 0, 0);
       }
     }
-#pragma unroll
-    for (int c = 0; c < 16; ++c)
-      *reinterpret_cast<uint4*>(pbuf + tile_off(r, c)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+    tmem_st32(t_lane + kTmemP + (T & 1) * 64, pk);
+    tmem_st32(t_lane + kTmemP + (T & 1) * 64 + 32, pk + 32);
     if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      // O must hold P V of tile T-1 before it is rescaled
+      if (!warp_wait(&B.o_done[(T - 1) & 1], ((T - 1) >> 1) & 1, abort_flag)) return false;
+      tc_fence_after();
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -401,12 +385,12 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
         for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
         tmem_st32(t_lane + kTmemO + c * 32, o);
       }
-      tmem_wait_st();
     }
-    fence_proxy_async_smem();
+    tmem_wait_st();
+    fence_proxy_async_smem();  // the zeroed V rows (generic stores) before the MMA reads them
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(B.p_full);
+    if (lane == 0) mbar_arrive(&B.p_full[T & 1]);
     rk.advance<L::kStagesK>();
     rv.advance<L::kStagesV>();
   }
@@ -414,7 +398,8 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
   // epilogue: O / l -> bf16 rows, natural-log LSE
   __nv_bfloat16* dst = p.out + (int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head;
   if (n > 0) {
-    if (!warp_wait(B.o_done, (pt + n - 1) & 1, abort_flag)) return false;
+    const uint32_t T = pt + n - 1;
+    if (!warp_wait(&B.o_done[T & 1], (T >> 1) & 1, abort_flag)) return false;
     tc_fence_after();
     const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
@@ -445,7 +430,7 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
   return true;
 }
 
-// ------------------------------------------------------------------ warp-MMA tiles (decode; fp8 prefill)
+// ------------------------------------------------------------------ warp-MMA tiles of a bf16 cache (decode)
 // KPW = keys of each 128-key tile handled by one warp: 32 (decode), 128 (prefill).
 template <int D, bool FP8, int KPW>
 __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, const Bars& B,
@@ -495,29 +480,14 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
 #pragma unroll
   for (int n = 0; n < NO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  int merge_stage = -1;
 
   for (int t0 = w.kv_begin; t0 < w.kv_end; t0 += kKvTile) {
     if (!warp_wait(&B.full_k[rk.stage], rk.phase, abort_flag)) return false;
     uint8_t* stage_k = smem + L::kKOff + rk.stage * L::kTileBytes;
     uint8_t* stage_v = smem + L::kVOff + rv.stage * L::kTileBytes;
-    uint32_t kb, vb;
-    if constexpr (FP8) {
-      uint8_t* dk = smem + L::kDeqOff;
-      uint8_t* dv = dk + L::kBf16Tile;
-      dequant_tile(stage_k, dk, ctid);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&B.empty_k[rk.stage]);
-      if (!warp_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
-      dequant_tile(stage_v, dv, ctid);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&B.empty_v[rv.stage]);
-      named_bar_sync(1, kConsumerThreads);
-      kb = smem_u32(dk);
-      vb = smem_u32(dv);
-    } else {
-      kb = smem_u32(stage_k);
-      vb = smem_u32(stage_v);
-    }
+    const uint32_t kb = smem_u32(stage_k);
+    const uint32_t vb = smem_u32(stage_v);
 
     // S = Q K^T over this warp's keys
     float s[NT][4];
@@ -536,10 +506,8 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
       }
     }
 
-    if constexpr (!FP8) {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&B.empty_k[rk.stage]);
-    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&B.empty_k[rk.stage]);
 
     // mask (select, never add) + online softmax in the log2 domain
     const int jb = t0 + kw0 + 2 * t;
@@ -586,9 +554,7 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
     }
 
     // O += P V
-    if constexpr (!FP8) {
-      if (!warp_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
-    }
+    if (!warp_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
     const bool vmask = t0 + kKvTile > w.lk;  // rows past the sequence may hold anything: zero them
 #pragma unroll
     for (int kk = 0; kk < KPW / 16; ++kk) {
@@ -615,11 +581,11 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
         mma_bf16(o[2 * dp + 1], a0, a1, a2, a3, b2, b3);
       }
     }
-    if constexpr (!FP8) {
+    if (kDecodeTile && t0 + kKvTile >= w.kv_end) {
+      merge_stage = rv.stage;  // released after the merge below, which uses it as scratch
+    } else {
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.empty_v[rv.stage]);
-    } else {
-      named_bar_sync(1, kConsumerThreads);  // bf16 copies free for the next tile
     }
     rk.advance<L::kStagesK>();
     rv.advance<L::kStagesV>();
@@ -632,8 +598,19 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
 
   if constexpr (kDecodeTile) {
+    if (merge_stage < 0) {
+      // no key at all: every row is 0 with LSE -inf
+      for (int idx = ctid; idx < R * D; idx += kConsumerThreads) {
+        const int row = idx / D, d = idx % D;
+        const int tok = w.q_row0 + row / p.G;
+        const int head = w.hk * p.G + row % p.G;
+        p.out[(int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head + d] = __float2bfloat16_rn(0.f);
+        if (d == 0 && p.lse != nullptr) p.lse[(int64_t)head * p.total_q + tok] = -INFINITY;
+      }
+      return true;
+    }
     float* ml = reinterpret_cast<float*>(smem + L::kMlOff);
-    float* mo = reinterpret_cast<float*>(smem + L::kPOff);
+    float* mo = reinterpret_cast<float*>(smem + L::kVOff + merge_stage * L::kTileBytes);
     if (t == 0) {
       ml[(cw * 16 + g) * 2 + 0] = m0;
       ml[(cw * 16 + g) * 2 + 1] = l0;
@@ -681,6 +658,10 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
       }
     }
     named_bar_sync(1, kConsumerThreads);
+    // the borrowed V stage goes back to the producer (generic writes before the next async copy)
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&B.empty_v[merge_stage]);
   } else {
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
@@ -704,12 +685,266 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
   return true;
 }
 
+// ------------------------------------------------------------------ fp8-cache tiles (warp MMA, f16)
+// e4m3 K and V are converted to f16 straight into MMA fragments (exact).
+// K: a dot product over d does not depend on the order of d, so the k slots
+// of k-step ks = 4*G + u map to d = 64G + 16t + 4u + {0,1 | 2,3} for both Q and
+// K, and each thread reads its 16 bytes of a key row with one 128-bit load.
+// V: ldmatrix.trans on byte pairs gives a thread (key 2t, 2t+1) x (d 2g, 2g+1);
+// a byte permute splits that into the fragment of column d = 2g (even O tile)
+// and of d = 2g+1 (odd O tile); the epilogue puts O columns back in order.
+template <int KPW>
+__device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* smem, const Bars& B,
+                             volatile int* abort_flag, Ring& rk, Ring& rv, float sl2, float vscale) {
+  using L = Layout<128, true>;
+  constexpr int D = 128;
+  constexpr int NT = KPW / 8;
+  constexpr bool kDecodeTile = (KPW != kKvTile);
+  const int lane = threadIdx.x & 31;
+  const int cw = (threadIdx.x >> 5) - 2;
+  const int ctid = threadIdx.x - 64;
+  const int g = lane >> 2, t = lane & 3;
+  const int row_blk = kDecodeTile ? 0 : cw;
+  const int kw0 = kDecodeTile ? cw * KPW : 0;
+  const int R = w.n_q * p.G;
+  const int r0 = row_blk * 16 + g, r1 = r0 + 8;
+  auto limit_of = [&](int r) {
+    if (r >= R) return w.kv_begin;
+    int lim = w.kv_end;
+    if (p.causal) lim = min(lim, w.q_i0 + r / p.G + w.lk - w.lq + 1);
+    return lim;
+  };
+  const int lim0 = limit_of(r0), lim1 = limit_of(r1);
+
+  uint32_t qa[8][4];
+  {
+    const __nv_bfloat16* q0 = nullptr;
+    const __nv_bfloat16* q1 = nullptr;
+    if (r0 < R)
+      q0 = p.q + (int64_t)(w.q_row0 + r0 / p.G) * p.q_stride_tok + (int64_t)(w.hk * p.G + r0 % p.G) * p.q_stride_head;
+    if (r1 < R)
+      q1 = p.q + (int64_t)(w.q_row0 + r1 / p.G) * p.q_stride_tok + (int64_t)(w.hk * p.G + r1 % p.G) * p.q_stride_head;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int d0 = 64 * (ks >> 2) + 16 * t + 4 * (ks & 3);
+      qa[ks][0] = q0 ? bf16x2_to_f16x2(ld_u32(q0 + d0)) : 0u;
+      qa[ks][1] = q1 ? bf16x2_to_f16x2(ld_u32(q1 + d0)) : 0u;
+      qa[ks][2] = q0 ? bf16x2_to_f16x2(ld_u32(q0 + d0 + 2)) : 0u;
+      qa[ks][3] = q1 ? bf16x2_to_f16x2(ld_u32(q1 + d0 + 2)) : 0u;
+    }
+  }
+
+  float o[16][4];
+#pragma unroll
+  for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+  for (int t0 = w.kv_begin; t0 < w.kv_end; t0 += kKvTile) {
+    if (!warp_wait(&B.full_k[rk.stage], rk.phase, abort_flag)) return false;
+    const uint32_t kraw = smem_u32(smem + L::kKOff + rk.stage * L::kTileBytes);
+    float s[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int key = kw0 + nt * 8 + g;
+#pragma unroll
+      for (int G = 0; G < 2; ++G) {
+        const uint4 kv = lds_u128(kraw + key * 128 + ((((4 * G + t) ^ (key & 7))) << 4));
+        const uint32_t wd[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int ks = 4 * G + u;
+          mma_f16(s[nt], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], e4m3x2_to_f16x2(wd[u]),
+                  e4m3x2_to_f16x2(wd[u] >> 16));
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&B.empty_k[rk.stage]);
+
+    const int jb = t0 + kw0 + 2 * t;
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int j = jb + n * 8 + e;
+        s[n][e] = j < lim0 ? s[n][e] * sl2 : -INFINITY;
+        s[n][2 + e] = j < lim1 ? s[n][2 + e] * sl2 : -INFINITY;
+        mx0 = fmaxf(mx0, s[n][e]);
+        mx1 = fmaxf(mx1, s[n][2 + e]);
+      }
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+    const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float al0 = ex2(m0 - mu0), al1 = ex2(m1 - mu1);
+    m0 = mn0;
+    m1 = mn1;
+    float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      s[n][0] = ex2(s[n][0] - mu0);
+      s[n][1] = ex2(s[n][1] - mu0);
+      s[n][2] = ex2(s[n][2] - mu1);
+      s[n][3] = ex2(s[n][3] - mu1);
+      ls0 += s[n][0] + s[n][1];
+      ls1 += s[n][2] + s[n][3];
+    }
+    l0 = l0 * al0 + ls0;
+    l1 = l1 * al1 + ls1;
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+      o[n][0] *= al0;
+      o[n][1] *= al0;
+      o[n][2] *= al1;
+      o[n][3] *= al1;
+    }
+
+    if (!warp_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
+    const uint32_t vraw = smem_u32(smem + L::kVOff + rv.stage * L::kTileBytes);
+    const bool vmask = t0 + kKvTile > w.lk;  // rows past the sequence may hold anything: zero them
+#pragma unroll
+    for (int kk = 0; kk < KPW / 16; ++kk) {
+      const uint32_t a0 = pack_f16(s[2 * kk][0], s[2 * kk][1]);
+      const uint32_t a1 = pack_f16(s[2 * kk][2], s[2 * kk][3]);
+      const uint32_t a2 = pack_f16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+      const uint32_t a3 = pack_f16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+      const int kbase = t0 + kw0 + kk * 16 + 2 * t;
+      const uint32_t mlo0 = (kbase < w.lk ? 0x0000FFFFu : 0u) | (kbase + 1 < w.lk ? 0xFFFF0000u : 0u);
+      const uint32_t mlo1 = (kbase + 8 < w.lk ? 0x0000FFFFu : 0u) | (kbase + 9 < w.lk ? 0xFFFF0000u : 0u);
+      const int mi = lane >> 3;
+      const int key = kw0 + kk * 16 + (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+      for (int db = 0; db < 4; ++db) {
+        const int chunk = 2 * db + (mi >> 1);
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_t(vraw + key * 128 + ((chunk ^ (key & 7)) << 4), v0, v1, v2, v3);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t va = h ? v2 : v0, vb = h ? v3 : v1;
+          uint32_t e0 = e4m3x2_to_f16x2(prmt(va, 0u, 0x0020u)), e1 = e4m3x2_to_f16x2(prmt(vb, 0u, 0x0020u));
+          uint32_t d0 = e4m3x2_to_f16x2(prmt(va, 0u, 0x0031u)), d1 = e4m3x2_to_f16x2(prmt(vb, 0u, 0x0031u));
+          if (vmask) {
+            e0 &= mlo0;
+            d0 &= mlo0;
+            e1 &= mlo1;
+            d1 &= mlo1;
+          }
+          mma_f16(o[4 * db + 2 * h], a0, a1, a2, a3, e0, e1);
+          mma_f16(o[4 * db + 2 * h + 1], a0, a1, a2, a3, d0, d1);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&B.empty_v[rv.stage]);
+    rk.advance<L::kStagesK>();
+    rv.advance<L::kStagesV>();
+  }
+
+  // epilogue.  O tile 4db+2h+par, column c holds d = 32db + 16h + 2c + par, so a
+  // thread's (even, odd) tile pair covers d = 32db + 16h + 4t + {0,1,2,3}.
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  if constexpr (kDecodeTile) {
+    float* ml = reinterpret_cast<float*>(smem + L::kMlOff);
+    float* mo = reinterpret_cast<float*>(smem + L::kMergeOff);
+    if (t == 0) {
+      ml[(cw * 16 + g) * 2 + 0] = m0;
+      ml[(cw * 16 + g) * 2 + 1] = l0;
+      ml[(cw * 16 + g + 8) * 2 + 0] = m1;
+      ml[(cw * 16 + g + 8) * 2 + 1] = l1;
+    }
+    named_bar_sync(1, kConsumerThreads);
+    float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll
+    for (int ww = 0; ww < kConsumerWarps; ++ww) {
+      M0 = fmaxf(M0, ml[(ww * 16 + g) * 2]);
+      M1 = fmaxf(M1, ml[(ww * 16 + g + 8) * 2]);
+    }
+    const float f0 = ex2(m0 - (M0 == -INFINITY ? 0.f : M0));
+    const float f1 = ex2(m1 - (M1 == -INFINITY ? 0.f : M1));
+#pragma unroll
+    for (int db = 0; db < 4; ++db)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float* e = o[4 * db + 2 * h];
+        const float* d = o[4 * db + 2 * h + 1];
+        const int col = 32 * db + 16 * h + 4 * t;
+        *reinterpret_cast<float4*>(mo + (cw * 16 + g) * D + col) =
+            make_float4(e[0] * f0, d[0] * f0, e[1] * f0, d[1] * f0);
+        *reinterpret_cast<float4*>(mo + (cw * 16 + g + 8) * D + col) =
+            make_float4(e[2] * f1, d[2] * f1, e[3] * f1, d[3] * f1);
+      }
+    named_bar_sync(1, kConsumerThreads);
+    for (int idx = ctid; idx < R * D; idx += kConsumerThreads) {
+      const int row = idx / D, dd = idx % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int ww = 0; ww < kConsumerWarps; ++ww) M = fmaxf(M, ml[(ww * 16 + row) * 2]);
+      const float Mu = M == -INFINITY ? 0.f : M;
+      float Lsum = 0.f, acc = 0.f;
+#pragma unroll
+      for (int ww = 0; ww < kConsumerWarps; ++ww) {
+        Lsum += ml[(ww * 16 + row) * 2 + 1] * ex2(ml[(ww * 16 + row) * 2] - Mu);
+        acc += mo[(ww * 16 + row) * D + dd];
+      }
+      const float val = Lsum > 0.f ? acc / Lsum * vscale : 0.f;
+      const float lse2 = Lsum > 0.f ? Mu + __log2f(Lsum) : -INFINITY;
+      if (w.partial >= 0) {
+        p.partial_o[((int64_t)w.partial * kDecodeRows + row) * D + dd] = val;
+        if (dd == 0) p.partial_lse[w.partial * kDecodeRows + row] = lse2;
+      } else {
+        const int tok = w.q_row0 + row / p.G;
+        const int head = w.hk * p.G + row % p.G;
+        p.out[(int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head + dd] = __float2bfloat16_rn(val);
+        if (dd == 0 && p.lse != nullptr) p.lse[(int64_t)head * p.total_q + tok] = lse2 * kLn2;
+      }
+    }
+    named_bar_sync(1, kConsumerThreads);
+  } else {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int r = half ? r1 : r0;
+      if (r >= R) continue;
+      const float l = half ? l1 : l0;
+      const float m = half ? m1 : m0;
+      const float inv = l > 0.f ? vscale / l : 0.f;
+      const int tok = w.q_row0 + r / p.G;
+      const int head = w.hk * p.G + r % p.G;
+      __nv_bfloat16* dst = p.out + (int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head;
+#pragma unroll
+      for (int db = 0; db < 4; ++db)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float* e = o[4 * db + 2 * h];
+          const float* d = o[4 * db + 2 * h + 1];
+          uint2 v;
+          v.x = pack_bf16(e[half * 2] * inv, d[half * 2] * inv);
+          v.y = pack_bf16(e[half * 2 + 1] * inv, d[half * 2 + 1] * inv);
+          *reinterpret_cast<uint2*>(dst + 32 * db + 16 * h + 4 * t) = v;
+        }
+      if (t == 0 && p.lse != nullptr)
+        p.lse[(int64_t)head * p.total_q + tok] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+    }
+  }
+  return true;
+}
+
 template <int D, bool FP8>
 __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, volatile int* abort_flag, uint32_t tmem,
                          int it0, int it1) {
   using L = Layout<D, FP8>;
   const int ctid = threadIdx.x - 64;
-  if (blockIdx.x == 0) {
+  const bool mma_consumer = ctid < kConsumerThreads;  // warps 2..5
+  if (blockIdx.x == 0 && mma_consumer) {
     for (int b = ctid; b < p.batch; b += kConsumerThreads)
       if (__ldg(p.cache_seqlens + b) != __ldg(p.plan_lc + b))
         record_status(p.status, PKV_ERR_PLAN_MISMATCH, b, __ldg(p.cache_seqlens + b));
@@ -721,13 +956,21 @@ __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
   uint32_t pt = 0;
   for (int it = it0; it < it1; ++it) {
     const WorkItem w = p.items[it];
-    bool ok;
+    bool ok = true;
     if (w.kind == kDecode) {
-      ok = run_item<D, FP8, kKvTile / kConsumerWarps>(p, w, smem, B, abort_flag, rk, rv, sl2, vscale);
+      if (mma_consumer) {
+        if constexpr (FP8)
+          ok = run_item_fp8<kKvTile / kConsumerWarps>(p, w, smem, B, abort_flag, rk, rv, sl2, vscale);
+        else
+          ok = run_item<D, FP8, kKvTile / kConsumerWarps>(p, w, smem, B, abort_flag, rk, rv, sl2, vscale);
+      } else {
+        rk.advance<L::kStagesK>(num_tiles(w));
+        rv.advance<L::kStagesV>(num_tiles(w));
+      }
     } else if constexpr (L::kTc) {
       ok = softmax_item<D>(p, w, smem, B, abort_flag, tmem, rk, rv, pt, sl2);
     } else {
-      ok = run_item<D, FP8, kKvTile>(p, w, smem, B, abort_flag, rk, rv, sl2, vscale);
+      ok = run_item_fp8<kKvTile>(p, w, smem, B, abort_flag, rk, rv, sl2, vscale);
     }
     if (!ok) {
       record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, it);
@@ -739,12 +982,17 @@ __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
 }
 
 template <int D, bool FP8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Layout<D, FP8>::kThreads, 1)
     attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q) {
   using L = Layout<D, FP8>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if ((smem_u32(smem_raw) & 1023) != 0) {
+    // the swizzled TMA / MMA layouts need a 1024-byte aligned base: refuse, never overrun
+    if (threadIdx.x == 0) record_status(p.status, PKV_ERR_UNSUPPORTED, blockIdx.x, (int)(smem_u32(smem_raw) & 1023));
+    return;
+  }
+  uint8_t* smem = smem_raw;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   Bars B;
   B.full_k = bars;
@@ -753,11 +1001,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   B.empty_v = bars + 2 * L::kStagesK + L::kStagesV;
   B.q_full = bars + 2 * L::kStagesK + 2 * L::kStagesV;
   B.q_empty = B.q_full + 1;
-  B.s_full = B.q_full + 2;
-  B.s_free = B.q_full + 4;
-  B.p_full = B.q_full + 6;
-  B.o_done = B.q_full + 7;
-  B.drain = B.q_full + 8;
+  B.drain = B.q_full + 2;
+  B.s_full = B.q_full + 3;
+  B.s_free = B.s_full + kSBufs;
+  B.p_full = B.s_free + kSBufs;
+  B.o_done = B.p_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -772,12 +1020,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(B.q_full, 1);
     mbar_init(B.q_empty, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSBufs; ++i) {
       mbar_init(&B.s_full[i], 1);
-      mbar_init(&B.s_free[i], kConsumerWarps);
+      mbar_init(&B.s_free[i], L::kSoftmaxWarps);
     }
-    mbar_init(B.p_full, kConsumerWarps);
-    mbar_init(B.o_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&B.p_full[i], L::kSoftmaxWarps);
+      mbar_init(&B.o_done[i], 1);
+    }
     mbar_init(B.drain, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
@@ -792,7 +1042,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = L::kTc ? *tmem_slot : 0u;
   const int it0 = p.cta_begin[blockIdx.x], it1 = p.cta_begin[blockIdx.x + 1];
   if (warp == 0) {
-    producer<D, FP8>(p, &tm_k, &tm_v, &tm_q, smem, B, abort_flag, it0, it1);
+    producer<D, FP8, false>(p, &tm_k, &tm_q, smem, B, abort_flag, it0, it1);
+    return;
+  }
+  if (warp == L::kVProducerWarp) {
+    producer<D, FP8, true>(p, &tm_v, &tm_q, smem, B, abort_flag, it0, it1);
     return;
   }
   if (warp == 1) {
@@ -814,7 +1068,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // warps 1..5: every tensor-memory access is done before warp 1 frees it
   tc_fence_before();
-  named_bar_sync(2, 32 * (1 + kConsumerWarps));
+  named_bar_sync(2, 32 * (1 + L::kSoftmaxWarps));
   tc_fence_after();
   if (L::kTc && warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
@@ -826,7 +1080,7 @@ cudaError_t launch_t(const AttnParams& p, const CUtensorMap& tk, const CUtensorM
   static_assert(L::kAlloc <= 232448, "shared memory budget");
   cudaError_t e = cudaFuncSetAttribute(attn_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
-  attn_kernel<D, FP8><<<num_ctas, kThreads, L::kAlloc, s>>>(p, tk, tv, tq);
+  attn_kernel<D, FP8><<<num_ctas, L::kThreads, L::kAlloc, s>>>(p, tk, tv, tq);
   return cudaGetLastError();
 }
 

@@ -12,7 +12,20 @@ constexpr int kKvTile = 128;        // keys per K/V tile (one pipeline stage)
 constexpr int kDecodeRows = 16;     // rows (query tokens x G) of a decode tile
 constexpr int kPrefillRowsTc = 128;  // rows of a bf16 prefill tile (tcgen05, one TMEM lane per row)
 constexpr int kPrefillRowsWarp = 64; // rows of an fp8-cache prefill tile (4 warps x 16, warp MMA)
-constexpr int kBoxRows = 16;        // cache rows per TMA box (divides every page size)
+constexpr int kBoxRows = 16;        // smallest TMA box (cache rows); every page size is a multiple
+
+// Rows per TMA box for a cache: for a contiguous cache the largest power of
+// two (16..128) not above its capacity, else the largest power of two (16..128)
+// dividing the page size, so a box never crosses a page.
+inline int cache_box_rows(int page_size, int capacity) {
+  int r = 128;
+  if (page_size <= 0) {
+    while (r > kBoxRows && r > capacity) r >>= 1;
+  } else {
+    while (page_size % r != 0) r >>= 1;
+  }
+  return r;
+}
 
 enum ItemKind : int32_t { kDecode = 0, kPrefill = 1 };
 

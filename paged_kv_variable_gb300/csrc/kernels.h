@@ -52,6 +52,7 @@ struct AttnParams {
   const int32_t* block_table;
   int32_t bt_stride;
   int32_t page_size;   // 0 = contiguous
+  int32_t box_rows;    // cache rows per TMA box (divides 128 and the page size)
   int32_t num_pages;   // page pool size (contiguous: batch rows of the cache)
   int32_t G;
   int32_t causal;
