@@ -228,9 +228,7 @@ __device__ bool mma_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, vo
       umma_ss(tmem + b * 128, sdesc_sw128(q_base + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024), kIdescQK,
               k > 0 ? 1u : 0u);
     }
-    umma_commit(&B.s_full[b]);
-#pragma unroll
-    for (int i = 0; i < kConsumerWarps; ++i) umma_commit(&B.empty_k[rk.stage]);
+    umma_commit(&B.s_full[b]);  // the softmax warps release the K stage once they have seen S complete
     rk.advance<L::kStagesK>();
     return true;
   };
@@ -246,8 +244,10 @@ __device__ bool mma_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, vo
       umma_ts(tmem + kTmemO, p_tmem + k * 8, bd, kIdescPV, (first && k == 0) ? 0u : 1u);
     }
     umma_commit(&B.o_done[T & 1]);
-#pragma unroll
-    for (int i = 0; i < kConsumerWarps; ++i) umma_commit(&B.empty_v[rv.stage]);
+    // the V stage barrier expects one arrival per consumer warp (as the decode
+    // warps give): all but one now, the last when these MMAs complete
+    mbar_arrive_cnt(&B.empty_v[rv.stage], kConsumerWarps - 1);
+    umma_commit(&B.empty_v[rv.stage]);
     rv.advance<L::kStagesV>();
     return true;
   };
@@ -316,7 +316,10 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
     tmem_wait_ld();
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&B.s_free[sb]);
+    if (lane == 0) {
+      mbar_arrive(&B.s_free[sb]);
+      mbar_arrive(&B.empty_k[rk.stage]);  // S of this tile is complete: its K stage is free
+    }
 
     // mask by select (rows past the sequence see nothing), row max as a tree
     const bool need_mask = t0 + kKvTile > lim;
