@@ -246,7 +246,7 @@ extern "C" pkv_status pkv_attn_varlen_kvcache_fwd(const pkv_problem* problem, co
   st = make_cache_map(&tv, pr, *args, args->v_cache);
   if (st != PKV_OK) return st;
   memset(&tq, 0, sizeof(tq));
-  if (pr.cache_dtype == PKV_BF16 && plan->num_prefill_items > 0) {
+  if (plan->num_prefill_items > 0) {
     st = make_q_map(&tq, pr, *args, plan->total_q);
     if (st != PKV_OK) return st;
   }

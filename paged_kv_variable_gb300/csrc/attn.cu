@@ -46,26 +46,30 @@ constexpr uint32_t kTmemP = 384;
 
 template <int D, bool FP8>
 struct Layout {
-  static constexpr bool kTc = !FP8;                        // tensor-core (tcgen05) prefill tiles
-  // softmax warps of a tensor-core prefill tile: one per TMEM lane quarter (warps 2..5)
-  static constexpr int kSoftmaxWarps = kConsumerWarps;
-  static constexpr int kVProducerWarp = 2 + kSoftmaxWarps;   // after the consumer warps
-  static constexpr int kThreads = 32 * (3 + kSoftmaxWarps);
+  // Warp roles: 0 K/Q producer, 1 MMA issuer, 2..5 consumers (softmax of
+  // prefill tiles, warp-MMA decode tiles), 6 V producer, and for an fp8 cache
+  // 7..10 converters (e4m3 K/V tiles and the bf16 Q tile to f16 MMA operands).
+  static constexpr bool kTc = true;                         // prefill tiles on tcgen05
+  static constexpr int kSoftmaxWarps = kConsumerWarps;      // one per TMEM lane quarter
+  static constexpr int kVProducerWarp = 2 + kSoftmaxWarps;
+  static constexpr int kConvWarp0 = kVProducerWarp + 1;
+  static constexpr int kConvWarps = FP8 ? 4 : 0;
+  static constexpr int kThreads = 32 * (3 + kSoftmaxWarps + kConvWarps);
   static constexpr int kEsize = FP8 ? 1 : 2;
-  static constexpr int kStagesK = FP8 ? 4 : (D == 128 ? 3 : 4);  // K ring (released after S = Q K^T)
-  static constexpr int kStagesV = FP8 ? 4 : (D == 128 ? 3 : 4);  // V ring (released after O += P V)
+  static constexpr int kStagesK = FP8 ? 2 : (D == 128 ? 3 : 4);  // K ring (released after S = Q K^T)
+  static constexpr int kStagesV = FP8 ? 2 : (D == 128 ? 3 : 4);  // V ring (released after O += P V)
   static constexpr int kTileBytes = kKvTile * D * kEsize;   // one raw K (or V) tile
   static constexpr int kChunks = D * kEsize / 128;            // 128-byte column chunks per cache row
   static constexpr int kKOff = 0;                             // K ring
   static constexpr int kVOff = kStagesK * kTileBytes;         // V ring
-  static constexpr int kQOff = kVOff + kStagesV * kTileBytes; // tcgen05 path: Q tile (128 x D bf16)
-  // decode merge scratch: the fp8 layout has its own; the bf16 layout borrows
-  // the item's last V stage (as large as the scratch) before releasing it
-  static constexpr int kMergeBytes = kConsumerWarps * kDecodeRows * D * 4;
-  static constexpr int kMergeOff = kQOff + (kTc ? kKvTile * D * 2 : 0);
-  static constexpr int kMlOff = kMergeOff + (FP8 ? kMergeBytes : 0);  // float[4][16][2]: (m, l)
+  static constexpr int kQOff = kVOff + kStagesV * kTileBytes; // Q tile (128 x D, bf16; f16 after conversion)
+  static constexpr int kConvTile = kKvTile * D * 2;           // one converted (f16) K or V tile
+  static constexpr int kKcOff = kQOff + kKvTile * D * 2;      // fp8: converted K tiles [2]
+  static constexpr int kVcOff = kKcOff + (FP8 ? 2 * kConvTile : 0);  // fp8: converted V tiles [2]
+  // decode merge scratch: the item's last V stage, borrowed before it is released
+  static constexpr int kMlOff = kVcOff + (FP8 ? 2 * kConvTile : 0);  // float[4][16][2]: (m, l)
   static constexpr int kBarOff = kMlOff + kConsumerWarps * kDecodeRows * 2 * 4;
-  static constexpr int kNumBars = 2 * kStagesK + 2 * kStagesV + 3 + 2 * kSBufs + 4;
+  static constexpr int kNumBars = 2 * kStagesK + 2 * kStagesV + 3 + 2 * kSBufs + 4 + (FP8 ? 9 : 0);
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;     // tmem base, abort flag
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes;                       // base is 1024-aligned (checked in the kernel)
@@ -83,6 +87,12 @@ struct Bars {
   uint64_t* p_full;   // [2] P of a tile is in shared memory (and O rescaled)
   uint64_t* o_done;   // [2] P V of a tile has completed
   uint64_t* drain;    // MMA completion before tensor memory is freed after an abort
+  // fp8 cache only
+  uint64_t* qc_full;   // the Q tile is f16
+  uint64_t* kc_full;   // [2] converted K tile ready
+  uint64_t* kc_empty;  // [2] S of the tile using it has completed
+  uint64_t* vc_full;   // [2] converted V tile ready
+  uint64_t* vc_empty;  // [2] P V of the tile using it has completed
 };
 
 // Byte offset of 16-byte chunk c of row r in a bf16 tile stored as
@@ -205,49 +215,69 @@ __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CU
 // ------------------------------------------------------------------ MMA issuer (prefill tiles)
 // Order per item with n tiles: S_0, S_1, then for each j: S_{j+2}, P_j V_j.
 // S_{j+2} needs S buffer j % 2 read by the softmax of tile j; P_j V_j needs
-// P_j (tensor-memory buffer j % 2, written by the softmax) and V_j.
-template <int D>
+// P_j (tensor-memory buffer j % 2, written by the softmax) and V_j.  With an
+// fp8 cache the K and V operands are the converted f16 tiles (buffer T % 2)
+// and Q is f16 too.
+template <int D, bool FP8>
 __device__ bool mma_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, volatile int* abort_flag,
                            uint32_t tmem, int it0, int it1) {
-  using L = Layout<D, false>;
-  constexpr uint32_t kIdescQK = idesc_f16(1, 0, 128, 128);
-  constexpr uint32_t kIdescPV = idesc_f16(1, 1, 128, D);
+  using L = Layout<D, FP8>;
+  constexpr int kAB = FP8 ? 0 : 1;  // operand type: f16 or bf16
+  constexpr uint32_t kIdescQK = idesc_f16(kAB, 0, 128, 128);
+  constexpr uint32_t kIdescPV = idesc_f16(kAB, 1, 128, D);
   const uint32_t q_base = smem_u32(smem + L::kQOff);
   Ring rk, rv;
   uint32_t pt = 0, pi = 0;
 
   auto issue_s = [&](uint32_t T) -> bool {
     const uint32_t b = T % kSBufs, use = T / kSBufs;
-    if (!mbar_wait(&B.full_k[rk.stage], rk.phase, abort_flag)) return false;
+    uint32_t k_base;
+    if constexpr (FP8) {
+      if (!mbar_wait(&B.kc_full[T & 1], (T >> 1) & 1, abort_flag)) return false;
+      k_base = smem_u32(smem + L::kKcOff + (T & 1) * L::kConvTile);
+    } else {
+      if (!mbar_wait(&B.full_k[rk.stage], rk.phase, abort_flag)) return false;
+      k_base = smem_u32(smem + L::kKOff + rk.stage * L::kTileBytes);
+    }
     if (use >= 1 && !mbar_wait(&B.s_free[b], (use - 1) & 1, abort_flag)) return false;
     tc_fence_after();
-    const uint32_t k_base = smem_u32(smem + L::kKOff + rk.stage * L::kTileBytes);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
       const uint32_t off = (k >> 2) * (kKvTile * 128) + (k & 3) * 32;
       umma_ss(tmem + b * 128, sdesc_sw128(q_base + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024), kIdescQK,
               k > 0 ? 1u : 0u);
     }
-    umma_commit(&B.s_full[b]);  // the softmax warps release the K stage once they have seen S complete
+    umma_commit(&B.s_full[b]);  // bf16: the softmax warps release the K stage once they have seen S complete
+    if constexpr (FP8) umma_commit(&B.kc_empty[T & 1]);
     rk.advance<L::kStagesK>();
     return true;
   };
   auto issue_pv = [&](uint32_t T, bool first) -> bool {
     if (!mbar_wait(&B.p_full[T & 1], (T >> 1) & 1, abort_flag)) return false;
-    if (!mbar_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
+    uint32_t v_base;
+    if constexpr (FP8) {
+      if (!mbar_wait(&B.vc_full[T & 1], (T >> 1) & 1, abort_flag)) return false;
+      v_base = smem_u32(smem + L::kVcOff + (T & 1) * L::kConvTile);
+    } else {
+      if (!mbar_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
+      v_base = smem_u32(smem + L::kVOff + rv.stage * L::kTileBytes);
+    }
     tc_fence_after();
     const uint32_t p_tmem = tmem + kTmemP + (T & 1) * 64;
-    const uint32_t v_base = smem_u32(smem + L::kVOff + rv.stage * L::kTileBytes);
 #pragma unroll
     for (int k = 0; k < kKvTile / 16; ++k) {
       const uint64_t bd = sdesc_sw128(v_base + k * 16 * 128, kKvTile * 128, 1024);
       umma_ts(tmem + kTmemO, p_tmem + k * 8, bd, kIdescPV, (first && k == 0) ? 0u : 1u);
     }
     umma_commit(&B.o_done[T & 1]);
-    // the V stage barrier expects one arrival per consumer warp (as the decode
-    // warps give): all but one now, the last when these MMAs complete
-    mbar_arrive_cnt(&B.empty_v[rv.stage], kConsumerWarps - 1);
-    umma_commit(&B.empty_v[rv.stage]);
+    if constexpr (FP8) {
+      umma_commit(&B.vc_empty[T & 1]);
+    } else {
+      // the V stage barrier expects one arrival per consumer warp (as the decode
+      // warps give): all but one now, the last when these MMAs complete
+      mbar_arrive_cnt(&B.empty_v[rv.stage], kConsumerWarps - 1);
+      umma_commit(&B.empty_v[rv.stage]);
+    }
     rv.advance<L::kStagesV>();
     return true;
   };
@@ -261,7 +291,7 @@ __device__ bool mma_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, vo
       continue;
     }
     if (n == 0) continue;
-    if (!mbar_wait(B.q_full, pi & 1, abort_flag)) return false;
+    if (!mbar_wait(FP8 ? B.qc_full : B.q_full, pi & 1, abort_flag)) return false;
     const int ahead = n < 2 ? n : 2;
     for (int j = 0; j < ahead; ++j)
       if (!issue_s(pt + j)) return false;
@@ -279,15 +309,107 @@ __device__ bool mma_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, vo
   return true;
 }
 
+// ------------------------------------------------------------------ converters (fp8 cache, prefill tiles)
+// Four warps turn each raw e4m3 K / V tile (128 rows x 128 B, swizzled) into
+// an f16 tile in the layout the MMA reads (2 x [128 rows][128 B], swizzled),
+// exactly (every e4m3 value is an f16 value), zeroing V rows past the
+// sequence; and the bf16 Q tile of each item into f16 in place.  Converted
+// tiles are double-buffered (T % 2); raw stages are released after conversion.
+__device__ __forceinline__ void convert_tile(const uint8_t* raw, uint8_t* conv, int ct, int zero_from) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int u = ct + 128 * k;
+    const int r = u >> 3, c = u & 7;  // raw 16-byte chunk c of row r: d = 16c .. 16c+15
+    uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+    if (r < zero_from) {
+      const uint4 w = *reinterpret_cast<const uint4*>(raw + r * 128 + ((c ^ (r & 7)) << 4));
+      lo = make_uint4(e4m3x2_to_f16x2(w.x), e4m3x2_to_f16x2(w.x >> 16), e4m3x2_to_f16x2(w.y),
+                      e4m3x2_to_f16x2(w.y >> 16));
+      hi = make_uint4(e4m3x2_to_f16x2(w.z), e4m3x2_to_f16x2(w.z >> 16), e4m3x2_to_f16x2(w.w),
+                      e4m3x2_to_f16x2(w.w >> 16));
+    }
+    *reinterpret_cast<uint4*>(conv + tile_off(r, 2 * c)) = lo;
+    *reinterpret_cast<uint4*>(conv + tile_off(r, 2 * c + 1)) = hi;
+  }
+}
+
+template <int D>
+__device__ bool converter(const AttnParams& p, uint8_t* smem, const Bars& B, volatile int* abort_flag, int it0,
+                          int it1) {
+  using L = Layout<D, true>;
+  const int lane = threadIdx.x & 31;
+  const int ct = threadIdx.x - 32 * L::kConvWarp0;  // 0..127
+  Ring rk, rv;
+  uint32_t pt = 0, pi = 0;
+  for (int it = it0; it < it1; ++it) {
+    const WorkItem w = p.items[it];
+    const int n = num_tiles(w);
+    if (w.kind != kPrefill) {
+      rk.advance<L::kStagesK>(n);
+      rv.advance<L::kStagesV>(n);
+      continue;
+    }
+    if (n == 0) continue;
+    // Q: bf16 -> f16 in place (elementwise, so the swizzle does not matter)
+    if (!warp_wait(B.q_full, pi & 1, abort_flag)) return false;
+    uint4* q = reinterpret_cast<uint4*>(smem + L::kQOff);
+#pragma unroll 4
+    for (int k = 0; k < kKvTile * D * 2 / 16 / 128; ++k) {
+      uint4 v = q[ct + 128 * k];
+      v = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+      q[ct + 128 * k] = v;
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(B.qc_full);
+    ++pi;
+    for (int j = 0; j < n; ++j) {
+      const uint32_t T = pt + j;
+      const int t0 = w.kv_begin + j * kKvTile;
+      if (!warp_wait(&B.full_k[rk.stage], rk.phase, abort_flag)) return false;
+      if (T >= 2 && !warp_wait(&B.kc_empty[T & 1], ((T >> 1) - 1) & 1, abort_flag)) return false;
+      convert_tile(smem + L::kKOff + rk.stage * L::kTileBytes, smem + L::kKcOff + (T & 1) * L::kConvTile, ct,
+                   kKvTile);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&B.kc_full[T & 1]);
+        mbar_arrive(&B.empty_k[rk.stage]);
+      }
+      if (!warp_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
+      if (T >= 2 && !warp_wait(&B.vc_empty[T & 1], ((T >> 1) - 1) & 1, abort_flag)) return false;
+      // rows past the sequence may hold anything (even NaN): they become zeros
+      convert_tile(smem + L::kVOff + rv.stage * L::kTileBytes, smem + L::kVcOff + (T & 1) * L::kConvTile, ct,
+                   w.lk - t0);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&B.vc_full[T & 1]);
+        mbar_arrive(&B.empty_v[rv.stage]);
+      }
+      rk.advance<L::kStagesK>();
+      rv.advance<L::kStagesV>();
+    }
+    pt += n;
+  }
+  return true;
+}
+
 // ------------------------------------------------------------------ prefill tile softmax (tcgen05 path)
 // Four warps, one query row per thread (TMEM lane), all 128 keys of a tile.
 // P of tile T goes to tensor-memory buffer T % 2, so it only waits for P V of
 // tile T-2; O is rescaled (which needs P V of tile T-1 done) only when a row's
-// running max moves.
-template <int D>
+// running max moves.  bf16 cache: P is bf16, this warp releases the K stage
+// and zeroes V rows past the sequence.  fp8 cache: P is f16 (the MMA runs on
+// f16), the converter warps own the raw stages and the zeroing, S is read in
+// two 64-column passes (fewer live registers in the larger block), and the
+// output carries v_scale.
+template <int D, bool FP8>
 __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, const Bars& B,
-                             volatile int* abort_flag, uint32_t tmem, Ring& rk, Ring& rv, uint32_t& pt, float sl2) {
-  using L = Layout<D, false>;
+                             volatile int* abort_flag, uint32_t tmem, Ring& rk, Ring& rv, uint32_t& pt, float sl2,
+                             float vscale) {
+  using L = Layout<D, FP8>;
+  constexpr int kPass = FP8 ? 64 : 128;      // S columns held in registers at a time
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qw = warp & 3;                   // TMEM lane quarter this warp may access
   const int r = qw * 32 + lane;              // tile row == TMEM lane
@@ -308,34 +430,41 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
     const uint32_t T = pt + j;
     const int t0 = w.kv_begin + j * kKvTile;
     const uint32_t sb = T % kSBufs;
+    const uint32_t s_col = sb * 128;
     if (!warp_wait(&B.s_full[sb], (T / kSBufs) & 1, abort_flag)) return false;
     tc_fence_after();
-    uint32_t s[128];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) tmem_ld32(t_lane + sb * 128 + c * 32, s + c * 32);
-    tmem_wait_ld();
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) {
-      mbar_arrive(&B.s_free[sb]);
-      mbar_arrive(&B.empty_k[rk.stage]);  // S of this tile is complete: its K stage is free
-    }
+    const bool need_mask = __any_sync(0xffffffffu, t0 + kKvTile > lim);
+    uint32_t s[kPass];
 
-    // mask by select (rows past the sequence see nothing), row max as a tree
-    const bool need_mask = t0 + kKvTile > lim;
+    // row max as a tree, masked by select (rows past the sequence see nothing)
     float mx8[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
-    if (__any_sync(0xffffffffu, need_mask)) {
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const float v = (t0 + c < lim) ? __uint_as_float(s[c]) : -INFINITY;
-        s[c] = __float_as_uint(v);
-        mx8[c & 7] = fmaxf(mx8[c & 7], v);
+    for (int h = 0; h < 128 / kPass; ++h) {
+#pragma unroll
+      for (int c = 0; c < kPass / 32; ++c) tmem_ld32(t_lane + s_col + h * kPass + c * 32, s + c * 32);
+      tmem_wait_ld();
+      if constexpr (!FP8) {
+        // all of S is in registers now: release the S buffer and the K stage
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&B.s_free[sb]);
+          mbar_arrive(&B.empty_k[rk.stage]);  // S of this tile is complete: its K stage is free
+        }
       }
-    } else {
+      if (need_mask) {
 #pragma unroll
-      for (int c = 0; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(s[c]));
+        for (int c = 0; c < kPass; ++c) {
+          const float v = (t0 + h * kPass + c < lim) ? __uint_as_float(s[c]) : -INFINITY;
+          s[c] = __float_as_uint(v);
+          mx8[c & 7] = fmaxf(mx8[c & 7], v);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kPass; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(s[c]));
+      }
     }
     const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                            fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
@@ -347,22 +476,45 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
     const float m_new = bump ? mx2 : m;
     const float mu = m_new == -INFINITY ? 0.f : m_new;
     const float alpha = bump ? ex2(m - mu) : 1.f;
-    float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-    uint32_t pk[64];
-#pragma unroll
-    for (int c = 0; c < 64; ++c) {
-      const float p0 = ex2(fmaf(__uint_as_float(s[2 * c]), sl2, -mu));
-      const float p1 = ex2(fmaf(__uint_as_float(s[2 * c + 1]), sl2, -mu));
-      sum4[c & 3] += p0 + p1;
-      pk[c] = pack_bf16(p0, p1);
-    }
-    l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
     m = m_new;
 
     // P buffer T % 2 is free once P V of tile T-2 has completed
     if (j >= 2 && !warp_wait(&B.o_done[T & 1], ((T - 2) >> 1) & 1, abort_flag)) return false;
     tc_fence_after();
-    if (t0 + kKvTile > w.lk) {
+    float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int h = 0; h < 128 / kPass; ++h) {
+      if (FP8) {
+        // second pass: read this half of S again
+#pragma unroll
+        for (int c = 0; c < kPass / 32; ++c) tmem_ld32(t_lane + s_col + h * kPass + c * 32, s + c * 32);
+        tmem_wait_ld();
+        if (need_mask) {
+#pragma unroll
+          for (int c = 0; c < kPass; ++c)
+            if (t0 + h * kPass + c >= lim) s[c] = __float_as_uint(-INFINITY);
+        }
+      }
+      uint32_t pk[kPass / 2];
+#pragma unroll
+      for (int c = 0; c < kPass / 2; ++c) {
+        const float p0 = ex2(fmaf(__uint_as_float(s[2 * c]), sl2, -mu));
+        const float p1 = ex2(fmaf(__uint_as_float(s[2 * c + 1]), sl2, -mu));
+        sum4[c & 3] += p0 + p1;
+        pk[c] = FP8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
+      }
+#pragma unroll
+      for (int c = 0; c < kPass / 64; ++c)
+        tmem_st32(t_lane + kTmemP + (T & 1) * 64 + h * (kPass / 2) + c * 32, pk + c * 32);
+    }
+    if constexpr (FP8) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B.s_free[sb]);
+    }
+    l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+
+    if (!FP8 && t0 + kKvTile > w.lk) {
       // rows past the sequence may hold anything (even NaN): zero them in V
       if (!warp_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
       if (t0 + r >= w.lk) {
@@ -373,8 +525,6 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
           for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(vrow + c * (kKvTile * 128) + q * 16) = make_uint4(0, 0, 0, 0);
       }
     }
-    tmem_st32(t_lane + kTmemP + (T & 1) * 64, pk);
-    tmem_st32(t_lane + kTmemP + (T & 1) * 64 + 32, pk + 32);
     if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
       // O must hold P V of tile T-1 before it is rescaled
       if (!warp_wait(&B.o_done[(T - 1) & 1], ((T - 1) >> 1) & 1, abort_flag)) return false;
@@ -404,7 +554,7 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
     const uint32_t T = pt + n - 1;
     if (!warp_wait(&B.o_done[T & 1], (T >> 1) & 1, abort_flag)) return false;
     tc_fence_after();
-    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const float inv = l > 0.f ? vscale / l : 0.f;
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
       uint32_t o[32];
@@ -741,6 +891,7 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
 #pragma unroll
   for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  int merge_stage = -1;
 
   for (int t0 = w.kv_begin; t0 < w.kv_end; t0 += kKvTile) {
     if (!warp_wait(&B.full_k[rk.stage], rk.phase, abort_flag)) return false;
@@ -844,8 +995,12 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&B.empty_v[rv.stage]);
+    if (kDecodeTile && t0 + kKvTile >= w.kv_end) {
+      merge_stage = rv.stage;  // released after the merge below, which uses it as scratch
+    } else {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B.empty_v[rv.stage]);
+    }
     rk.advance<L::kStagesK>();
     rv.advance<L::kStagesV>();
   }
@@ -857,8 +1012,22 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
   if constexpr (kDecodeTile) {
+    if (merge_stage < 0) {
+      // no key at all: every row is 0 with LSE -inf
+      for (int idx = ctid; idx < R * D; idx += kConsumerThreads) {
+        const int row = idx / D, dd = idx % D;
+        const int tok = w.q_row0 + row / p.G;
+        const int head = w.hk * p.G + row % p.G;
+        p.out[(int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head + dd] = __float2bfloat16_rn(0.f);
+        if (dd == 0 && p.lse != nullptr) p.lse[(int64_t)head * p.total_q + tok] = -INFINITY;
+      }
+      return true;
+    }
+    // Merge of the four warps' partial results in the borrowed 16 KB V stage:
+    // fragments are added in fragment order (all warps share the layout),
+    // warps 2,3 into 0,1, then warp 1 into warp 0, which writes the rows.
     float* ml = reinterpret_cast<float*>(smem + L::kMlOff);
-    float* mo = reinterpret_cast<float*>(smem + L::kMergeOff);
+    float4* buf = reinterpret_cast<float4*>(smem + L::kVOff + merge_stage * L::kTileBytes);  // [2][16][32] float4
     if (t == 0) {
       ml[(cw * 16 + g) * 2 + 0] = m0;
       ml[(cw * 16 + g) * 2 + 1] = l0;
@@ -866,52 +1035,91 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
       ml[(cw * 16 + g + 8) * 2 + 1] = l1;
     }
     named_bar_sync(1, kConsumerThreads);
-    float M0 = -INFINITY, M1 = -INFINITY;
+    float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
 #pragma unroll
     for (int ww = 0; ww < kConsumerWarps; ++ww) {
       M0 = fmaxf(M0, ml[(ww * 16 + g) * 2]);
       M1 = fmaxf(M1, ml[(ww * 16 + g + 8) * 2]);
     }
-    const float f0 = ex2(m0 - (M0 == -INFINITY ? 0.f : M0));
-    const float f1 = ex2(m1 - (M1 == -INFINITY ? 0.f : M1));
+    const float Mu0 = M0 == -INFINITY ? 0.f : M0, Mu1 = M1 == -INFINITY ? 0.f : M1;
 #pragma unroll
-    for (int db = 0; db < 4; ++db)
+    for (int ww = 0; ww < kConsumerWarps; ++ww) {
+      L0 += ml[(ww * 16 + g) * 2 + 1] * ex2(ml[(ww * 16 + g) * 2] - Mu0);
+      L1 += ml[(ww * 16 + g + 8) * 2 + 1] * ex2(ml[(ww * 16 + g + 8) * 2] - Mu1);
+    }
+    const float f0 = ex2(m0 - Mu0), f1 = ex2(m1 - Mu1);
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const float* e = o[4 * db + 2 * h];
-        const float* d = o[4 * db + 2 * h + 1];
-        const int col = 32 * db + 16 * h + 4 * t;
-        *reinterpret_cast<float4*>(mo + (cw * 16 + g) * D + col) =
-            make_float4(e[0] * f0, d[0] * f0, e[1] * f0, d[1] * f0);
-        *reinterpret_cast<float4*>(mo + (cw * 16 + g + 8) * D + col) =
-            make_float4(e[2] * f1, d[2] * f1, e[3] * f1, d[3] * f1);
+    for (int n = 0; n < 16; ++n) {
+      o[n][0] *= f0;
+      o[n][1] *= f0;
+      o[n][2] *= f1;
+      o[n][3] *= f1;
+    }
+    auto put = [&](int slot) {
+#pragma unroll
+      for (int n = 0; n < 16; ++n) buf[(slot * 16 + n) * 32 + lane] = make_float4(o[n][0], o[n][1], o[n][2], o[n][3]);
+    };
+    auto add = [&](int slot) {
+#pragma unroll
+      for (int n = 0; n < 16; ++n) {
+        const float4 v = buf[(slot * 16 + n) * 32 + lane];
+        o[n][0] += v.x;
+        o[n][1] += v.y;
+        o[n][2] += v.z;
+        o[n][3] += v.w;
       }
+    };
+    if (cw >= 2) put(cw - 2);
     named_bar_sync(1, kConsumerThreads);
-    for (int idx = ctid; idx < R * D; idx += kConsumerThreads) {
-      const int row = idx / D, dd = idx % D;
-      float M = -INFINITY;
+    if (cw < 2) add(cw);
+    named_bar_sync(1, kConsumerThreads);
+    if (cw == 1) put(0);
+    named_bar_sync(1, kConsumerThreads);
+    if (cw == 0) {
+      add(0);
+      // O tile 4db+2h+par, column c holds d = 32db + 16h + 2c + par: a thread's
+      // (even, odd) tile pair covers d = 32db + 16h + 4t + {0,1,2,3}
 #pragma unroll
-      for (int ww = 0; ww < kConsumerWarps; ++ww) M = fmaxf(M, ml[(ww * 16 + row) * 2]);
-      const float Mu = M == -INFINITY ? 0.f : M;
-      float Lsum = 0.f, acc = 0.f;
-#pragma unroll
-      for (int ww = 0; ww < kConsumerWarps; ++ww) {
-        Lsum += ml[(ww * 16 + row) * 2 + 1] * ex2(ml[(ww * 16 + row) * 2] - Mu);
-        acc += mo[(ww * 16 + row) * D + dd];
-      }
-      const float val = Lsum > 0.f ? acc / Lsum * vscale : 0.f;
-      const float lse2 = Lsum > 0.f ? Mu + __log2f(Lsum) : -INFINITY;
-      if (w.partial >= 0) {
-        p.partial_o[((int64_t)w.partial * kDecodeRows + row) * D + dd] = val;
-        if (dd == 0) p.partial_lse[w.partial * kDecodeRows + row] = lse2;
-      } else {
+      for (int half = 0; half < 2; ++half) {
+        const int row = half ? r1 : r0;
+        if (row >= R) continue;
+        const float Ls = half ? L1 : L0;
+        const float inv = Ls > 0.f ? vscale / Ls : 0.f;
+        const float lse2 = Ls > 0.f ? (half ? Mu1 : Mu0) + __log2f(Ls) : -INFINITY;
         const int tok = w.q_row0 + row / p.G;
         const int head = w.hk * p.G + row % p.G;
-        p.out[(int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head + dd] = __float2bfloat16_rn(val);
-        if (dd == 0 && p.lse != nullptr) p.lse[(int64_t)head * p.total_q + tok] = lse2 * kLn2;
+#pragma unroll
+        for (int db = 0; db < 4; ++db)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float* e = o[4 * db + 2 * h];
+            const float* d = o[4 * db + 2 * h + 1];
+            const int col = 32 * db + 16 * h + 4 * t;
+            const float4 v = make_float4(e[2 * half] * inv, d[2 * half] * inv, e[2 * half + 1] * inv,
+                                         d[2 * half + 1] * inv);
+            if (w.partial >= 0) {
+              *reinterpret_cast<float4*>(p.partial_o + ((int64_t)w.partial * kDecodeRows + row) * D + col) = v;
+            } else {
+              uint2 pk2;
+              pk2.x = pack_bf16(v.x, v.y);
+              pk2.y = pack_bf16(v.z, v.w);
+              *reinterpret_cast<uint2*>(p.out + (int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head + col) =
+                  pk2;
+            }
+          }
+        if (t == 0) {
+          if (w.partial >= 0)
+            p.partial_lse[w.partial * kDecodeRows + row] = lse2;
+          else if (p.lse != nullptr)
+            p.lse[(int64_t)head * p.total_q + tok] = lse2 * kLn2;
+        }
       }
     }
     named_bar_sync(1, kConsumerThreads);
+    // the borrowed V stage goes back to the producer (generic writes before the next async copy)
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&B.empty_v[merge_stage]);
   } else {
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
@@ -970,10 +1178,8 @@ __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
         rk.advance<L::kStagesK>(num_tiles(w));
         rv.advance<L::kStagesV>(num_tiles(w));
       }
-    } else if constexpr (L::kTc) {
-      ok = softmax_item<D>(p, w, smem, B, abort_flag, tmem, rk, rv, pt, sl2);
     } else {
-      ok = run_item_fp8<kKvTile>(p, w, smem, B, abort_flag, rk, rv, sl2, vscale);
+      ok = softmax_item<D, FP8>(p, w, smem, B, abort_flag, tmem, rk, rv, pt, sl2, vscale);
     }
     if (!ok) {
       record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, it);
@@ -1009,6 +1215,11 @@ __global__ void __launch_bounds__(Layout<D, FP8>::kThreads, 1)
   B.s_free = B.s_full + kSBufs;
   B.p_full = B.s_free + kSBufs;
   B.o_done = B.p_full + 2;
+  B.qc_full = B.o_done + 2;
+  B.kc_full = B.qc_full + 1;
+  B.kc_empty = B.kc_full + 2;
+  B.vc_full = B.kc_empty + 2;
+  B.vc_empty = B.vc_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1031,6 +1242,15 @@ __global__ void __launch_bounds__(Layout<D, FP8>::kThreads, 1)
       mbar_init(&B.p_full[i], L::kSoftmaxWarps);
       mbar_init(&B.o_done[i], 1);
     }
+    if (FP8) {
+      mbar_init(B.qc_full, L::kConvWarps);
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&B.kc_full[i], L::kConvWarps);
+        mbar_init(&B.kc_empty[i], 1);
+        mbar_init(&B.vc_full[i], L::kConvWarps);
+        mbar_init(&B.vc_empty[i], 1);
+      }
+    }
     mbar_init(B.drain, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
@@ -1052,10 +1272,19 @@ __global__ void __launch_bounds__(Layout<D, FP8>::kThreads, 1)
     producer<D, FP8, true>(p, &tm_v, &tm_q, smem, B, abort_flag, it0, it1);
     return;
   }
+  if constexpr (FP8) {
+    if (warp >= L::kConvWarp0) {
+      if (!converter<D>(p, smem, B, abort_flag, it0, it1)) {
+        if (lane == 0) record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, -2);
+        *abort_flag = 1;
+      }
+      return;
+    }
+  }
   if (warp == 1) {
     if constexpr (L::kTc) {
       if (lane == 0) {
-        if (!mma_issuer<D>(p, smem, B, abort_flag, tmem, it0, it1)) {
+        if (!mma_issuer<D, FP8>(p, smem, B, abort_flag, tmem, it0, it1)) {
           record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, -1);
           *abort_flag = 1;
           // wait (bounded) for the MMAs already issued before the memory is freed

@@ -10,8 +10,7 @@ namespace pkv {
 
 constexpr int kKvTile = 128;        // keys per K/V tile (one pipeline stage)
 constexpr int kDecodeRows = 16;     // rows (query tokens x G) of a decode tile
-constexpr int kPrefillRowsTc = 128;  // rows of a bf16 prefill tile (tcgen05, one TMEM lane per row)
-constexpr int kPrefillRowsWarp = 64; // rows of an fp8-cache prefill tile (4 warps x 16, warp MMA)
+constexpr int kPrefillRowsTc = 128;  // rows of a prefill tile (tcgen05, one TMEM lane per row)
 constexpr int kBoxRows = 16;        // smallest TMA box (cache rows); every page size is a multiple
 
 // Rows per TMA box for a cache: for a contiguous cache the largest power of

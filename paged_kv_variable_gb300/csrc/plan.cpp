@@ -89,7 +89,7 @@ extern "C" pkv_status pkv_plan(const pkv_problem* problem, const int32_t* h_q_le
   const int G = p.num_heads_q / p.num_heads_kv;
   const int D = p.head_dim;
   const int esize = p.cache_dtype == PKV_BF16 ? 2 : 1;
-  const int prefill_rows = p.cache_dtype == PKV_BF16 ? kPrefillRowsTc : kPrefillRowsWarp;
+  const int prefill_rows = kPrefillRowsTc;
   const int tq_prefill = prefill_rows / G;  // query tokens per prefill tile
 
   int64_t total_q = 0, total_new = 0, total_decode_keys = 0;
