@@ -280,7 +280,8 @@ extern "C" pkv_status pkv_attn_varlen_kvcache_fwd(const pkv_problem* problem, co
   p.batch = pr.batch;
   cudaError_t e;
   if (g_ev_start && (e = cudaEventRecord(g_ev_start, s)) != cudaSuccess) return cuda_fail(e, "profile event");
-  e = launch_attention(p, tk, tv, tq, plan->num_ctas, pr.head_dim, pr.cache_dtype == PKV_FP8_E4M3, s);
+  e = launch_attention(p, tk, tv, tq, plan->num_ctas, pr.head_dim, pr.cache_dtype == PKV_FP8_E4M3,
+                       plan->num_prefill_items > 0, s);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   if (g_ev_stop && (e = cudaEventRecord(g_ev_stop, s)) != cudaSuccess) return cuda_fail(e, "profile event");
 

@@ -44,32 +44,33 @@ constexpr int kSBufs = 2;             // S = Q K^T of tile j+2 is issued before 
 constexpr uint32_t kTmemO = 256;
 constexpr uint32_t kTmemP = 384;
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool PF>
 struct Layout {
   // Warp roles: 0 K/Q producer, 1 MMA issuer, 2..5 consumers (softmax of
   // prefill tiles, warp-MMA decode tiles), 6 V producer, and for an fp8 cache
   // 7..10 converters (e4m3 K/V tiles and the bf16 Q tile to f16 MMA operands).
-  static constexpr bool kTc = true;                         // prefill tiles on tcgen05
+  static constexpr bool kTc = PF;                           // prefill tiles (on tcgen05) in the plan
   static constexpr int kSoftmaxWarps = kConsumerWarps;      // one per TMEM lane quarter
   static constexpr int kVProducerWarp = 2 + kSoftmaxWarps;
   static constexpr int kConvWarp0 = kVProducerWarp + 1;
-  static constexpr int kConvWarps = FP8 ? 4 : 0;
+  static constexpr int kConvWarps = (FP8 && PF) ? 4 : 0;
   static constexpr int kThreads = 32 * (3 + kSoftmaxWarps + kConvWarps);
   static constexpr int kEsize = FP8 ? 1 : 2;
-  static constexpr int kStagesK = FP8 ? 2 : (D == 128 ? 3 : 4);  // K ring (released after S = Q K^T)
-  static constexpr int kStagesV = FP8 ? 2 : (D == 128 ? 3 : 4);  // V ring (released after O += P V)
+  // decode-only plans give all shared memory to the rings
+  static constexpr int kStagesK = PF ? (FP8 ? 2 : (D == 128 ? 3 : 4)) : (FP8 || D == 64 ? 6 : 4);
+  static constexpr int kStagesV = PF ? (FP8 ? 2 : (D == 128 ? 3 : 4)) : (FP8 || D == 64 ? 6 : 3);
   static constexpr int kTileBytes = kKvTile * D * kEsize;   // one raw K (or V) tile
   static constexpr int kChunks = D * kEsize / 128;            // 128-byte column chunks per cache row
   static constexpr int kKOff = 0;                             // K ring
   static constexpr int kVOff = kStagesK * kTileBytes;         // V ring
   static constexpr int kQOff = kVOff + kStagesV * kTileBytes; // Q tile (128 x D, bf16; f16 after conversion)
   static constexpr int kConvTile = kKvTile * D * 2;           // one converted (f16) K or V tile
-  static constexpr int kKcOff = kQOff + kKvTile * D * 2;      // fp8: converted K tiles [2]
-  static constexpr int kVcOff = kKcOff + (FP8 ? 2 * kConvTile : 0);  // fp8: converted V tiles [2]
+  static constexpr int kKcOff = kQOff + (PF ? kKvTile * D * 2 : 0);  // fp8: converted K tiles [2]
+  static constexpr int kVcOff = kKcOff + (kConvWarps ? 2 * kConvTile : 0);  // fp8: converted V tiles [2]
   // decode merge scratch: the item's last V stage, borrowed before it is released
-  static constexpr int kMlOff = kVcOff + (FP8 ? 2 * kConvTile : 0);  // float[4][16][2]: (m, l)
+  static constexpr int kMlOff = kVcOff + (kConvWarps ? 2 * kConvTile : 0);  // float[4][16][2]: (m, l)
   static constexpr int kBarOff = kMlOff + kConsumerWarps * kDecodeRows * 2 * 4;
-  static constexpr int kNumBars = 2 * kStagesK + 2 * kStagesV + 3 + 2 * kSBufs + 4 + (FP8 ? 9 : 0);
+  static constexpr int kNumBars = 2 * kStagesK + 2 * kStagesV + 3 + 2 * kSBufs + 4 + 9;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;     // tmem base, abort flag
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes;                       // base is 1024-aligned (checked in the kernel)
@@ -131,10 +132,10 @@ struct Ring {
 // box_rows cache rows (128 for a contiguous cache, the largest power of two
 // dividing the page size for a paged one), so the block_table reads of a tile
 // are one coalesced load.
-template <int D, bool FP8, bool kIsV>
+template <int D, bool FP8, bool PF, bool kIsV>
 __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CUtensorMap* tm_q, uint8_t* smem,
                          const Bars& B, volatile int* abort_flag, int it0, int it1) {
-  using L = Layout<D, FP8>;
+  using L = Layout<D, FP8, PF>;
   constexpr int kStages = kIsV ? L::kStagesV : L::kStagesK;
   uint64_t* full = kIsV ? B.full_v : B.full_k;
   uint64_t* empty = kIsV ? B.empty_v : B.empty_k;
@@ -218,10 +219,10 @@ __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CU
 // P_j (tensor-memory buffer j % 2, written by the softmax) and V_j.  With an
 // fp8 cache the K and V operands are the converted f16 tiles (buffer T % 2)
 // and Q is f16 too.
-template <int D, bool FP8>
+template <int D, bool FP8, bool PF>
 __device__ bool mma_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, volatile int* abort_flag,
                            uint32_t tmem, int it0, int it1) {
-  using L = Layout<D, FP8>;
+  using L = Layout<D, FP8, PF>;
   constexpr int kAB = FP8 ? 0 : 1;  // operand type: f16 or bf16
   constexpr uint32_t kIdescQK = idesc_f16(kAB, 0, 128, 128);
   constexpr uint32_t kIdescPV = idesc_f16(kAB, 1, 128, D);
@@ -333,10 +334,10 @@ __device__ __forceinline__ void convert_tile(const uint8_t* raw, uint8_t* conv, 
   }
 }
 
-template <int D>
+template <int D, bool PF>
 __device__ bool converter(const AttnParams& p, uint8_t* smem, const Bars& B, volatile int* abort_flag, int it0,
                           int it1) {
-  using L = Layout<D, true>;
+  using L = Layout<D, true, PF>;
   const int lane = threadIdx.x & 31;
   const int ct = threadIdx.x - 32 * L::kConvWarp0;  // 0..127
   Ring rk, rv;
@@ -404,11 +405,11 @@ __device__ bool converter(const AttnParams& p, uint8_t* smem, const Bars& B, vol
 // f16), the converter warps own the raw stages and the zeroing, S is read in
 // two 64-column passes (fewer live registers in the larger block), and the
 // output carries v_scale.
-template <int D, bool FP8>
+template <int D, bool FP8, bool PF>
 __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, const Bars& B,
                              volatile int* abort_flag, uint32_t tmem, Ring& rk, Ring& rv, uint32_t& pt, float sl2,
                              float vscale) {
-  using L = Layout<D, FP8>;
+  using L = Layout<D, FP8, PF>;
   constexpr int kPass = FP8 ? 64 : 128;      // S columns held in registers at a time
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qw = warp & 3;                   // TMEM lane quarter this warp may access
@@ -585,10 +586,10 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
 
 // ------------------------------------------------------------------ warp-MMA tiles of a bf16 cache (decode)
 // KPW = keys of each 128-key tile handled by one warp: 32 (decode), 128 (prefill).
-template <int D, bool FP8, int KPW>
+template <int D, bool FP8, bool PF, int KPW>
 __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, const Bars& B,
                          volatile int* abort_flag, Ring& rk, Ring& rv, float sl2, float vscale) {
-  using L = Layout<D, FP8>;
+  using L = Layout<D, FP8, PF>;
   constexpr int NT = KPW / 8;       // S column tiles per warp
   constexpr int KS = D / 16;        // k-steps of Q K^T
   constexpr int NO = D / 8;         // O column tiles
@@ -846,10 +847,10 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
 // V: ldmatrix.trans on byte pairs gives a thread (key 2t, 2t+1) x (d 2g, 2g+1);
 // a byte permute splits that into the fragment of column d = 2g (even O tile)
 // and of d = 2g+1 (odd O tile); the epilogue puts O columns back in order.
-template <int KPW>
+template <bool PF, int KPW>
 __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* smem, const Bars& B,
                              volatile int* abort_flag, Ring& rk, Ring& rv, float sl2, float vscale) {
-  using L = Layout<128, true>;
+  using L = Layout<128, true, PF>;
   constexpr int D = 128;
   constexpr int NT = KPW / 8;
   constexpr bool kDecodeTile = (KPW != kKvTile);
@@ -1149,10 +1150,10 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
   return true;
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool PF>
 __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, volatile int* abort_flag, uint32_t tmem,
                          int it0, int it1) {
-  using L = Layout<D, FP8>;
+  using L = Layout<D, FP8, PF>;
   const int ctid = threadIdx.x - 64;
   const bool mma_consumer = ctid < kConsumerThreads;  // warps 2..5
   if (blockIdx.x == 0 && mma_consumer) {
@@ -1171,15 +1172,17 @@ __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
     if (w.kind == kDecode) {
       if (mma_consumer) {
         if constexpr (FP8)
-          ok = run_item_fp8<kKvTile / kConsumerWarps>(p, w, smem, B, abort_flag, rk, rv, sl2, vscale);
+          ok = run_item_fp8<PF, kKvTile / kConsumerWarps>(p, w, smem, B, abort_flag, rk, rv, sl2, vscale);
         else
-          ok = run_item<D, FP8, kKvTile / kConsumerWarps>(p, w, smem, B, abort_flag, rk, rv, sl2, vscale);
+          ok = run_item<D, FP8, PF, kKvTile / kConsumerWarps>(p, w, smem, B, abort_flag, rk, rv, sl2, vscale);
       } else {
         rk.advance<L::kStagesK>(num_tiles(w));
         rv.advance<L::kStagesV>(num_tiles(w));
       }
+    } else if constexpr (PF) {
+      ok = softmax_item<D, FP8, PF>(p, w, smem, B, abort_flag, tmem, rk, rv, pt, sl2, vscale);
     } else {
-      ok = softmax_item<D, FP8>(p, w, smem, B, abort_flag, tmem, rk, rv, pt, sl2, vscale);
+      ok = false;  // a decode-only launch never receives prefill tiles
     }
     if (!ok) {
       record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, it);
@@ -1190,11 +1193,11 @@ __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
   return true;
 }
 
-template <int D, bool FP8>
-__global__ void __launch_bounds__(Layout<D, FP8>::kThreads, 1)
+template <int D, bool FP8, bool PF>
+__global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
     attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q) {
-  using L = Layout<D, FP8>;
+  using L = Layout<D, FP8, PF>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if ((smem_u32(smem_raw) & 1023) != 0) {
     // the swizzled TMA / MMA layouts need a 1024-byte aligned base: refuse, never overrun
@@ -1242,7 +1245,7 @@ __global__ void __launch_bounds__(Layout<D, FP8>::kThreads, 1)
       mbar_init(&B.p_full[i], L::kSoftmaxWarps);
       mbar_init(&B.o_done[i], 1);
     }
-    if (FP8) {
+    if (L::kConvWarps > 0) {
       mbar_init(B.qc_full, L::kConvWarps);
       for (int i = 0; i < 2; ++i) {
         mbar_init(&B.kc_full[i], L::kConvWarps);
@@ -1265,16 +1268,16 @@ __global__ void __launch_bounds__(Layout<D, FP8>::kThreads, 1)
   const uint32_t tmem = L::kTc ? *tmem_slot : 0u;
   const int it0 = p.cta_begin[blockIdx.x], it1 = p.cta_begin[blockIdx.x + 1];
   if (warp == 0) {
-    producer<D, FP8, false>(p, &tm_k, &tm_q, smem, B, abort_flag, it0, it1);
+    producer<D, FP8, PF, false>(p, &tm_k, &tm_q, smem, B, abort_flag, it0, it1);
     return;
   }
   if (warp == L::kVProducerWarp) {
-    producer<D, FP8, true>(p, &tm_v, &tm_q, smem, B, abort_flag, it0, it1);
+    producer<D, FP8, PF, true>(p, &tm_v, &tm_q, smem, B, abort_flag, it0, it1);
     return;
   }
-  if constexpr (FP8) {
+  if constexpr (L::kConvWarps > 0) {
     if (warp >= L::kConvWarp0) {
-      if (!converter<D>(p, smem, B, abort_flag, it0, it1)) {
+      if (!converter<D, PF>(p, smem, B, abort_flag, it0, it1)) {
         if (lane == 0) record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, -2);
         *abort_flag = 1;
       }
@@ -1284,7 +1287,7 @@ __global__ void __launch_bounds__(Layout<D, FP8>::kThreads, 1)
   if (warp == 1) {
     if constexpr (L::kTc) {
       if (lane == 0) {
-        if (!mma_issuer<D, FP8>(p, smem, B, abort_flag, tmem, it0, it1)) {
+        if (!mma_issuer<D, FP8, PF>(p, smem, B, abort_flag, tmem, it0, it1)) {
           record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, -1);
           *abort_flag = 1;
           // wait (bounded) for the MMAs already issued before the memory is freed
@@ -1296,7 +1299,7 @@ __global__ void __launch_bounds__(Layout<D, FP8>::kThreads, 1)
       __syncwarp();
     }
   } else {
-    consumer<D, FP8>(p, smem, B, abort_flag, tmem, it0, it1);
+    consumer<D, FP8, PF>(p, smem, B, abort_flag, tmem, it0, it1);
   }
   // warps 1..5: every tensor-memory access is done before warp 1 frees it
   tc_fence_before();
@@ -1305,25 +1308,31 @@ __global__ void __launch_bounds__(Layout<D, FP8>::kThreads, 1)
   if (L::kTc && warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool PF>
 cudaError_t launch_t(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
                      int num_ctas, cudaStream_t s) {
-  using L = Layout<D, FP8>;
+  using L = Layout<D, FP8, PF>;
   static_assert(L::kAlloc <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(attn_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  cudaError_t e = cudaFuncSetAttribute(attn_kernel<D, FP8, PF>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
-  attn_kernel<D, FP8><<<num_ctas, L::kThreads, L::kAlloc, s>>>(p, tk, tv, tq);
+  attn_kernel<D, FP8, PF><<<num_ctas, L::kThreads, L::kAlloc, s>>>(p, tk, tv, tq);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                             const CUtensorMap& tm_q, int num_ctas, int head_dim, bool fp8, cudaStream_t stream) {
+                             const CUtensorMap& tm_q, int num_ctas, int head_dim, bool fp8, bool has_prefill,
+                             cudaStream_t stream) {
   if (num_ctas == 0) return cudaSuccess;
-  if (fp8) return launch_t<128, true>(p, tm_k, tm_v, tm_q, num_ctas, stream);
-  if (head_dim == 128) return launch_t<128, false>(p, tm_k, tm_v, tm_q, num_ctas, stream);
-  return launch_t<64, false>(p, tm_k, tm_v, tm_q, num_ctas, stream);
+  if (fp8)
+    return has_prefill ? launch_t<128, true, true>(p, tm_k, tm_v, tm_q, num_ctas, stream)
+                       : launch_t<128, true, false>(p, tm_k, tm_v, tm_q, num_ctas, stream);
+  if (head_dim == 128)
+    return has_prefill ? launch_t<128, false, true>(p, tm_k, tm_v, tm_q, num_ctas, stream)
+                       : launch_t<128, false, false>(p, tm_k, tm_v, tm_q, num_ctas, stream);
+  return has_prefill ? launch_t<64, false, true>(p, tm_k, tm_v, tm_q, num_ctas, stream)
+                     : launch_t<64, false, false>(p, tm_k, tm_v, tm_q, num_ctas, stream);
 }
 
 }  // namespace pkv

@@ -72,6 +72,7 @@ struct AttnParams {
 cudaError_t launch_kv_append(const AppendParams& p, int head_dim, bool fp8, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, int num_items, int head_dim, cudaStream_t stream);
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                             const CUtensorMap& tm_q, int num_ctas, int head_dim, bool fp8, cudaStream_t stream);
+                             const CUtensorMap& tm_q, int num_ctas, int head_dim, bool fp8, bool has_prefill,
+                             cudaStream_t stream);
 
 }  // namespace pkv
