@@ -9,9 +9,12 @@ split-KV combine.  value = algorithmic bytes of the step / device time, GB/s.
 The other workloads (prefill with a cached prefix, the mixed batch, the fp8
 cache) are measured the same way and reported under "workloads".
 
-Timing: W warm-up steps, then K steps each timed with CUDA events on the
-launching stream; L2 is flushed (256 MB write) before every timed step,
-outside the timed events.  --impl reference times the CPU oracle instead.
+Timing: W warm-up steps, then the call is captured into a CUDA graph and K
+replays are timed, each with CUDA events on the launching stream (the eager,
+uncaptured call is timed too and reported beside it); L2 is flushed (256 MB
+write, then a 256 MB read of another buffer so that the write's dirty lines
+drain outside the timed region) before every timed step and before every
+timed kernel.  --impl reference times the CPU oracle instead.
 """
 from __future__ import annotations
 
@@ -119,7 +122,10 @@ def aggregate_over_ranks(t_step_ms: float, units_per_rank: float, world: int, de
 
 # --------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi clock / throttle samples while the timed region runs."""
+    """nvidia-smi clock / throttle samples (every 50 ms) while the timed region runs.
+
+    One `nvidia-smi -lms 50` child streams the samples; only those taken between
+    mark_start() and mark_end() are summarised (all of them if none fell there)."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -127,41 +133,63 @@ class ClockSampler:
 
     def __init__(self, index: int):
         self.index = index
-        self.samples = []
-        self._stop = threading.Event()
+        self.samples = []   # (time, fields)
+        self.window = (None, None)
+        self._proc = None
         self._t = None
 
-    def _run(self):
-        while not self._stop.is_set():
-            try:
-                r = subprocess.run(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                                    "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=5)
-                if r.returncode == 0 and r.stdout.strip():
-                    self.samples.append([x.strip() for x in r.stdout.strip().split(",")])
-            except Exception:
-                return
-            self._stop.wait(0.2)
+    def _read(self):
+        for line in self._proc.stdout:
+            f = [x.strip() for x in line.strip().split(",")]
+            if len(f) >= 3:
+                self.samples.append((time.perf_counter(), f))
 
     def __enter__(self):
-        self._t = threading.Thread(target=self._run, daemon=True)
+        try:
+            self._proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                           "--format=csv,noheader,nounits", "-lms", "50"],
+                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self._proc = None
+            return self
+        self._t = threading.Thread(target=self._read, daemon=True)
         self._t.start()
+        t0 = time.perf_counter()
+        while not self.samples and time.perf_counter() - t0 < 5.0 and self._proc.poll() is None:
+            time.sleep(0.01)
         return self
 
+    def mark_start(self):
+        self.window = (time.perf_counter(), None)
+
+    def mark_end(self):
+        self.window = (self.window[0], time.perf_counter())
+
     def __exit__(self, *a):
-        self._stop.set()
+        if self._proc is not None:
+            time.sleep(0.06)  # one more sample after the region
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self._proc.kill()
+                self._proc.wait(timeout=5)
         if self._t:
-            self._t.join(timeout=10)
+            self._t.join(timeout=5)
 
     def summary(self):
-        if not self.samples:
+        t0, t1 = self.window
+        inside = [f for t, f in self.samples if t0 is not None and t1 is not None and t0 <= t <= t1]
+        rows = inside or [f for _, f in self.samples]
+        if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
-        sm = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
-        mx = [float(s[2]) for s in self.samples if s[2].replace(".", "").isdigit()]
+        sm = [float(s[1]) for s in rows if s[1].replace(".", "").isdigit()]
+        mx = [float(s[2]) for s in rows if s[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[k] for s in self.samples for k in range(4) if len(s) > 5 + k and
+        reasons = sorted({names[k] for s in rows for k in range(4) if len(s) > 5 + k and
                           s[5 + k].lower().startswith("active")})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(self.samples)}
+                "reasons": reasons, "samples": len(rows), "samples_in_timed_region": len(inside)}
 
 
 # --------------------------------------------------------------------------- GPU arm
@@ -182,30 +210,75 @@ class Workload:
     def launches_per_step(self):
         return (1 if self.case.k_new is not None else 0) + 1 + (1 if self.nsplit else 0)
 
-    def step(self):
-        self.g.run()
+    def step(self, stream=None):
+        self.g.run(stream)
 
 
-def time_workload(wl, steps, warmup, flush, stream):
+def time_workload(wl, steps, warmup, flush, stream, graph=True):
+    """Per-step device times (whole call, attention kernel) over `steps` steps.
+
+    graph=True: the library call is captured once into a CUDA graph and each
+    step is one replay, as a serving loop runs a fixed-shape decode step (no
+    host launch gaps between the append, attention and combine kernels).
+    graph=False: each step is an eager call from Python."""
     import torch
     import paged_kv_variable_gb300 as pkv
     for _ in range(warmup):
         wl.step()
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    for s0, s1, k0, k1 in ev:
-        flush.zero_()
+    step_ms, kern_ms = [], []
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def capture(profiled):
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        if profiled:
+            pkv.set_profile_events(k0, k1)
+        with torch.cuda.graph(g, stream=cap):
+            wl.step(cap)
+        pkv.set_profile_events(None, None)
+        torch.cuda.synchronize()
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        return g
+
+    # The step is timed without the kernel events (with them the library keeps
+    # the kernels strictly in order); the attention kernel in a second replay
+    # of the same call captured with its events.
+    g_step = capture(False) if graph else None
+    g_prof = capture(True) if graph else None
+    for _ in range(steps):
+        flush_l2(flush)
         s0.record(stream)
-        pkv.set_profile_events(k0, k1)
-        wl.step()
+        if graph:
+            g_step.replay()
+        else:
+            wl.step()
         s1.record(stream)
-    pkv.set_profile_events(None, None)
-    torch.cuda.synchronize()
-    step_ms = [a.elapsed_time(b) for a, b, _, _ in ev]
-    kern_ms = [a.elapsed_time(b) for _, _, a, b in ev]
+        flush_l2(flush)
+        if graph:
+            g_prof.replay()
+        else:
+            pkv.set_profile_events(k0, k1)
+            wl.step()
+            pkv.set_profile_events(None, None)
+        torch.cuda.synchronize()
+        step_ms.append(s0.elapsed_time(s1))
+        kern_ms.append(k0.elapsed_time(k1))
     assert wl.g.status() == 0, wl.g.pkv.last_error()
+    del g_step, g_prof
     return step_ms, kern_ms
+
+
+def flush_l2(bufs):
+    """Evict L2 before a timed step: write one buffer twice the size of L2, then
+    read another, so that the dirty lines of the write are written back here
+    and not inside the timed region."""
+    bufs[0].zero_()
+    bufs[1].sum()
 
 
 def e2e_decode(case, steps, warmup, device):
@@ -293,7 +366,8 @@ def gpu_arm(args):
     from paged_kv_variable_gb300 import build
     build.build()
     stream = torch.cuda.current_stream()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush = (torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device),
+             torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device))
 
     if args.workload == "decode-small":
         # 16 sequences of the decode batch (about 150 MB of KV, above L2): profiler captures
@@ -301,6 +375,15 @@ def gpu_arm(args):
     elif args.workload == "prefill":
         # the contiguous-cache causal prefill (profiler captures of the tensor-core tile)
         main = Workload("prefill", synth.config3(True), device)
+    elif args.workload == "fp8-decode":
+        # decode token 2049 on the fp8 cache written by the fp8 prefill (profiler captures)
+        pre_case, dec_case = synth.config5()
+        main = Workload("fp8-decode", dec_case, device)
+        pre = Workload("fp8-prefill", pre_case, device)
+        pre.step()
+        main.g.k_cache.copy_(pre.g.k_cache)
+        main.g.v_cache.copy_(pre.g.v_cache)
+        del pre
     else:
         main = Workload("decode", decode_case, device)
     with ClockSampler(local) as clk:
@@ -308,12 +391,15 @@ def gpu_arm(args):
             dist.barrier()
         torch.cuda.synchronize()
         t_wall = time.perf_counter()
+        clk.mark_start()
         step_ms, kern_ms = time_workload(main, args.steps, args.warmup, flush, stream)
         torch.cuda.synchronize()
+        clk.mark_end()
         if world > 1:
             dist.barrier()
         t_wall = time.perf_counter() - t_wall
     clocks = clk.summary()
+    eager_ms, eager_kern_ms = time_workload(main, max(3, args.steps // 4), 3, flush, stream, graph=False)
     t_step, job_bytes_per_s = aggregate_over_ranks(sum(step_ms) / len(step_ms), main.work["bytes"], world, device)
     t_kern = sum(kern_ms) / len(kern_ms)
     value = job_bytes_per_s / 1e9
@@ -374,7 +460,9 @@ def gpu_arm(args):
             "config": {"workload": "decode: B=64, 1 query + 1 appended token each, Hq=32, Hkv=8, D=128, bf16 "
                                    "paged cache page 16 (seeded permutation), cache lens U[512,4096]",
                        "step": "kv append + persistent attention + split-KV combine (one library call)",
-                       "l2": "flushed before every timed step (256 MB write, outside the timed events)",
+                       "launch": "CUDA graph replay of the captured library call, one per step",
+                       "l2": "flushed before every timed step (256 MB write, then a 256 MB read of another "
+                             "buffer so no dirty line is written back inside the timed events)",
                        "parallelism": f"replicas x{world}", "split_units": main.nsplit},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(achieved / peaks["hbm_gbs"], 4),
@@ -386,6 +474,9 @@ def gpu_arm(args):
             "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 4)},
             "gpu_launches": main.launches_per_step() * args.steps,
+            "eager": {"ms_per_step": round(sum(eager_ms) / len(eager_ms), 5),
+                      "attn_kernel_ms": round(sum(eager_kern_ms) / len(eager_kern_ms), 5),
+                      "note": "the same step as separate eager calls from Python"},
             "clocks": clocks,
             "wall_s_timed_region": round(t_wall, 4),
             "workloads": extra,
@@ -432,11 +523,11 @@ def reference_arm(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-secondary", dest="secondary", action="store_false")
-    ap.add_argument("--workload", default="decode", choices=["decode", "decode-small", "prefill"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "decode-small", "prefill", "fp8-decode"])
     ap.add_argument("--no-cpu-leg", dest="cpu_leg", action="store_false")
     args = ap.parse_args()
     if args.warmup < 3:

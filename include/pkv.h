@@ -108,6 +108,11 @@ typedef struct {
   int32_t block_table_stride;
   const float* k_scale;          /* fp8 cache only: device fp32 scalar               */
   const float* v_scale;          /* fp8 cache only: device fp32 scalar               */
+  const int32_t* page_indptr;    /* nullable.  Ragged page list (the kv_indptr /
+                                    kv_indices form of the cutlass-sycl and flashinfer
+                                    pages): sequence b's pages are block_table[
+                                    page_indptr[b] + i], i < page_indptr[b+1] -
+                                    page_indptr[b]; block_table_stride is ignored.  */
 } pkv_fwd_args;
 
 typedef struct pkv_plan_s* pkv_plan_t;
@@ -242,7 +247,8 @@ const char* pkv_last_error(void);
  * passed as void*), every later pkv_attn_varlen_kvcache_fwd on this host
  * thread records `start` immediately before and `stop` immediately after the
  * persistent attention kernel, on the call's stream.  NULL, NULL turns it off.
- * The events stay owned by the caller. */
+ * A call captured into a CUDA graph records them as event-record nodes, so each
+ * replay of the graph re-records them.  The events stay owned by the caller. */
 pkv_status pkv_set_profile_events(void* start_event, void* stop_event);
 
 /* Library version string. */

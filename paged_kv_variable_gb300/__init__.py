@@ -51,7 +51,8 @@ class FwdArgs(ctypes.Structure):
                 ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p), ("kc_stride_page", ctypes.c_int64),
                 ("kc_stride_tok", ctypes.c_int64), ("kc_stride_head", ctypes.c_int64),
                 ("cache_seqlens", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
-                ("block_table_stride", ctypes.c_int32), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p)]
+                ("block_table_stride", ctypes.c_int32), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+                ("page_indptr", ctypes.c_void_p)]
 
 
 class WorkItemInfo(ctypes.Structure):
@@ -134,7 +135,8 @@ def make_problem(*, batch, num_heads_q, num_heads_kv, head_dim, page_size, cache
 
 
 def make_args(*, q, out, cu_seqlens_q, max_seqlen_q, k_cache, v_cache, cache_seqlens, lse=None, k_new=None,
-              v_new=None, cu_seqlens_knew=None, block_table=None, k_scale=None, v_scale=None) -> FwdArgs:
+              v_new=None, cu_seqlens_knew=None, block_table=None, k_scale=None, v_scale=None,
+              page_indptr=None) -> FwdArgs:
     """Pointers and element strides of torch tensors laid out as in pkv.h."""
     a = FwdArgs()
     if q is not None:
@@ -152,8 +154,10 @@ def make_args(*, q, out, cu_seqlens_q, max_seqlen_q, k_cache, v_cache, cache_seq
     a.kc_stride_page, a.kc_stride_tok, a.kc_stride_head = k_cache.stride(0), k_cache.stride(1), k_cache.stride(2)
     a.cache_seqlens = _ptr(cache_seqlens)
     if block_table is not None:
-        a.block_table, a.block_table_stride = block_table.data_ptr(), block_table.stride(0)
+        a.block_table = block_table.data_ptr()
+        a.block_table_stride = block_table.stride(0) if block_table.dim() > 1 else 0
     a.k_scale, a.v_scale = _ptr(k_scale), _ptr(v_scale)
+    a.page_indptr = _ptr(page_indptr)
     return a
 
 

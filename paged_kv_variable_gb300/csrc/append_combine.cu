@@ -21,6 +21,7 @@ namespace pkv {
 template <int D, bool FP8>
 __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
   constexpr int E = D / 32;  // elements per lane: 4 (D=128) or 2 (D=64)
+  grid_dep_launch();         // the attention kernel may start; it waits before reading appended rows
   const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (row >= (int64_t)p.total_new * p.hkv) return;
@@ -40,7 +41,10 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
   }
   int64_t dst;
   if (p.page_size > 0) {
-    const int page = __ldg(p.block_table + (int64_t)b * p.bt_stride + pos / p.page_size);
+    int npages;
+    const int32_t* pages = seq_pages(p.block_table, p.bt_stride, p.page_indptr, b, &npages);
+    const int pi = pos / p.page_size;
+    const int page = (npages >= 0 && pi >= npages) ? -1 : __ldg(pages + pi);
     if (page < 0 || page >= p.num_pages) {
       if (lane == 0) record_status(p.status, PKV_ERR_DEVICE_BOUNDS, b, page);
       return;
@@ -90,6 +94,7 @@ __global__ void __launch_bounds__(kDecodeRows * D / 8) combine_kernel(const Comb
   const int row = threadIdx.x / (D / 8);
   const int d0 = (threadIdx.x % (D / 8)) * 8;
   if (row >= ci.n_q * p.G) return;
+  grid_dep_wait();  // the partials come from the attention kernel launched just before
   constexpr float kLn2 = 0.693147180559945309f;
   const float* lse = p.partial_lse + (int64_t)ci.slot0 * kDecodeRows + row;
   float m = -INFINITY;
@@ -135,11 +140,21 @@ cudaError_t launch_kv_append(const AppendParams& p, int head_dim, bool fp8, cuda
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const CombineParams& p, int num_items, int head_dim, cudaStream_t stream) {
+cudaError_t launch_combine(const CombineParams& p, int num_items, int head_dim, bool overlap_prev,
+                           cudaStream_t stream) {
   if (num_items == 0) return cudaSuccess;
-  if (head_dim == 128) combine_kernel<128><<<num_items, kDecodeRows * 128 / 8, 0, stream>>>(p);
-  else combine_kernel<64><<<num_items, kDecodeRows * 64 / 8, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)num_items);
+  cfg.blockDim = dim3((unsigned)(kDecodeRows * head_dim / 8));
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap_prev ? 1 : 0;
+  return head_dim == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<128>, p)
+                         : cudaLaunchKernelEx(&cfg, combine_kernel<64>, p);
 }
 
 }  // namespace pkv

@@ -26,6 +26,8 @@
 // normalised output; their prefill tiles use the warp-level MMA path (64 rows).
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tcgen05.cuh"
@@ -150,9 +152,11 @@ __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CU
   int issued = 0;
   uint32_t pi = 0;  // prefill items with at least one tile
   bool ok = true;
+  bool dep_done = false;  // waited for the append kernel (rows at or past the old cache length)
 
   for (int it = it0; it < it1 && ok; ++it) {
     const WorkItem w = p.items[it];
+    const int lc_old = __ldg(p.plan_lc + w.b);
     if (!kIsV && L::kTc && w.kind == kPrefill && num_tiles(w) > 0) {
       if (!warp_wait(B.q_empty, (pi & 1) ^ 1, abort_flag)) {
         ok = false;
@@ -175,7 +179,10 @@ __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CU
       int page = p.num_pages, slot = 0;
       if (j0 < w.kv_end) {
         if (p.page_size > 0) {
-          const int pg = __ldg(p.block_table + (int64_t)w.b * p.bt_stride + j0 / p.page_size);
+          int npages;
+          const int32_t* pages = seq_pages(p.block_table, p.bt_stride, p.page_indptr, w.b, &npages);
+          const int pgi = j0 / p.page_size;
+          const int pg = (npages >= 0 && pgi >= npages) ? -1 : __ldg(pages + pgi);
           if (pg < 0 || pg >= p.num_pages) {
             if (active && !kIsV) record_status(p.status, PKV_ERR_DEVICE_BOUNDS, w.b, pg);
           } else {
@@ -186,6 +193,10 @@ __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CU
           page = w.b;
           slot = j0;
         }
+      }
+      if (!dep_done && t0 + kKvTile > lc_old && lc_old < w.lk) {
+        grid_dep_wait();
+        dep_done = true;
       }
       if (!warp_wait(&empty[ring.stage], ring.phase ^ 1, abort_flag)) {
         ok = false;
@@ -211,6 +222,9 @@ __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CU
     }
     __syncwarp();
   }
+  // this CTA ends only after the append kernel has: work issued after this
+  // launch on the stream then also follows the append
+  if (!dep_done) grid_dep_wait();
 }
 
 // ------------------------------------------------------------------ MMA issuer (prefill tiles)
@@ -1266,6 +1280,7 @@ __global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = L::kTc ? *tmem_slot : 0u;
+  grid_dep_launch();  // the combine kernel may be scheduled; it waits for this grid to finish
   const int it0 = p.cta_begin[blockIdx.x], it1 = p.cta_begin[blockIdx.x + 1];
   if (warp == 0) {
     producer<D, FP8, PF, false>(p, &tm_k, &tm_q, smem, B, abort_flag, it0, it1);
@@ -1310,29 +1325,48 @@ __global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
 
 template <int D, bool FP8, bool PF>
 cudaError_t launch_t(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
-                     int num_ctas, cudaStream_t s) {
+                     int num_ctas, bool overlap_prev, cudaStream_t s) {
   using L = Layout<D, FP8, PF>;
   static_assert(L::kAlloc <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(attn_kernel<D, FP8, PF>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  // once per device (kept out of the launch path, so the call can be captured in a graph)
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  attn_kernel<D, FP8, PF><<<num_ctas, L::kThreads, L::kAlloc, s>>>(p, tk, tv, tq);
-  return cudaGetLastError();
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured.load() & bit)) {
+    e = cudaFuncSetAttribute(attn_kernel<D, FP8, PF>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit);
+  }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)num_ctas);
+  cfg.blockDim = dim3(L::kThreads);
+  cfg.dynamicSmemBytes = L::kAlloc;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap_prev ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, attn_kernel<D, FP8, PF>, p, tk, tv, tq);
 }
 
 }  // namespace
 
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                              const CUtensorMap& tm_q, int num_ctas, int head_dim, bool fp8, bool has_prefill,
-                             cudaStream_t stream) {
+                             bool overlap_prev, cudaStream_t stream) {
   if (num_ctas == 0) return cudaSuccess;
+  const bool o = overlap_prev;
   if (fp8)
-    return has_prefill ? launch_t<128, true, true>(p, tm_k, tm_v, tm_q, num_ctas, stream)
-                       : launch_t<128, true, false>(p, tm_k, tm_v, tm_q, num_ctas, stream);
+    return has_prefill ? launch_t<128, true, true>(p, tm_k, tm_v, tm_q, num_ctas, o, stream)
+                       : launch_t<128, true, false>(p, tm_k, tm_v, tm_q, num_ctas, o, stream);
   if (head_dim == 128)
-    return has_prefill ? launch_t<128, false, true>(p, tm_k, tm_v, tm_q, num_ctas, stream)
-                       : launch_t<128, false, false>(p, tm_k, tm_v, tm_q, num_ctas, stream);
-  return has_prefill ? launch_t<64, false, true>(p, tm_k, tm_v, tm_q, num_ctas, stream)
-                     : launch_t<64, false, false>(p, tm_k, tm_v, tm_q, num_ctas, stream);
+    return has_prefill ? launch_t<128, false, true>(p, tm_k, tm_v, tm_q, num_ctas, o, stream)
+                       : launch_t<128, false, false>(p, tm_k, tm_v, tm_q, num_ctas, o, stream);
+  return has_prefill ? launch_t<64, false, true>(p, tm_k, tm_v, tm_q, num_ctas, o, stream)
+                     : launch_t<64, false, false>(p, tm_k, tm_v, tm_q, num_ctas, o, stream);
 }
 
 }  // namespace pkv

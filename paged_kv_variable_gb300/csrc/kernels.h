@@ -20,6 +20,7 @@ struct AppendParams {
   int64_t c_stride_page, c_stride_tok, c_stride_head;
   const int32_t* block_table;
   int32_t bt_stride;
+  const int32_t* page_indptr;  // nullable: ragged page list offsets
   int32_t page_size;
   int32_t num_pages;
   int32_t capacity;
@@ -51,6 +52,7 @@ struct AttnParams {
   int32_t total_q;
   const int32_t* block_table;
   int32_t bt_stride;
+  const int32_t* page_indptr;  // nullable: ragged page list offsets
   int32_t page_size;   // 0 = contiguous
   int32_t box_rows;    // cache rows per TMA box (divides 128 and the page size)
   int32_t num_pages;   // page pool size (contiguous: batch rows of the cache)
@@ -69,10 +71,27 @@ struct AttnParams {
   int32_t batch;
 };
 
+// Start of sequence b's page list, and how many pages it has (-1: unchecked).
+__device__ __forceinline__ const int32_t* seq_pages(const int32_t* bt, int32_t stride, const int32_t* indptr, int b,
+                                                    int* count) {
+  if (indptr != nullptr) {
+    const int a = __ldg(indptr + b);
+    *count = __ldg(indptr + b + 1) - a;
+    return bt + a;
+  }
+  *count = -1;
+  return bt + (int64_t)b * stride;
+}
+
 cudaError_t launch_kv_append(const AppendParams& p, int head_dim, bool fp8, cudaStream_t stream);
-cudaError_t launch_combine(const CombineParams& p, int num_items, int head_dim, cudaStream_t stream);
+// overlap_prev: launch with programmatic stream serialization, so that the
+// kernel's start overlaps the end of the kernel issued just before it on the
+// stream (the append kernel for the attention, the attention for the combine);
+// the kernel waits for that one before reading what it wrote.
+cudaError_t launch_combine(const CombineParams& p, int num_items, int head_dim, bool overlap_prev,
+                           cudaStream_t stream);
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                              const CUtensorMap& tm_q, int num_ctas, int head_dim, bool fp8, bool has_prefill,
-                             cudaStream_t stream);
+                             bool overlap_prev, cudaStream_t stream);
 
 }  // namespace pkv

@@ -106,8 +106,8 @@ class GpuCase:
                                k_scale=self.k_scale, v_scale=self.v_scale)
         self.pkv.kv_append(self.problem, a, int(spec.cache_lens.sum()), self.workspace)
 
-    def run(self):
-        self.pkv.attn_varlen_kvcache_fwd(self.problem, self.args(), self.plan, self.workspace)
+    def run(self, stream=None):
+        self.pkv.attn_varlen_kvcache_fwd(self.problem, self.args(), self.plan, self.workspace, stream=stream)
 
     def status(self) -> int:
         return self.pkv.get_status(self.workspace)

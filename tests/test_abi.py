@@ -169,6 +169,9 @@ class _FakeTensor:
     def numel(self):
         return int(np.prod(self.shape))
 
+    def dim(self):
+        return len(self.shape)
+
     def element_size(self):
         return self._esize
 

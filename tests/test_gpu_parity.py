@@ -279,3 +279,64 @@ def test_config5_fp8_prefill_then_decode():
     gd.run()
     assert gd.status() == 0
     check_sampled(dec, gd, n_rows=32, full_cache=False)
+
+
+# ------------------------------------------------------------------ widening: ragged page list, CUDA graphs
+def test_ragged_page_list_equals_block_table():
+    import torch
+    case = synth.random_case(71, batch=5, hq=8, hkv=2, d=128, page_size=16, causal=True, max_cache=700,
+                             max_new=60, allow_zero=True)
+    spec = case.spec
+    g = H.GpuCase(case)
+    g.run()
+    assert g.status() == 0
+    base = H.to_numpy_bits(g.out)
+    # kv_indices / kv_indptr: only the pages each sequence uses, concatenated
+    P = spec.page_size
+    counts = [(int(n) + P - 1) // P for n in spec.kv_lens]
+    flat = np.concatenate([case.block_table[b, :counts[b]] for b in range(spec.batch)] + [np.zeros(0, np.int32)])
+    indptr = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    r = H.GpuCase(case)
+    a = r.pkv.make_args(q=r.q, out=r.out, lse=r.lse, cu_seqlens_q=r.cu_q, max_seqlen_q=int(spec.q_lens.max()),
+                        k_cache=r.k_cache, v_cache=r.v_cache, cache_seqlens=r.cache_lens, k_new=r.k_new,
+                        v_new=r.v_new, cu_seqlens_knew=r.cu_new, block_table=H.i32(flat),
+                        page_indptr=H.i32(indptr))
+    r.pkv.attn_varlen_kvcache_fwd(r.problem, a, r.plan, r.workspace)
+    assert r.status() == 0
+    assert np.array_equal(base, H.to_numpy_bits(r.out))
+    assert torch.equal(g.k_cache, r.k_cache) and torch.equal(g.v_cache, r.v_cache)
+
+
+@pytest.mark.parametrize("kind", ["decode", "mixed"])
+def test_cuda_graph_capture_and_replay(kind):
+    import torch
+    if kind == "decode":
+        rng = np.random.default_rng(81)
+        case = synth.make_case(synth.uniform_spec("graph-decode", 6, 1, 1500, hq=8, hkv=2, d=128, page_size=16), rng)
+    else:
+        case = H.gpu_random_case(82, page_size=16, max_cache=600, max_new=70)
+    g = H.GpuCase(case)
+    g.run()                                   # first call outside capture (one-time set-up)
+    torch.cuda.synchronize()
+    assert g.status() == 0
+    first = H.to_numpy_bits(g.out)
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    args = g.args()
+    with torch.cuda.graph(graph, stream=stream):
+        g.pkv.attn_varlen_kvcache_fwd(g.problem, args, g.plan, g.workspace, stream=stream)
+    g.out.fill_(float("nan"))
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(first, H.to_numpy_bits(g.out))   # the append rewrites the same values
+    # new queries in the captured buffers: the replay attends them
+    rng = np.random.default_rng(83)
+    case.q = synth.f32_to_bf16_bits(rng.standard_normal(case.q.shape, dtype=np.float32))
+    g.q.copy_(H.bf16_tensor(case.q))
+    graph.replay()
+    torch.cuda.synchronize()
+    assert g.status() == 0
+    ref = oracle.forward(case)
+    H.compare_out(g.out, ref["out"], H.BF16_TOL)
