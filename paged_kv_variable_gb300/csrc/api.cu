@@ -292,10 +292,14 @@ extern "C" pkv_status pkv_attn_varlen_kvcache_fwd(const pkv_problem* problem, co
   p.batch = pr.batch;
   cudaError_t e;
   if (g_ev_start && (e = record_profile_event(g_ev_start, s)) != cudaSuccess) return cuda_fail(e, "profile event");
-  // overlap the attention kernel's start with the append kernel (not across a
-  // profiling event, which must see the kernels in order)
+  // Decode-only plans overlap the attention kernel's start with the (small)
+  // append kernel and the combine kernel's start with the attention's end.
+  // Plans with prefill tiles keep the kernels strictly in order: there the
+  // overlap measured slower (large appends, long attention kernels).  Never
+  // across a profiling event, which must see the kernels in order.
+  const bool overlap = plan->num_prefill_items == 0;
   e = launch_attention(p, tk, tv, tq, plan->num_ctas, pr.head_dim, pr.cache_dtype == PKV_FP8_E4M3,
-                       plan->num_prefill_items > 0, plan->total_new > 0 && !g_ev_start, s);
+                       plan->num_prefill_items > 0, overlap && plan->total_new > 0 && !g_ev_start, s);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   if (g_ev_stop && (e = record_profile_event(g_ev_stop, s)) != cudaSuccess) return cuda_fail(e, "profile event");
 
@@ -310,7 +314,7 @@ extern "C" pkv_status pkv_attn_varlen_kvcache_fwd(const pkv_problem* problem, co
     cp.lse = p.lse;
     cp.total_q = p.total_q;
     cp.G = p.G;
-    e = launch_combine(cp, plan->num_combine, pr.head_dim, !g_ev_stop, s);
+    e = launch_combine(cp, plan->num_combine, pr.head_dim, overlap && !g_ev_stop, s);
     if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   }
   return PKV_OK;

@@ -70,8 +70,8 @@ struct Layout {
   static constexpr int kKcOff = kQOff + (PF ? kKvTile * D * 2 : 0);  // fp8: converted K tiles [2]
   static constexpr int kVcOff = kKcOff + (kConvWarps ? 2 * kConvTile : 0);  // fp8: converted V tiles [2]
   // decode merge scratch: the item's last V stage, borrowed before it is released
-  static constexpr int kMlOff = kVcOff + (kConvWarps ? 2 * kConvTile : 0);  // float[4][16][2]: (m, l)
-  static constexpr int kBarOff = kMlOff + kConsumerWarps * kDecodeRows * 2 * 4;
+  static constexpr int kMlOff = kVcOff + (kConvWarps ? 2 * kConvTile : 0);  // float[4][16][2] (m, l), int[4]
+  static constexpr int kBarOff = kMlOff + kConsumerWarps * kDecodeRows * 2 * 4 + 16;  // + failed-wait flags
   static constexpr int kNumBars = 2 * kStagesK + 2 * kStagesV + 3 + 2 * kSBufs + 4 + 9;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;     // tmem base, abort flag
   static constexpr int kBytes = kMiscOff + 16;
@@ -127,13 +127,18 @@ struct Ring {
 };
 
 // ------------------------------------------------------------------ producers
-// Two producer warps, one per ring: warp 0 loads Q tiles and K tiles, the last
-// warp loads V tiles, each as soon as a stage of its own ring is free.  The
-// whole warp issues: lane l owns box (l % boxes) of 128-byte column chunk
-// (l / boxes) of every tile, where a tile of 128 keys is `boxes` boxes of
-// box_rows cache rows (128 for a contiguous cache, the largest power of two
-// dividing the page size for a paged one), so the block_table reads of a tile
-// are one coalesced load.
+// Two producer warps, one per ring: warp 0 loads Q tiles and K tiles, the V
+// producer warp loads V tiles, each as soon as a stage of its own ring is
+// free.  The whole warp issues: lane l owns box (l % boxes) of 128-byte column
+// chunk (l / boxes) of every tile, where a tile of 128 keys is `boxes` boxes
+// of box_rows cache rows (128 for a contiguous cache, the largest power of two
+// dividing the page size for a paged one).
+//
+// Within an item no global load sits between a free stage and its copy:
+// block_table entries are read one warp-wide load per group of 32 / boxes
+// tiles (lane l: box l % boxes of tile l / boxes of the group), a group ahead
+// of its use.  (Loading the next item's descriptor ahead as well measured
+// slower on prefill plans.)
 template <int D, bool FP8, bool PF, bool kIsV>
 __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CUtensorMap* tm_q, uint8_t* smem,
                          const Bars& B, volatile int* abort_flag, int it0, int it1) {
@@ -147,7 +152,22 @@ __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CU
   const int grp = lane % boxes, chunk = lane / boxes;
   const bool active = chunk < L::kChunks;
   const int box_off = chunk * (kKvTile * 128) + grp * (p.box_rows * 128);
+  const bool paged = p.page_size > 0;
+  const int per = 32 / boxes;  // tiles whose page numbers one warp-wide load covers
   if (lane == 0) tma_prefetch_desc(tm_kv);
+
+  // block_table entry of box (lane % boxes) of tile (lane / boxes) of the group
+  // of tiles starting at key t0g of item w (-1 past the sequence's page list)
+  auto load_pages = [&](const WorkItem& w, int t0g) -> int {
+    if (!paged) return 0;
+    const int j = t0g + (lane / boxes) * kKvTile + (lane % boxes) * p.box_rows;
+    if (j >= w.kv_end) return 0;
+    int npages;
+    const int32_t* pages = seq_pages(p.block_table, p.bt_stride, p.page_indptr, w.b, &npages);
+    const int pgi = j / p.page_size;
+    return (npages >= 0 && pgi >= npages) ? -1 : __ldg(pages + pgi);
+  };
+
   Ring ring;
   int issued = 0;
   uint32_t pi = 0;  // prefill items with at least one tile
@@ -157,6 +177,9 @@ __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CU
   for (int it = it0; it < it1 && ok; ++it) {
     const WorkItem w = p.items[it];
     const int lc_old = __ldg(p.plan_lc + w.b);
+    int gcur = load_pages(w, w.kv_begin);
+    int t0g = w.kv_begin;
+    int gnext = load_pages(w, t0g + per * kKvTile);
     if (!kIsV && L::kTc && w.kind == kPrefill && num_tiles(w) > 0) {
       if (!warp_wait(B.q_empty, (pi & 1) ^ 1, abort_flag)) {
         ok = false;
@@ -172,17 +195,21 @@ __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CU
         tma_load_3d(smem + L::kQOff + lane * (kKvTile * 128), tm_q, B.q_full, lane * 64, w.hk * p.G, w.q_row0);
       ++pi;
     }
+    int q = 0;  // tile of the current page group
     for (int t0 = w.kv_begin; t0 < w.kv_end; t0 += kKvTile) {
-      // this lane's box: page and slot (an out-of-range page fills zeros); the
-      // block_table read overlaps the wait below
+      if (q == per) {
+        gcur = gnext;
+        t0g += per * kKvTile;
+        q = 0;
+        gnext = load_pages(w, t0g + per * kKvTile);
+      }
+      const int pg = __shfl_sync(0xffffffffu, gcur, q * boxes + grp);
+      ++q;
+      // this lane's box: page and slot (an out-of-range page fills zeros)
       const int j0 = t0 + grp * p.box_rows;
       int page = p.num_pages, slot = 0;
       if (j0 < w.kv_end) {
-        if (p.page_size > 0) {
-          int npages;
-          const int32_t* pages = seq_pages(p.block_table, p.bt_stride, p.page_indptr, w.b, &npages);
-          const int pgi = j0 / p.page_size;
-          const int pg = (npages >= 0 && pgi >= npages) ? -1 : __ldg(pages + pgi);
+        if (paged) {
           if (pg < 0 || pg >= p.num_pages) {
             if (active && !kIsV) record_status(p.status, PKV_ERR_DEVICE_BOUNDS, w.b, pg);
           } else {
@@ -649,9 +676,16 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
   for (int n = 0; n < NO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   int merge_stage = -1;
+  // A failed (timed-out or aborted) wait ends this warp's tiles, but the warp
+  // still passes every barrier of the merge below, so that no other consumer
+  // warp can be left waiting there.
+  bool failed = false;
 
   for (int t0 = w.kv_begin; t0 < w.kv_end; t0 += kKvTile) {
-    if (!warp_wait(&B.full_k[rk.stage], rk.phase, abort_flag)) return false;
+    if (!warp_wait(&B.full_k[rk.stage], rk.phase, abort_flag)) {
+      failed = true;
+      break;
+    }
     uint8_t* stage_k = smem + L::kKOff + rk.stage * L::kTileBytes;
     uint8_t* stage_v = smem + L::kVOff + rv.stage * L::kTileBytes;
     const uint32_t kb = smem_u32(stage_k);
@@ -722,7 +756,10 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
     }
 
     // O += P V
-    if (!warp_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
+    if (!warp_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) {
+      failed = true;
+      break;
+    }
     const bool vmask = t0 + kKvTile > w.lk;  // rows past the sequence may hold anything: zero them
 #pragma unroll
     for (int kk = 0; kk < KPW / 16; ++kk) {
@@ -766,7 +803,7 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
 
   if constexpr (kDecodeTile) {
-    if (merge_stage < 0) {
+    if (num_tiles(w) == 0) {
       // no key at all: every row is 0 with LSE -inf
       for (int idx = ctid; idx < R * D; idx += kConsumerThreads) {
         const int row = idx / D, d = idx % D;
@@ -779,13 +816,17 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
     }
     float* ml = reinterpret_cast<float*>(smem + L::kMlOff);
     float* mo = reinterpret_cast<float*>(smem + L::kVOff + merge_stage * L::kTileBytes);
+    int* bad = reinterpret_cast<int*>(ml + kConsumerWarps * kDecodeRows * 2);  // [warp]: its waits failed
     if (t == 0) {
       ml[(cw * 16 + g) * 2 + 0] = m0;
       ml[(cw * 16 + g) * 2 + 1] = l0;
       ml[(cw * 16 + g + 8) * 2 + 0] = m1;
       ml[(cw * 16 + g + 8) * 2 + 1] = l1;
     }
+    if (lane == 0) bad[cw] = failed ? 1 : 0;
+    if (failed && lane == 0) *abort_flag = 1;
     named_bar_sync(1, kConsumerThreads);
+    const bool any_bad = (bad[0] | bad[1] | bad[2] | bad[3]) != 0;
     float M0 = -INFINITY, M1 = -INFINITY;
 #pragma unroll
     for (int ww = 0; ww < kConsumerWarps; ++ww) {
@@ -795,13 +836,13 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
     const float f0 = ex2(m0 - (M0 == -INFINITY ? 0.f : M0));
     const float f1 = ex2(m1 - (M1 == -INFINITY ? 0.f : M1));
 #pragma unroll
-    for (int n = 0; n < NO; ++n) {
+    for (int n = 0; n < NO && !any_bad; ++n) {
       *reinterpret_cast<float2*>(mo + (cw * 16 + g) * D + n * 8 + 2 * t) = make_float2(o[n][0] * f0, o[n][1] * f0);
       *reinterpret_cast<float2*>(mo + (cw * 16 + g + 8) * D + n * 8 + 2 * t) =
           make_float2(o[n][2] * f1, o[n][3] * f1);
     }
     named_bar_sync(1, kConsumerThreads);
-    for (int idx = ctid; idx < R * D; idx += kConsumerThreads) {
+    for (int idx = ctid; idx < R * D && !any_bad; idx += kConsumerThreads) {
       const int row = idx / D, d = idx % D;
       float M = -INFINITY;
 #pragma unroll
@@ -829,7 +870,8 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
     // the borrowed V stage goes back to the producer (generic writes before the next async copy)
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&B.empty_v[merge_stage]);
+    if (lane == 0 && merge_stage >= 0) mbar_arrive(&B.empty_v[merge_stage]);
+    if (any_bad) return false;
   } else {
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
@@ -907,9 +949,16 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
   for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   int merge_stage = -1;
+  // A failed (timed-out or aborted) wait ends this warp's tiles, but the warp
+  // still passes every barrier of the merge below, so that no other consumer
+  // warp can be left waiting there.
+  bool failed = false;
 
   for (int t0 = w.kv_begin; t0 < w.kv_end; t0 += kKvTile) {
-    if (!warp_wait(&B.full_k[rk.stage], rk.phase, abort_flag)) return false;
+    if (!warp_wait(&B.full_k[rk.stage], rk.phase, abort_flag)) {
+      failed = true;
+      break;
+    }
     const uint32_t kraw = smem_u32(smem + L::kKOff + rk.stage * L::kTileBytes);
     float s[NT][4];
 #pragma unroll
@@ -975,7 +1024,10 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
       o[n][3] *= al1;
     }
 
-    if (!warp_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
+    if (!warp_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) {
+      failed = true;
+      break;
+    }
     const uint32_t vraw = smem_u32(smem + L::kVOff + rv.stage * L::kTileBytes);
     const bool vmask = t0 + kKvTile > w.lk;  // rows past the sequence may hold anything: zero them
 #pragma unroll
@@ -1027,7 +1079,7 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
   if constexpr (kDecodeTile) {
-    if (merge_stage < 0) {
+    if (num_tiles(w) == 0) {
       // no key at all: every row is 0 with LSE -inf
       for (int idx = ctid; idx < R * D; idx += kConsumerThreads) {
         const int row = idx / D, dd = idx % D;
@@ -1043,13 +1095,17 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
     // warps 2,3 into 0,1, then warp 1 into warp 0, which writes the rows.
     float* ml = reinterpret_cast<float*>(smem + L::kMlOff);
     float4* buf = reinterpret_cast<float4*>(smem + L::kVOff + merge_stage * L::kTileBytes);  // [2][16][32] float4
+    int* bad = reinterpret_cast<int*>(ml + kConsumerWarps * kDecodeRows * 2);  // [warp]: its waits failed
     if (t == 0) {
       ml[(cw * 16 + g) * 2 + 0] = m0;
       ml[(cw * 16 + g) * 2 + 1] = l0;
       ml[(cw * 16 + g + 8) * 2 + 0] = m1;
       ml[(cw * 16 + g + 8) * 2 + 1] = l1;
     }
+    if (lane == 0) bad[cw] = failed ? 1 : 0;
+    if (failed && lane == 0) *abort_flag = 1;
     named_bar_sync(1, kConsumerThreads);
+    const bool any_bad = (bad[0] | bad[1] | bad[2] | bad[3]) != 0;
     float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
 #pragma unroll
     for (int ww = 0; ww < kConsumerWarps; ++ww) {
@@ -1084,13 +1140,13 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
         o[n][3] += v.w;
       }
     };
-    if (cw >= 2) put(cw - 2);
+    if (!any_bad && cw >= 2) put(cw - 2);
     named_bar_sync(1, kConsumerThreads);
-    if (cw < 2) add(cw);
+    if (!any_bad && cw < 2) add(cw);
     named_bar_sync(1, kConsumerThreads);
-    if (cw == 1) put(0);
+    if (!any_bad && cw == 1) put(0);
     named_bar_sync(1, kConsumerThreads);
-    if (cw == 0) {
+    if (!any_bad && cw == 0) {
       add(0);
       // O tile 4db+2h+par, column c holds d = 32db + 16h + 2c + par: a thread's
       // (even, odd) tile pair covers d = 32db + 16h + 4t + {0,1,2,3}
@@ -1134,7 +1190,8 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
     // the borrowed V stage goes back to the producer (generic writes before the next async copy)
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&B.empty_v[merge_stage]);
+    if (lane == 0 && merge_stage >= 0) mbar_arrive(&B.empty_v[merge_stage]);
+    if (any_bad) return false;
   } else {
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
