@@ -501,12 +501,11 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
         for (int c = 0; c < kPass; ++c) {
           const float v = (t0 + h * kPass + c < lim) ? __uint_as_float(s[c]) : -INFINITY;
           s[c] = __float_as_uint(v);
-          mx8[c & 7] = fmaxf(mx8[c & 7], v);
         }
-      } else {
-#pragma unroll
-        for (int c = 0; c < kPass; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(s[c]));
       }
+#pragma unroll
+      for (int c = 0; c < kPass; c += 2)
+        mx8[(c >> 1) & 7] = fmax3(mx8[(c >> 1) & 7], __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
     }
     const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                            fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
@@ -523,7 +522,10 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
     // P buffer T % 2 is free once P V of tile T-2 has completed
     if (j >= 2 && !warp_wait(&B.o_done[T & 1], ((T - 2) >> 1) & 1, abort_flag)) return false;
     tc_fence_after();
-    float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+    // probabilities two at a time: one packed FMA for the scaled logits, one
+    // packed add into the row sum
+    const uint64_t sl2x2 = f32x2(sl2, sl2), nmu2 = f32x2(-mu, -mu);
+    uint64_t sum2[2] = {0ull, 0ull};
 #pragma unroll
     for (int h = 0; h < 128 / kPass; ++h) {
       if (FP8) {
@@ -540,9 +542,10 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
       uint32_t pk[kPass / 2];
 #pragma unroll
       for (int c = 0; c < kPass / 2; ++c) {
-        const float p0 = ex2(fmaf(__uint_as_float(s[2 * c]), sl2, -mu));
-        const float p1 = ex2(fmaf(__uint_as_float(s[2 * c + 1]), sl2, -mu));
-        sum4[c & 3] += p0 + p1;
+        float y0, y1;
+        f32x2_split(fma_f32x2(f32x2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), sl2x2, nmu2), y0, y1);
+        const float p0 = ex2(y0), p1 = ex2(y1);
+        sum2[c & 1] = add_f32x2(sum2[c & 1], f32x2(p0, p1));
         pk[c] = FP8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
       }
 #pragma unroll
@@ -554,7 +557,10 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.s_free[sb]);
     }
-    l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+    float q0, q1, q2, q3;
+    f32x2_split(sum2[0], q0, q1);
+    f32x2_split(sum2[1], q2, q3);
+    l = l * alpha + ((q0 + q2) + (q1 + q3));
 
     if (!FP8 && t0 + kKvTile > w.lk) {
       // rows past the sequence may hold anything (even NaN): zero them in V
