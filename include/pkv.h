@@ -150,6 +150,26 @@ pkv_status pkv_plan(const pkv_problem* problem, const int32_t* h_q_lens,
                     const int32_t* h_cache_lens, const int32_t* h_new_lens,
                     int32_t num_sms, pkv_plan_t* out_plan, size_t* out_workspace_bytes);
 
+/*
+ * pkv_plan_decode_dynamic -- a plan for decode steps whose cache lengths are
+ * read on the device at every call, so that a serving loop can capture
+ * pkv_attn_varlen_kvcache_fwd once in a CUDA graph and replay it while
+ * cache_seqlens grows (flashinfer PR "[Refactor] Uniform PoDAttention API ...",
+ * Limitations: a host plan per step keeps the scheduler out of CUDA graphs;
+ * TransformerEngine PR "Add KV cache for paged/non-paged attention": its
+ * backends support graphs).  h_max_cache_lens[b] bounds cache_seqlens[b] of
+ * every call made with the plan; q lengths and new-token lengths are fixed by
+ * it.  Work is split and scheduled for the bounds; at run time each work
+ * item's key range is cut at the sequence's current key count (split-KV
+ * chunks past it contribute nothing).  Every request must be a decode unit
+ * (q_len * Hq/Hkv <= 16), else PKV_ERR_UNSUPPORTED.  A call whose
+ * cache_seqlens[b] exceeds its bound records PKV_ERR_PLAN_MISMATCH in the
+ * device status and attends at most the bound.  Pure host code.
+ */
+pkv_status pkv_plan_decode_dynamic(const pkv_problem* problem, const int32_t* h_q_lens,
+                                   const int32_t* h_max_cache_lens, const int32_t* h_new_lens,
+                                   int32_t num_sms, pkv_plan_t* out_plan, size_t* out_workspace_bytes);
+
 /* Copies the plan's work list into the caller's device workspace on `stream`
  * (asynchronously; the host copy stays valid until pkv_plan_destroy) and clears
  * the device status word.  Must precede pkv_attn_varlen_kvcache_fwd with this

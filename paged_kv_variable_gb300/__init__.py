@@ -26,7 +26,7 @@ STATUS_NAMES = {
 # every symbol the header declares
 EXPORTED = ["pkv_plan", "pkv_plan_upload", "pkv_plan_get_stats", "pkv_plan_get_items", "pkv_attn_varlen_kvcache_fwd", "pkv_kv_append",
             "pkv_get_status", "pkv_plan_destroy", "pkv_last_error", "pkv_version", "pkv_set_profile_events",
-            "pkv_attn_varlen_kvcache_fwd_noalloc"]
+            "pkv_attn_varlen_kvcache_fwd_noalloc", "pkv_plan_decode_dynamic"]
 
 
 class PkvError(RuntimeError):
@@ -81,6 +81,7 @@ def lib() -> ctypes.CDLL:
         L = ctypes.CDLL(LIB_PATH)
         vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
         L.pkv_plan.argtypes = [ctypes.POINTER(Problem), vp, vp, vp, i32, ctypes.POINTER(vp), ctypes.POINTER(sz)]
+        L.pkv_plan_decode_dynamic.argtypes = L.pkv_plan.argtypes
         L.pkv_plan_upload.argtypes = [vp, vp, sz, vp]
         L.pkv_plan_get_stats.argtypes = [vp, ctypes.POINTER(PlanStats)]
         L.pkv_plan_get_items.argtypes = [vp, ctypes.POINTER(WorkItemInfo), i32, ctypes.POINTER(i32)]
@@ -164,7 +165,7 @@ def make_args(*, q, out, cu_seqlens_q, max_seqlen_q, k_cache, v_cache, cache_seq
 class Plan:
     """Host work list made by ``pkv_plan`` (owned until ``close``)."""
 
-    def __init__(self, problem: Problem, q_lens, cache_lens, new_lens, num_sms: int):
+    def __init__(self, problem: Problem, q_lens, cache_lens, new_lens, num_sms: int, dynamic: bool = False):
         import numpy as np
         self.problem = problem
         self._q = np.ascontiguousarray(q_lens, dtype=np.int32)
@@ -172,9 +173,9 @@ class Plan:
         self._n = None if new_lens is None else np.ascontiguousarray(new_lens, dtype=np.int32)
         h = ctypes.c_void_p()
         ws = ctypes.c_size_t()
-        _check(lib().pkv_plan(ctypes.byref(problem), self._q.ctypes.data, self._c.ctypes.data,
-                              None if self._n is None else self._n.ctypes.data, int(num_sms), ctypes.byref(h),
-                              ctypes.byref(ws)))
+        fn = lib().pkv_plan_decode_dynamic if dynamic else lib().pkv_plan
+        _check(fn(ctypes.byref(problem), self._q.ctypes.data, self._c.ctypes.data,
+                  None if self._n is None else self._n.ctypes.data, int(num_sms), ctypes.byref(h), ctypes.byref(ws)))
         self.handle = h
         self.workspace_bytes = int(ws.value)
 
@@ -211,6 +212,16 @@ def plan(problem: Problem, q_lens, cache_lens, new_lens=None, num_sms: Optional[
         import torch
         num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     return Plan(problem, q_lens, cache_lens, new_lens, num_sms)
+
+
+def plan_decode_dynamic(problem: Problem, q_lens, max_cache_lens, new_lens=None,
+                        num_sms: Optional[int] = None) -> Plan:
+    """A decode plan whose cache lengths are read on the device at every call
+    (bounded by max_cache_lens), for a call captured once in a CUDA graph."""
+    if num_sms is None:
+        import torch
+        num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return Plan(problem, q_lens, max_cache_lens, new_lens, num_sms, dynamic=True)
 
 
 def attn_varlen_kvcache_fwd(problem: Problem, args: FwdArgs, plan_: Plan, workspace, stream=None) -> None:

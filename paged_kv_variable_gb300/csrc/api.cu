@@ -290,6 +290,7 @@ extern "C" pkv_status pkv_attn_varlen_kvcache_fwd(const pkv_problem* problem, co
   p.cache_seqlens = args->cache_seqlens;
   p.plan_lc = reinterpret_cast<const int32_t*>(ws + plan->layout.plan_lc);
   p.batch = pr.batch;
+  p.dynamic = plan->dynamic;
   cudaError_t e;
   if (g_ev_start && (e = record_profile_event(g_ev_start, s)) != cudaSuccess) return cuda_fail(e, "profile event");
   // Decode-only plans overlap the attention kernel's start with the (small)

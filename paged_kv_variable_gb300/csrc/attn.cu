@@ -108,6 +108,22 @@ __device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16* p) {
   return __ldg(reinterpret_cast<const unsigned int*>(p));
 }
 
+// Work item `it` as this call runs it.  A dynamic plan was made for bounds on
+// the cache lengths: the sequence's current length (cache_seqlens, clamped to
+// its bound) cuts the item's key range.  Every role of the kernel reads items
+// through here, so they all see the same tiles.
+__device__ __forceinline__ WorkItem load_item(const AttnParams& p, int it) {
+  WorkItem w = p.items[it];
+  if (p.dynamic) {
+    const int bound = __ldg(p.plan_lc + w.b);
+    const int lc = min(max(__ldg(p.cache_seqlens + w.b), 0), bound);
+    w.lk = w.lk - bound + lc;  // the plan's key count holds bound + new tokens
+    w.kv_end = min(w.kv_end, w.lk);
+    w.kv_begin = min(w.kv_begin, w.kv_end);
+  }
+  return w;
+}
+
 __device__ __forceinline__ int num_tiles(const WorkItem& w) {
   return w.kv_end > w.kv_begin ? (w.kv_end - w.kv_begin + kKvTile - 1) / kKvTile : 0;
 }
@@ -175,8 +191,10 @@ __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CU
   bool dep_done = false;  // waited for the append kernel (rows at or past the old cache length)
 
   for (int it = it0; it < it1 && ok; ++it) {
-    const WorkItem w = p.items[it];
-    const int lc_old = __ldg(p.plan_lc + w.b);
+    const WorkItem w = load_item(p, it);
+    // cache length before this call's append
+    const int lc_old = p.dynamic ? min(max(__ldg(p.cache_seqlens + w.b), 0), __ldg(p.plan_lc + w.b))
+                                 : __ldg(p.plan_lc + w.b);
     int gcur = load_pages(w, w.kv_begin);
     int t0g = w.kv_begin;
     int gnext = load_pages(w, t0g + per * kKvTile);
@@ -325,7 +343,7 @@ __device__ bool mma_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, vo
   };
 
   for (int it = it0; it < it1; ++it) {
-    const WorkItem w = p.items[it];
+    const WorkItem w = load_item(p, it);
     const int n = num_tiles(w);
     if (w.kind != kPrefill) {
       rk.advance<L::kStagesK>(n);
@@ -384,7 +402,7 @@ __device__ bool converter(const AttnParams& p, uint8_t* smem, const Bars& B, vol
   Ring rk, rv;
   uint32_t pt = 0, pi = 0;
   for (int it = it0; it < it1; ++it) {
-    const WorkItem w = p.items[it];
+    const WorkItem w = load_item(p, it);
     const int n = num_tiles(w);
     if (w.kind != kPrefill) {
       rk.advance<L::kStagesK>(n);
@@ -810,9 +828,15 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
 
   if constexpr (kDecodeTile) {
     if (num_tiles(w) == 0) {
-      // no key at all: every row is 0 with LSE -inf
+      // no key at all: every row is 0 with LSE -inf (a split-KV chunk that a
+      // dynamic plan's current length left empty gives such a partial)
       for (int idx = ctid; idx < R * D; idx += kConsumerThreads) {
         const int row = idx / D, d = idx % D;
+        if (w.partial >= 0) {
+          p.partial_o[((int64_t)w.partial * kDecodeRows + row) * D + d] = 0.f;
+          if (d == 0) p.partial_lse[w.partial * kDecodeRows + row] = -INFINITY;
+          continue;
+        }
         const int tok = w.q_row0 + row / p.G;
         const int head = w.hk * p.G + row % p.G;
         p.out[(int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head + d] = __float2bfloat16_rn(0.f);
@@ -1086,9 +1110,15 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
   if constexpr (kDecodeTile) {
     if (num_tiles(w) == 0) {
-      // no key at all: every row is 0 with LSE -inf
+      // no key at all: every row is 0 with LSE -inf (a split-KV chunk that a
+      // dynamic plan's current length left empty gives such a partial)
       for (int idx = ctid; idx < R * D; idx += kConsumerThreads) {
         const int row = idx / D, dd = idx % D;
+        if (w.partial >= 0) {
+          p.partial_o[((int64_t)w.partial * kDecodeRows + row) * D + dd] = 0.f;
+          if (dd == 0) p.partial_lse[w.partial * kDecodeRows + row] = -INFINITY;
+          continue;
+        }
         const int tok = w.q_row0 + row / p.G;
         const int head = w.hk * p.G + row % p.G;
         p.out[(int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head + dd] = __float2bfloat16_rn(0.f);
@@ -1234,9 +1264,10 @@ __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
   const int ctid = threadIdx.x - 64;
   const bool mma_consumer = ctid < kConsumerThreads;  // warps 2..5
   if (blockIdx.x == 0 && mma_consumer) {
-    for (int b = ctid; b < p.batch; b += kConsumerThreads)
-      if (__ldg(p.cache_seqlens + b) != __ldg(p.plan_lc + b))
-        record_status(p.status, PKV_ERR_PLAN_MISMATCH, b, __ldg(p.cache_seqlens + b));
+    for (int b = ctid; b < p.batch; b += kConsumerThreads) {
+      const int lc = __ldg(p.cache_seqlens + b), planned = __ldg(p.plan_lc + b);
+      if (p.dynamic ? (lc < 0 || lc > planned) : lc != planned) record_status(p.status, PKV_ERR_PLAN_MISMATCH, b, lc);
+    }
   }
   const float kscale = FP8 ? __ldg(p.k_scale) : 1.f;
   const float vscale = FP8 ? __ldg(p.v_scale) : 1.f;
@@ -1244,7 +1275,7 @@ __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
   Ring rk, rv;
   uint32_t pt = 0;
   for (int it = it0; it < it1; ++it) {
-    const WorkItem w = p.items[it];
+    const WorkItem w = load_item(p, it);
     bool ok = true;
     if (w.kind == kDecode) {
       if (mma_consumer) {

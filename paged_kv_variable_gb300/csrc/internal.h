@@ -87,6 +87,7 @@ struct pkv_plan_s {
   size_t image_bytes;
   int32_t num_items;
   int32_t num_combine;
+  int32_t dynamic;  // cache lengths read on the device; plan_lc holds their bounds
 };
 
 namespace pkv {

@@ -69,6 +69,7 @@ struct AttnParams {
   const int32_t* cache_seqlens;
   const int32_t* plan_lc;
   int32_t batch;
+  int32_t dynamic;     // plan_lc holds bounds; the cache lengths come from cache_seqlens
 };
 
 // Start of sequence b's page list, and how many pages it has (-1: unchecked).

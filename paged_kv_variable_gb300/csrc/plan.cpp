@@ -73,9 +73,11 @@ pkv_status validate_problem(const pkv_problem* p) {
 
 using namespace pkv;
 
-extern "C" pkv_status pkv_plan(const pkv_problem* problem, const int32_t* h_q_lens,
-                               const int32_t* h_cache_lens, const int32_t* h_new_lens,
-                               int32_t num_sms, pkv_plan_t* out_plan, size_t* out_workspace_bytes) {
+namespace {
+
+pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const int32_t* h_cache_lens,
+                     const int32_t* h_new_lens, int32_t num_sms, bool dynamic, pkv_plan_t* out_plan,
+                     size_t* out_workspace_bytes) {
   if (!out_plan || !out_workspace_bytes) return fail(PKV_ERR_INVALID_ARG, "output pointers are NULL");
   *out_plan = nullptr;
   *out_workspace_bytes = 0;
@@ -101,6 +103,9 @@ extern "C" pkv_status pkv_plan(const pkv_problem* problem, const int32_t* h_q_le
                   p.cache_capacity);
     total_q += lq;
     total_new += ln;
+    if (dynamic && lq > 0 && (int64_t)lq * G > kDecodeRows)
+      return fail(PKV_ERR_UNSUPPORTED, "dynamic plans take decode requests only (sequence %d: %d query rows > %d)", b,
+                  lq * G, kDecodeRows);
     if (lq > 0 && (int64_t)lq * G <= kDecodeRows) total_decode_keys += (int64_t)(lc + ln) * p.num_heads_kv;
   }
   if (total_q > INT32_MAX / 2 || total_new > INT32_MAX / 2)
@@ -249,6 +254,7 @@ extern "C" pkv_status pkv_plan(const pkv_problem* problem, const int32_t* h_q_le
   plan->image_bytes = image_bytes;
   plan->num_items = num_items;
   plan->num_combine = (int32_t)combines.size();
+  plan->dynamic = dynamic ? 1 : 0;
 
   WorkItem* items = (WorkItem*)(plan->image + L.items);
   int32_t* cta_begin = (int32_t*)(plan->image + L.cta_begin);
@@ -265,6 +271,20 @@ extern "C" pkv_status pkv_plan(const pkv_problem* problem, const int32_t* h_q_le
   *out_plan = plan;
   *out_workspace_bytes = L.total;
   return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" pkv_status pkv_plan(const pkv_problem* problem, const int32_t* h_q_lens,
+                               const int32_t* h_cache_lens, const int32_t* h_new_lens,
+                               int32_t num_sms, pkv_plan_t* out_plan, size_t* out_workspace_bytes) {
+  return make_plan(problem, h_q_lens, h_cache_lens, h_new_lens, num_sms, false, out_plan, out_workspace_bytes);
+}
+
+extern "C" pkv_status pkv_plan_decode_dynamic(const pkv_problem* problem, const int32_t* h_q_lens,
+                                              const int32_t* h_max_cache_lens, const int32_t* h_new_lens,
+                                              int32_t num_sms, pkv_plan_t* out_plan, size_t* out_workspace_bytes) {
+  return make_plan(problem, h_q_lens, h_max_cache_lens, h_new_lens, num_sms, true, out_plan, out_workspace_bytes);
 }
 
 extern "C" pkv_status pkv_plan_get_stats(pkv_plan_t plan, pkv_plan_stats* s) {

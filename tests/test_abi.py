@@ -145,6 +145,22 @@ def test_plan_accepts_zero_lengths(pkv):
     assert zero and all(it["kv_begin"] == it["kv_end"] == 0 for it in zero)
 
 
+def test_dynamic_plan_decode_only(pkv):
+    """A dynamic plan schedules decode units for the bounds and refuses prefill requests."""
+    spec = synth.config2(draw_values=False).spec
+    prob = pkv.make_problem(batch=spec.batch, num_heads_q=spec.hq, num_heads_kv=spec.hkv, head_dim=spec.d,
+                            page_size=spec.page_size, cache_capacity=spec.capacity, num_pages=100000,
+                            cache_dtype=spec.cache_dtype, causal=spec.causal, softmax_scale=spec.softmax_scale)
+    bounds = np.minimum(spec.cache_lens + 64, spec.capacity - 1).astype(np.int32)
+    dyn = pkv.plan_decode_dynamic(prob, spec.q_lens, bounds, spec.new_lens, num_sms=152)
+    fixed = pkv.plan(prob, spec.q_lens, bounds, spec.new_lens, num_sms=152)
+    # the same work list as a plan for the bounds themselves
+    assert dyn.items() == fixed.items() and dyn.workspace_bytes == fixed.workspace_bytes
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.plan_decode_dynamic(_problem(pkv, batch=2), [1, 9], [3, 3], [1, 9], num_sms=4)
+    assert e.value.status == 2 and "decode" in pkv.last_error()
+
+
 def test_empty_batch(pkv):
     pl = pkv.plan(_problem(pkv, batch=0), np.zeros(0, np.int32), np.zeros(0, np.int32), None, num_sms=4)
     assert pl.stats()["num_items"] == 0

@@ -340,3 +340,67 @@ def test_cuda_graph_capture_and_replay(kind):
     assert g.status() == 0
     ref = oracle.forward(case)
     H.compare_out(g.out, ref["out"], H.BF16_TOL)
+
+
+def test_dynamic_plan_graph_decode_steps():
+    """One dynamic plan and one captured graph serve several decode steps while
+    cache_seqlens grows on the device; every step matches the oracle."""
+    import dataclasses
+    import math
+    import torch
+    steps = 5
+    rng = np.random.default_rng(91)
+    B, hq, hkv, d, P = 6, 8, 2, 128, 16
+    base = rng.integers(100, 1500, B).astype(np.int32)
+    base[0] = 0                         # a sequence that starts empty
+    total = base + steps                # the tokens the steps will append are drawn up front
+    cap = int((total.max() + 1 + P - 1) // P * P)
+    spec = synth.Spec(batch=B, hq=hq, hkv=hkv, d=d, page_size=P, causal=True,
+                      softmax_scale=float(np.float32(1.0 / math.sqrt(d))), cache_dtype="bf16",
+                      q_lens=np.ones(B, np.int32), cache_lens=total.astype(np.int32),
+                      new_lens=np.ones(B, np.int32), capacity=cap, name="dynamic-decode")
+    case = synth.make_case(spec, rng)
+    g = H.GpuCase(case)
+    bounds = (base + steps - 1).astype(np.int32)
+    plan = g.pkv.plan_decode_dynamic(g.problem, spec.q_lens, bounds, spec.new_lens)
+    assert plan.stats()["num_split_units"] > 0          # split chunks that early steps leave empty
+    ws = g.pkv.workspace_tensor(plan.workspace_bytes)
+    plan.upload(ws)
+
+    def token(pos_of_b):                                 # cached K/V rows at one position per sequence
+        k = np.stack([case.k_cache[case.block_table[b, p // P], p % P] for b, p in enumerate(pos_of_b)])
+        v = np.stack([case.v_cache[case.block_table[b, p // P], p % P] for b, p in enumerate(pos_of_b)])
+        return k, v
+
+    g.cache_lens.copy_(H.i32(base))
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    args = g.args()
+    g.pkv.attn_varlen_kvcache_fwd(g.problem, args, plan, ws, stream=stream)   # first call outside capture
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        g.pkv.attn_varlen_kvcache_fwd(g.problem, args, plan, ws, stream=stream)
+    for s in range(steps):
+        lc = (base + s).astype(np.int32)
+        kt, vt = token(lc)
+        q = synth.f32_to_bf16_bits(rng.standard_normal((B, hq, d), dtype=np.float32))
+        g.cache_lens.copy_(H.i32(lc))
+        g.k_new.copy_(H.bf16_tensor(kt))
+        g.v_new.copy_(H.bf16_tensor(vt))
+        g.q.copy_(H.bf16_tensor(q))
+        g.out.fill_(float("nan"))
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert g.pkv.get_status(ws) == 0
+        step_case = dataclasses.replace(case, spec=dataclasses.replace(spec, cache_lens=lc), q=q, k_new=kt, v_new=vt)
+        ref = oracle.forward(step_case)
+        H.compare_out(g.out, ref["out"], H.BF16_TOL)
+        H.compare_lse(g.lse, ref["lse"])
+    # a length past the plan's bound is reported
+    g.cache_lens.copy_(H.i32(bounds + 1))
+    graph.replay()
+    torch.cuda.synchronize()
+    assert g.pkv.get_status(ws) == 7
