@@ -11,7 +11,8 @@ namespace pkv {
 constexpr int kKvTile = 128;        // keys per K/V tile (one pipeline stage)
 constexpr int kDecodeRows = 16;     // rows (query tokens x G) of a decode tile
 constexpr int kPrefillRowsTc = 128;  // rows of a prefill tile (tcgen05, one TMEM lane per row)
-constexpr int kBoxRows = 16;        // smallest TMA box (cache rows); every page size is a multiple
+constexpr int kBoxRows = 8;         // smallest TMA box (cache rows, 1 KB at 128 B a row, so every box
+                                    // starts on a 128-byte-swizzle atom); every page size is a multiple
 
 // Rows per TMA box for a cache: for a contiguous cache the largest power of
 // two (16..128) not above its capacity, else the largest power of two (16..128)

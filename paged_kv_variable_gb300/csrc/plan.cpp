@@ -57,7 +57,7 @@ pkv_status validate_problem(const pkv_problem* p) {
   if (p->cache_dtype == PKV_FP8_E4M3 && p->head_dim != 128)
     return fail(PKV_ERR_UNSUPPORTED, "fp8 cache needs head_dim 128");
   if (p->page_size < 0 || (p->page_size > 0 && (p->page_size % kBoxRows != 0 || p->page_size > 256)))
-    return fail(PKV_ERR_UNSUPPORTED, "page_size %d: 0 or a multiple of 16 up to 256", p->page_size);
+    return fail(PKV_ERR_UNSUPPORTED, "page_size %d: 0 or a multiple of %d up to 256", p->page_size, kBoxRows);
   if (p->cache_capacity <= 0) return fail(PKV_ERR_INVALID_ARG, "cache_capacity must be positive");
   if (p->page_size > 0 && p->cache_capacity % p->page_size != 0)
     return fail(PKV_ERR_INVALID_ARG, "cache_capacity must be a multiple of page_size");

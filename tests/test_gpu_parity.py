@@ -404,3 +404,24 @@ def test_dynamic_plan_graph_decode_steps():
     graph.replay()
     torch.cuda.synchronize()
     assert g.pkv.get_status(ws) == 7
+
+
+@pytest.mark.parametrize("P,cache_dtype,d", [(8, "bf16", 128), (8, "bf16", 64), (24, "bf16", 128), (8, "fp8", 128)])
+def test_small_and_odd_pages(P, cache_dtype, d):
+    """Pages of 8 tokens (one 8-row TMA box each) and of 24 (three boxes): random
+    decode + prefill batches against the oracle, and paged == contiguous."""
+    case = synth.random_case(100 + P + d, batch=4, hq=8, hkv=2, d=d, page_size=P, causal=True, max_cache=700,
+                             max_new=70, cache_dtype=cache_dtype)
+    g = H.GpuCase(case)
+    g.write_prefix()
+    g.run()
+    assert g.status() == 0
+    ref = oracle.forward(case)
+    tol = H.FP8_TOL if cache_dtype == "fp8" else H.BF16_TOL
+    H.compare_out(g.out, ref["out"], tol)
+    H.compare_lse(g.lse, ref["lse"])
+    if cache_dtype == "bf16":
+        c = H.GpuCase(synth.to_contiguous(case))
+        c.run()
+        assert c.status() == 0
+        assert np.array_equal(H.to_numpy_bits(g.out), H.to_numpy_bits(c.out))
