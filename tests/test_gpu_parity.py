@@ -342,9 +342,11 @@ def test_cuda_graph_capture_and_replay(kind):
     H.compare_out(g.out, ref["out"], H.BF16_TOL)
 
 
-def test_dynamic_plan_graph_decode_steps():
+@pytest.mark.parametrize("cache_dtype,ragged", [("bf16", False), ("bf16", True), ("fp8", False)])
+def test_dynamic_plan_graph_decode_steps(cache_dtype, ragged):
     """One dynamic plan and one captured graph serve several decode steps while
-    cache_seqlens grows on the device; every step matches the oracle."""
+    cache_seqlens grows on the device; every step matches the oracle (bf16 and
+    fp8 caches, padded block table or ragged page list)."""
     import dataclasses
     import math
     import torch
@@ -356,32 +358,50 @@ def test_dynamic_plan_graph_decode_steps():
     total = base + steps                # the tokens the steps will append are drawn up front
     cap = int((total.max() + 1 + P - 1) // P * P)
     spec = synth.Spec(batch=B, hq=hq, hkv=hkv, d=d, page_size=P, causal=True,
-                      softmax_scale=float(np.float32(1.0 / math.sqrt(d))), cache_dtype="bf16",
+                      softmax_scale=float(np.float32(1.0 / math.sqrt(d))), cache_dtype=cache_dtype,
                       q_lens=np.ones(B, np.int32), cache_lens=total.astype(np.int32),
                       new_lens=np.ones(B, np.int32), capacity=cap, name="dynamic-decode")
     case = synth.make_case(spec, rng)
     g = H.GpuCase(case)
+    g.write_prefix()                    # fp8: the whole drawn prefix, quantised by the library's append
     bounds = (base + steps - 1).astype(np.int32)
     plan = g.pkv.plan_decode_dynamic(g.problem, spec.q_lens, bounds, spec.new_lens)
     assert plan.stats()["num_split_units"] > 0          # split chunks that early steps leave empty
     ws = g.pkv.workspace_tensor(plan.workspace_bytes)
     plan.upload(ws)
+    cu_total = np.concatenate([[0], np.cumsum(total)]).astype(np.int64)
 
-    def token(pos_of_b):                                 # cached K/V rows at one position per sequence
+    def token(pos_of_b):                 # the drawn K/V of one position per sequence (bf16 bits)
+        if cache_dtype == "fp8":
+            rows = [cu_total[b] + p for b, p in enumerate(pos_of_b)]
+            return case.prefix_k[rows], case.prefix_v[rows]
         k = np.stack([case.k_cache[case.block_table[b, p // P], p % P] for b, p in enumerate(pos_of_b)])
         v = np.stack([case.v_cache[case.block_table[b, p // P], p % P] for b, p in enumerate(pos_of_b)])
         return k, v
 
+    extra = {}
+    if ragged:
+        counts = [(int(t) + 1 + P - 1) // P for t in total]
+        flat = np.concatenate([case.block_table[b, :counts[b]] for b in range(B)])
+        extra = dict(block_table=H.i32(flat), page_indptr=H.i32(np.concatenate([[0], np.cumsum(counts)])))
+    args = g.pkv.make_args(q=g.q, out=g.out, lse=g.lse, cu_seqlens_q=g.cu_q, max_seqlen_q=1, k_cache=g.k_cache,
+                           v_cache=g.v_cache, cache_seqlens=g.cache_lens, k_new=g.k_new, v_new=g.v_new,
+                           cu_seqlens_knew=g.cu_new, k_scale=g.k_scale if cache_dtype == "fp8" else None,
+                           v_scale=g.v_scale if cache_dtype == "fp8" else None,
+                           **(extra or dict(block_table=g.block_table)))
+    kt, vt = token(base)
+    g.k_new.copy_(H.bf16_tensor(kt))
+    g.v_new.copy_(H.bf16_tensor(vt))
     g.cache_lens.copy_(H.i32(base))
     torch.cuda.synchronize()
     stream = torch.cuda.Stream()
     stream.wait_stream(torch.cuda.current_stream())
-    args = g.args()
     g.pkv.attn_varlen_kvcache_fwd(g.problem, args, plan, ws, stream=stream)   # first call outside capture
     stream.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         g.pkv.attn_varlen_kvcache_fwd(g.problem, args, plan, ws, stream=stream)
+    tol = H.FP8_TOL if cache_dtype == "fp8" else H.BF16_TOL
     for s in range(steps):
         lc = (base + s).astype(np.int32)
         kt, vt = token(lc)
@@ -395,9 +415,13 @@ def test_dynamic_plan_graph_decode_steps():
         graph.replay()
         torch.cuda.synchronize()
         assert g.pkv.get_status(ws) == 0
-        step_case = dataclasses.replace(case, spec=dataclasses.replace(spec, cache_lens=lc), q=q, k_new=kt, v_new=vt)
+        step = dict(q=q, k_new=kt, v_new=vt)
+        if cache_dtype == "fp8":          # the oracle writes its own prefix: the first lc tokens
+            rows = np.concatenate([np.arange(cu_total[b], cu_total[b] + lc[b]) for b in range(B)]).astype(np.int64)
+            step.update(prefix_k=case.prefix_k[rows], prefix_v=case.prefix_v[rows])
+        step_case = dataclasses.replace(case, spec=dataclasses.replace(spec, cache_lens=lc), **step)
         ref = oracle.forward(step_case)
-        H.compare_out(g.out, ref["out"], H.BF16_TOL)
+        H.compare_out(g.out, ref["out"], tol)
         H.compare_lse(g.lse, ref["lse"])
     # a length past the plan's bound is reported
     g.cache_lens.copy_(H.i32(bounds + 1))
