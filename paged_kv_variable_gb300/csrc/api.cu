@@ -291,6 +291,12 @@ extern "C" pkv_status pkv_attn_varlen_kvcache_fwd(const pkv_problem* problem, co
   p.plan_lc = reinterpret_cast<const int32_t*>(ws + plan->layout.plan_lc);
   p.batch = pr.batch;
   p.dynamic = plan->dynamic;
+  p.row_gather = pr.page_size > 0 && pr.page_size < kBoxRows;
+  p.kc = args->k_cache;
+  p.vc = args->v_cache;
+  p.c_stride_page = args->kc_stride_page;
+  p.c_stride_tok = args->kc_stride_tok;
+  p.c_stride_head = args->kc_stride_head;
   cudaError_t e;
   if (g_ev_start && (e = record_profile_event(g_ev_start, s)) != cudaSuccess) return cuda_fail(e, "profile event");
   // Decode-only plans overlap the attention kernel's start with the (small)

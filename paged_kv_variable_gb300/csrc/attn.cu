@@ -169,19 +169,58 @@ __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CU
   const bool active = chunk < L::kChunks;
   const int box_off = chunk * (kKvTile * 128) + grp * (p.box_rows * 128);
   const bool paged = p.page_size > 0;
-  const int per = 32 / boxes;  // tiles whose page numbers one warp-wide load covers
+  const bool rows = p.row_gather != 0;          // pages of 1, 2 or 4 tokens
+  const int per = boxes <= 32 ? 32 / boxes : 1;  // tiles whose page numbers one warp-wide load covers
   if (lane == 0) tma_prefetch_desc(tm_kv);
 
   // block_table entry of box (lane % boxes) of tile (lane / boxes) of the group
   // of tiles starting at key t0g of item w (-1 past the sequence's page list)
   auto load_pages = [&](const WorkItem& w, int t0g) -> int {
-    if (!paged) return 0;
+    if (!paged || rows) return 0;
     const int j = t0g + (lane / boxes) * kKvTile + (lane % boxes) * p.box_rows;
     if (j >= w.kv_end) return 0;
     int npages;
     const int32_t* pages = seq_pages(p.block_table, p.bt_stride, p.page_indptr, w.b, &npages);
     const int pgi = j / p.page_size;
     return (npages >= 0 && pgi >= npages) ? -1 : __ldg(pages + pgi);
+  };
+
+  // Row gather: lane l copies rows l, l+32, l+64, l+96 of a tile in 16-byte
+  // cp.async pieces into the swizzled layout (rows past the key range become
+  // zeros).  A tile is marked full once its copies have landed, which is
+  // checked when the next tile has been issued (or at the end).
+  auto gather_tile = [&](const WorkItem& w, int t0, uint8_t* stage) {
+    const uint8_t* base = static_cast<const uint8_t*>(kIsV ? p.vc : p.kc);
+    constexpr int kPieces = D * L::kEsize / 16;  // 16-byte pieces of a cache row
+#pragma unroll
+    for (int i = 0; i < kKvTile / 32; ++i) {
+      const int r = lane + 32 * i, j = t0 + r;
+      const uint8_t* src = base;
+      uint32_t bytes = 0;
+      if (j < w.kv_end) {
+        int npages;
+        const int32_t* pages = seq_pages(p.block_table, p.bt_stride, p.page_indptr, w.b, &npages);
+        const int pgi = j / p.page_size;
+        const int pg = (npages >= 0 && pgi >= npages) ? -1 : __ldg(pages + pgi);
+        if (pg < 0 || pg >= p.num_pages) {
+          if (!kIsV) record_status(p.status, PKV_ERR_DEVICE_BOUNDS, w.b, pg);
+        } else {
+          src = base + ((int64_t)pg * p.c_stride_page + (int64_t)(j % p.page_size) * p.c_stride_tok +
+                        (int64_t)w.hk * p.c_stride_head) * L::kEsize;
+          bytes = 16;
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < kPieces; ++c)
+        cp_async_16(stage + (c >> 3) * (kKvTile * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4),
+                    src + (bytes ? c * 16 : 0), bytes);
+    }
+    cp_async_commit();
+  };
+  int pend = -1;  // row gather: stage whose copies are in flight, not yet marked full
+  auto mark_full = [&](int stage) {
+    fence_proxy_async_smem();  // the copies (generic proxy) before tensor-core reads of the stage
+    mbar_arrive(&full[stage]);
   };
 
   Ring ring;
@@ -221,7 +260,7 @@ __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CU
         q = 0;
         gnext = load_pages(w, t0g + per * kKvTile);
       }
-      const int pg = __shfl_sync(0xffffffffu, gcur, q * boxes + grp);
+      const int pg = rows ? 0 : __shfl_sync(0xffffffffu, gcur, q * boxes + grp);
       ++q;
       // this lane's box: page and slot (an out-of-range page fills zeros)
       const int j0 = t0 + grp * p.box_rows;
@@ -247,20 +286,34 @@ __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CU
         ok = false;
         break;
       }
-      if (lane == 0) mbar_arrive_expect_tx(&full[ring.stage], L::kTileBytes);
-      __syncwarp();
-      if (active)
-        tma_load_4d(ring_base + ring.stage * L::kTileBytes + box_off, tm_kv, &full[ring.stage],
-                    chunk * (128 / L::kEsize), w.hk, slot, page);
+      if (rows) {
+        gather_tile(w, t0, ring_base + ring.stage * L::kTileBytes);
+        if (pend >= 0) {
+          cp_async_wait_group<1>();  // all but the tile just issued have landed
+          mark_full(pend);
+        }
+        pend = ring.stage;
+      } else {
+        if (lane == 0) mbar_arrive_expect_tx(&full[ring.stage], L::kTileBytes);
+        __syncwarp();
+        if (active)
+          tma_load_4d(ring_base + ring.stage * L::kTileBytes + box_off, tm_kv, &full[ring.stage],
+                      chunk * (128 / L::kEsize), w.hk, slot, page);
+      }
       ++issued;
       ring.advance<kStages>();
     }
+  }
+  if (rows) {
+    // the last tile's copies land before it is marked full (and before the CTA can exit)
+    cp_async_wait_group<0>();
+    if (ok && pend >= 0) mark_full(pend);
   }
   if (!ok) {
     if (lane == 0) record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, kIsV ? 2 : 1);
     *abort_flag = 1;
     // let the copies already issued land before the CTA can exit (bounded)
-    if (lane == 0) {
+    if (lane == 0 && !rows) {
       int zero = 0;
       const int n = issued < kStages ? issued : kStages;
       for (int k = issued - n; k < issued; ++k) mbar_wait(&full[k % kStages], (uint32_t)((k / kStages) & 1), &zero);
@@ -1372,12 +1425,15 @@ __global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
+    // a full barrier takes the producer's arrival (with the copies' bytes), or
+    // one arrival per producer lane when rows are gathered
+    const uint32_t full_count = p.row_gather ? 32u : 1u;
     for (int s = 0; s < L::kStagesK; ++s) {
-      mbar_init(&B.full_k[s], 1);
+      mbar_init(&B.full_k[s], full_count);
       mbar_init(&B.empty_k[s], kConsumerWarps);
     }
     for (int s = 0; s < L::kStagesV; ++s) {
-      mbar_init(&B.full_v[s], 1);
+      mbar_init(&B.full_v[s], full_count);
       mbar_init(&B.empty_v[s], kConsumerWarps);
     }
     mbar_init(B.q_full, 1);

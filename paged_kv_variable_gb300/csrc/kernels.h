@@ -55,6 +55,10 @@ struct AttnParams {
   const int32_t* page_indptr;  // nullable: ragged page list offsets
   int32_t page_size;   // 0 = contiguous
   int32_t box_rows;    // cache rows per TMA box (divides 128 and the page size)
+  int32_t row_gather;  // pages of 1, 2 or 4 tokens: rows gathered with cp.async instead of TMA boxes
+  const void* kc;      // caches and their element strides (row gather)
+  const void* vc;
+  int64_t c_stride_page, c_stride_tok, c_stride_head;
   int32_t num_pages;   // page pool size (contiguous: batch rows of the cache)
   int32_t G;
   int32_t causal;

@@ -56,8 +56,11 @@ pkv_status validate_problem(const pkv_problem* p) {
     return fail(PKV_ERR_UNSUPPORTED, "head_dim %d not in {64, 128}", p->head_dim);
   if (p->cache_dtype == PKV_FP8_E4M3 && p->head_dim != 128)
     return fail(PKV_ERR_UNSUPPORTED, "fp8 cache needs head_dim 128");
-  if (p->page_size < 0 || (p->page_size > 0 && (p->page_size % kBoxRows != 0 || p->page_size > 256)))
-    return fail(PKV_ERR_UNSUPPORTED, "page_size %d: 0 or a multiple of %d up to 256", p->page_size, kBoxRows);
+  if (p->page_size < 0 || p->page_size > 256 ||
+      (p->page_size >= kBoxRows && p->page_size % kBoxRows != 0) ||
+      (p->page_size > 0 && p->page_size < kBoxRows && (p->page_size & (p->page_size - 1)) != 0))
+    return fail(PKV_ERR_UNSUPPORTED, "page_size %d: 0, 1, 2, 4 or a multiple of %d up to 256", p->page_size,
+                kBoxRows);
   if (p->cache_capacity <= 0) return fail(PKV_ERR_INVALID_ARG, "cache_capacity must be positive");
   if (p->page_size > 0 && p->cache_capacity % p->page_size != 0)
     return fail(PKV_ERR_INVALID_ARG, "cache_capacity must be a multiple of page_size");

@@ -48,7 +48,8 @@ def _problem(pkv, **kw):
 @pytest.mark.parametrize("kw,status", [
     (dict(num_heads_q=6, num_heads_kv=4), 1),
     (dict(head_dim=96), 2),
-    (dict(page_size=4), 2),
+    (dict(page_size=3), 2),
+    (dict(page_size=12), 2),
     (dict(page_size=512), 2),
     (dict(cache_dtype="fp8", head_dim=64), 2),
     (dict(num_heads_q=64, num_heads_kv=2), 2),

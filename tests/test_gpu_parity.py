@@ -430,10 +430,13 @@ def test_dynamic_plan_graph_decode_steps(cache_dtype, ragged):
     assert g.pkv.get_status(ws) == 7
 
 
-@pytest.mark.parametrize("P,cache_dtype,d", [(8, "bf16", 128), (8, "bf16", 64), (24, "bf16", 128), (8, "fp8", 128)])
+@pytest.mark.parametrize("P,cache_dtype,d", [(8, "bf16", 128), (8, "bf16", 64), (24, "bf16", 128), (8, "fp8", 128),
+                                             (1, "bf16", 128), (2, "bf16", 64), (4, "bf16", 128), (4, "fp8", 128),
+                                             (1, "fp8", 128)])
 def test_small_and_odd_pages(P, cache_dtype, d):
-    """Pages of 8 tokens (one 8-row TMA box each) and of 24 (three boxes): random
-    decode + prefill batches against the oracle, and paged == contiguous."""
+    """Pages of 8 tokens (one 8-row TMA box each), of 24 (three boxes) and of
+    1, 2 or 4 tokens (rows gathered one by one): random decode + prefill
+    batches against the oracle, and paged == contiguous."""
     case = synth.random_case(100 + P + d, batch=4, hq=8, hkv=2, d=d, page_size=P, causal=True, max_cache=700,
                              max_new=70, cache_dtype=cache_dtype)
     g = H.GpuCase(case)
@@ -449,3 +452,20 @@ def test_small_and_odd_pages(P, cache_dtype, d):
         c.run()
         assert c.status() == 0
         assert np.array_equal(H.to_numpy_bits(g.out), H.to_numpy_bits(c.out))
+
+
+@pytest.mark.parametrize("P,cache_dtype", [(1, "bf16"), (4, "bf16"), (2, "fp8")])
+def test_small_pages_decode(P, cache_dtype):
+    """Decode batches (split-KV chunks included) over pages of 1, 2 and 4 tokens."""
+    rng = np.random.default_rng(140 + P)
+    spec = synth.uniform_spec("small-page-decode", 6, 1, 2500, hq=16, hkv=4, d=128, page_size=P,
+                              cache_dtype=cache_dtype)
+    case = synth.make_case(spec, rng)
+    g = H.GpuCase(case, num_sms=8)
+    assert g.plan.stats()["num_split_units"] > 0
+    g.write_prefix()
+    g.run()
+    assert g.status() == 0
+    ref = oracle.forward(case)
+    H.compare_out(g.out, ref["out"], H.FP8_TOL if cache_dtype == "fp8" else H.BF16_TOL)
+    H.compare_lse(g.lse, ref["lse"])
