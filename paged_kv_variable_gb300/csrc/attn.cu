@@ -405,18 +405,21 @@ __device__ bool mma_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, vo
     }
     if (n == 0) continue;
     if (!mbar_wait(FP8 ? B.qc_full : B.q_full, pi & 1, abort_flag)) return false;
-    if constexpr (!FP8) {
-      // Two queues, each in order: S_j (K_j loaded, S buffer j % 2 read by the
-      // softmax of tile j-2) and P_j V_j (P_j written, V_j loaded).  Whichever
-      // head is ready is issued, so a K tile still in flight does not hold up
-      // a P V whose completion the softmax is waiting for.
+    {
+      // Two queues, each in order: S_j (K_j loaded -- converted, for an fp8
+      // cache -- and S buffer j % 2 read by the softmax of tile j-2) and P_j V_j
+      // (P_j written, V_j loaded).  Whichever head is ready is issued, so a K
+      // tile still in flight does not hold up a P V whose completion the
+      // softmax is waiting for.
       int ns = 0, npv = 0;
       uint64_t t_last = globaltimer_ns();
       while (npv < n) {
         bool progressed = false;
         if (npv < ns) {
           const uint32_t T = pt + npv;
-          if (mbar_test_wait(&B.p_full[T & 1], (T >> 1) & 1) && mbar_test_wait(&B.full_v[rv.stage], rv.phase)) {
+          const bool v_ready = FP8 ? mbar_test_wait(&B.vc_full[T & 1], (T >> 1) & 1)
+                                   : mbar_test_wait(&B.full_v[rv.stage], rv.phase);
+          if (mbar_test_wait(&B.p_full[T & 1], (T >> 1) & 1) && v_ready) {
             if (!issue_pv(T, npv == 0)) return false;  // its waits are already satisfied
             ++npv;
             progressed = true;
@@ -424,8 +427,9 @@ __device__ bool mma_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, vo
         }
         if (ns < n && ns < npv + 3) {  // S runs up to two tiles ahead of P V
           const uint32_t T = pt + ns, b = T % kSBufs, use = T / kSBufs;
-          if (mbar_test_wait(&B.full_k[rk.stage], rk.phase) &&
-              (use == 0 || mbar_test_wait(&B.s_free[b], (use - 1) & 1))) {
+          const bool k_ready = FP8 ? mbar_test_wait(&B.kc_full[T & 1], (T >> 1) & 1)
+                                   : mbar_test_wait(&B.full_k[rk.stage], rk.phase);
+          if (k_ready && (use == 0 || mbar_test_wait(&B.s_free[b], (use - 1) & 1))) {
             if (!issue_s(T)) return false;
             if (ns == n - 1) umma_commit(B.q_empty);
             ++ns;
@@ -439,18 +443,6 @@ __device__ bool mma_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, vo
           if (globaltimer_ns() - t_last > kWaitLimitNs) return false;
           __nanosleep(32);
         }
-      }
-    } else {
-      const int ahead = n < 2 ? n : 2;
-      for (int j = 0; j < ahead; ++j)
-        if (!issue_s(pt + j)) return false;
-      if (ahead == n) umma_commit(B.q_empty);
-      for (int j = 0; j < n; ++j) {
-        if (j + 2 < n) {
-          if (!issue_s(pt + j + 2)) return false;
-          if (j + 2 == n - 1) umma_commit(B.q_empty);
-        }
-        if (!issue_pv(pt + j, j == 0)) return false;
       }
     }
     pt += n;
