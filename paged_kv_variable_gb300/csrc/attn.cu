@@ -4,26 +4,31 @@
 // "[Refactor] Uniform PoDAttention API with Horizontal Fusion SMs Schedule",
 // Key Changes 2: prefill and decode work share one persistent launch).
 //
-// Warp roles (224 threads):
+// Warp roles (224 threads; 352 with the fp8 converters):
 //   warps 0, 6  TMA producers (K and Q; V): tiles of 128 keys, boxes of up to
 //               128 rows per (page, 128-byte column chunk), page numbers read from
-//               block_table (vLLM PR "[Kernel][Triton][FP8] ...", review:
-//               block_table support; TransformerEngine PR "Add KV cache for
-//               paged/non-paged attention": one table for K and V, bshd pages)
-//               into a ring of shared-memory stages (the cached-KV prefetch of
-//               the cutlass-sycl PR "Extend FlashAttention Prefill with KV
-//               cache"); plus the 128-row Q tile of a prefill item.
+//               block_table or a ragged page list (vLLM PR "[Kernel][Triton][FP8]
+//               ...", review: block_table support; TransformerEngine PR "Add KV
+//               cache for paged/non-paged attention": one table for K and V, bshd
+//               pages; the kv_indptr / kv_indices form asked for in the review of
+//               the cutlass-sycl PR "Extend FlashAttention Prefill with KV cache")
+//               into rings of shared-memory stages (that PR's cached-KV
+//               prefetch); plus the 128-row Q tile of a prefill item.  Pages of
+//               1, 2 or 4 tokens are gathered row by row with cp.async.
 //   warp 1      owns tensor memory and issues the tcgen05 MMAs of prefill
-//               tiles: S = Q K^T into TMEM (two buffers), O += P V into TMEM.
+//               tiles: S = Q K^T into TMEM (two buffers), O += P V into TMEM
+//               with P read from TMEM.
 //   warps 2..5  consumers.  Prefill tile: one query row per thread, masked
-//               online softmax on S read from TMEM, P written to shared memory
-//               for the next MMA, O rescaled in TMEM, epilogue.  Decode tile
+//               online softmax on S read from TMEM, P written back to TMEM for
+//               the next MMA, O rescaled in TMEM, epilogue.  Decode tile
 //               (<= 16 rows): warp-level MMAs, the four warps split the keys
 //               of each tile and merge at the end of the item.
+//   warps 7..10 (fp8 cache with prefill tiles) convert e4m3 K/V tiles and the
+//               bf16 Q tile into f16 MMA operands in shared memory.
 //
-// fp8 caches (vLLM PR, 8-bit KV cache) are converted to bf16 in shared memory
-// (exact), with k_scale folded into the logit scale and v_scale applied to the
-// normalised output; their prefill tiles use the warp-level MMA path (64 rows).
+// fp8 caches (vLLM PR, 8-bit KV cache): decode tiles convert e4m3 to f16 in
+// registers, straight into MMA fragments (exact); k_scale is folded into the
+// logit scale and v_scale applied to the normalised output.
 #include <cuda_bf16.h>
 
 #include <atomic>
@@ -732,7 +737,7 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
 }
 
 // ------------------------------------------------------------------ warp-MMA tiles of a bf16 cache (decode)
-// KPW = keys of each 128-key tile handled by one warp: 32 (decode), 128 (prefill).
+// KPW = keys of each 128-key tile handled by one warp (the four warps split a tile).
 template <int D, bool FP8, bool PF, int KPW>
 __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, const Bars& B,
                          volatile int* abort_flag, Ring& rk, Ring& rv, float sl2, float vscale) {
@@ -740,13 +745,12 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
   constexpr int NT = KPW / 8;       // S column tiles per warp
   constexpr int KS = D / 16;        // k-steps of Q K^T
   constexpr int NO = D / 8;         // O column tiles
-  constexpr bool kDecodeTile = (KPW != kKvTile);
   const int lane = threadIdx.x & 31;
   const int cw = (threadIdx.x >> 5) - 2;  // consumer warp 0..3
   const int ctid = threadIdx.x - 64;
   const int g = lane >> 2, t = lane & 3;
-  const int row_blk = kDecodeTile ? 0 : cw;
-  const int kw0 = kDecodeTile ? cw * KPW : 0;
+  const int row_blk = 0;    // a decode unit is at most 16 rows: one MMA row block
+  const int kw0 = cw * KPW;  // this warp's keys of each tile
   const int R = w.n_q * p.G;
   const int r0 = row_blk * 16 + g, r1 = r0 + 8;
 
@@ -892,7 +896,7 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
         mma_bf16(o[2 * dp + 1], a0, a1, a2, a3, b2, b3);
       }
     }
-    if (kDecodeTile && t0 + kKvTile >= w.kv_end) {
+    if (t0 + kKvTile >= w.kv_end) {
       merge_stage = rv.stage;  // released after the merge below, which uses it as scratch
     } else {
       __syncwarp();
@@ -908,103 +912,81 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
 
-  if constexpr (kDecodeTile) {
-    if (num_tiles(w) == 0) {
-      // no key at all: every row is 0 with LSE -inf (a split-KV chunk that a
-      // dynamic plan's current length left empty gives such a partial)
-      for (int idx = ctid; idx < R * D; idx += kConsumerThreads) {
-        const int row = idx / D, d = idx % D;
-        if (w.partial >= 0) {
-          p.partial_o[((int64_t)w.partial * kDecodeRows + row) * D + d] = 0.f;
-          if (d == 0) p.partial_lse[w.partial * kDecodeRows + row] = -INFINITY;
-          continue;
-        }
-        const int tok = w.q_row0 + row / p.G;
-        const int head = w.hk * p.G + row % p.G;
-        p.out[(int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head + d] = __float2bfloat16_rn(0.f);
-        if (d == 0 && p.lse != nullptr) p.lse[(int64_t)head * p.total_q + tok] = -INFINITY;
+  if (num_tiles(w) == 0) {
+    // no key at all: every row is 0 with LSE -inf (a split-KV chunk that a
+    // dynamic plan's current length left empty gives such a partial)
+    for (int idx = ctid; idx < R * D; idx += kConsumerThreads) {
+      const int row = idx / D, d = idx % D;
+      if (w.partial >= 0) {
+        p.partial_o[((int64_t)w.partial * kDecodeRows + row) * D + d] = 0.f;
+        if (d == 0) p.partial_lse[w.partial * kDecodeRows + row] = -INFINITY;
+        continue;
       }
-      return true;
+      const int tok = w.q_row0 + row / p.G;
+      const int head = w.hk * p.G + row % p.G;
+      p.out[(int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head + d] = __float2bfloat16_rn(0.f);
+      if (d == 0 && p.lse != nullptr) p.lse[(int64_t)head * p.total_q + tok] = -INFINITY;
     }
-    float* ml = reinterpret_cast<float*>(smem + L::kMlOff);
-    float* mo = reinterpret_cast<float*>(smem + L::kVOff + merge_stage * L::kTileBytes);
-    int* bad = reinterpret_cast<int*>(ml + kConsumerWarps * kDecodeRows * 2);  // [warp]: its waits failed
-    if (t == 0) {
-      ml[(cw * 16 + g) * 2 + 0] = m0;
-      ml[(cw * 16 + g) * 2 + 1] = l0;
-      ml[(cw * 16 + g + 8) * 2 + 0] = m1;
-      ml[(cw * 16 + g + 8) * 2 + 1] = l1;
-    }
-    if (lane == 0) bad[cw] = failed ? 1 : 0;
-    if (failed && lane == 0) *abort_flag = 1;
-    named_bar_sync(1, kConsumerThreads);
-    const bool any_bad = (bad[0] | bad[1] | bad[2] | bad[3]) != 0;
-    float M0 = -INFINITY, M1 = -INFINITY;
+    return true;
+  }
+  float* ml = reinterpret_cast<float*>(smem + L::kMlOff);
+  float* mo = reinterpret_cast<float*>(smem + L::kVOff + merge_stage * L::kTileBytes);
+  int* bad = reinterpret_cast<int*>(ml + kConsumerWarps * kDecodeRows * 2);  // [warp]: its waits failed
+  if (t == 0) {
+    ml[(cw * 16 + g) * 2 + 0] = m0;
+    ml[(cw * 16 + g) * 2 + 1] = l0;
+    ml[(cw * 16 + g + 8) * 2 + 0] = m1;
+    ml[(cw * 16 + g + 8) * 2 + 1] = l1;
+  }
+  if (lane == 0) bad[cw] = failed ? 1 : 0;
+  if (failed && lane == 0) *abort_flag = 1;
+  named_bar_sync(1, kConsumerThreads);
+  const bool any_bad = (bad[0] | bad[1] | bad[2] | bad[3]) != 0;
+  float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll
+  for (int ww = 0; ww < kConsumerWarps; ++ww) {
+    M0 = fmaxf(M0, ml[(ww * 16 + g) * 2]);
+    M1 = fmaxf(M1, ml[(ww * 16 + g + 8) * 2]);
+  }
+  const float f0 = ex2(m0 - (M0 == -INFINITY ? 0.f : M0));
+  const float f1 = ex2(m1 - (M1 == -INFINITY ? 0.f : M1));
+#pragma unroll
+  for (int n = 0; n < NO && !any_bad; ++n) {
+    *reinterpret_cast<float2*>(mo + (cw * 16 + g) * D + n * 8 + 2 * t) = make_float2(o[n][0] * f0, o[n][1] * f0);
+    *reinterpret_cast<float2*>(mo + (cw * 16 + g + 8) * D + n * 8 + 2 * t) =
+        make_float2(o[n][2] * f1, o[n][3] * f1);
+  }
+  named_bar_sync(1, kConsumerThreads);
+  for (int idx = ctid; idx < R * D && !any_bad; idx += kConsumerThreads) {
+    const int row = idx / D, d = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int ww = 0; ww < kConsumerWarps; ++ww) M = fmaxf(M, ml[(ww * 16 + row) * 2]);
+    const float Mu = M == -INFINITY ? 0.f : M;
+    float Lsum = 0.f, acc = 0.f;
 #pragma unroll
     for (int ww = 0; ww < kConsumerWarps; ++ww) {
-      M0 = fmaxf(M0, ml[(ww * 16 + g) * 2]);
-      M1 = fmaxf(M1, ml[(ww * 16 + g + 8) * 2]);
+      Lsum += ml[(ww * 16 + row) * 2 + 1] * ex2(ml[(ww * 16 + row) * 2] - Mu);
+      acc += mo[(ww * 16 + row) * D + d];
     }
-    const float f0 = ex2(m0 - (M0 == -INFINITY ? 0.f : M0));
-    const float f1 = ex2(m1 - (M1 == -INFINITY ? 0.f : M1));
-#pragma unroll
-    for (int n = 0; n < NO && !any_bad; ++n) {
-      *reinterpret_cast<float2*>(mo + (cw * 16 + g) * D + n * 8 + 2 * t) = make_float2(o[n][0] * f0, o[n][1] * f0);
-      *reinterpret_cast<float2*>(mo + (cw * 16 + g + 8) * D + n * 8 + 2 * t) =
-          make_float2(o[n][2] * f1, o[n][3] * f1);
-    }
-    named_bar_sync(1, kConsumerThreads);
-    for (int idx = ctid; idx < R * D && !any_bad; idx += kConsumerThreads) {
-      const int row = idx / D, d = idx % D;
-      float M = -INFINITY;
-#pragma unroll
-      for (int ww = 0; ww < kConsumerWarps; ++ww) M = fmaxf(M, ml[(ww * 16 + row) * 2]);
-      const float Mu = M == -INFINITY ? 0.f : M;
-      float Lsum = 0.f, acc = 0.f;
-#pragma unroll
-      for (int ww = 0; ww < kConsumerWarps; ++ww) {
-        Lsum += ml[(ww * 16 + row) * 2 + 1] * ex2(ml[(ww * 16 + row) * 2] - Mu);
-        acc += mo[(ww * 16 + row) * D + d];
-      }
-      const float val = Lsum > 0.f ? acc / Lsum * vscale : 0.f;
-      const float lse2 = Lsum > 0.f ? Mu + __log2f(Lsum) : -INFINITY;
-      if (w.partial >= 0) {
-        p.partial_o[((int64_t)w.partial * kDecodeRows + row) * D + d] = val;
-        if (d == 0) p.partial_lse[w.partial * kDecodeRows + row] = lse2;
-      } else {
-        const int tok = w.q_row0 + row / p.G;
-        const int head = w.hk * p.G + row % p.G;
-        p.out[(int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head + d] = __float2bfloat16_rn(val);
-        if (d == 0 && p.lse != nullptr) p.lse[(int64_t)head * p.total_q + tok] = lse2 * kLn2;
-      }
-    }
-    named_bar_sync(1, kConsumerThreads);
-    // the borrowed V stage goes back to the producer (generic writes before the next async copy)
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0 && merge_stage >= 0) mbar_arrive(&B.empty_v[merge_stage]);
-    if (any_bad) return false;
-  } else {
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int r = half ? r1 : r0;
-      if (r >= R) continue;
-      const float l = half ? l1 : l0;
-      const float m = half ? m1 : m0;
-      const float inv = l > 0.f ? vscale / l : 0.f;
-      const int tok = w.q_row0 + r / p.G;
-      const int head = w.hk * p.G + r % p.G;
-      __nv_bfloat16* dst = p.out + (int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head;
-#pragma unroll
-      for (int n = 0; n < NO; ++n) {
-        const float x = o[n][half * 2] * inv, y = o[n][half * 2 + 1] * inv;
-        *reinterpret_cast<uint32_t*>(dst + n * 8 + 2 * t) = pack_bf16(x, y);
-      }
-      if (t == 0 && p.lse != nullptr)
-        p.lse[(int64_t)head * p.total_q + tok] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+    const float val = Lsum > 0.f ? acc / Lsum * vscale : 0.f;
+    const float lse2 = Lsum > 0.f ? Mu + __log2f(Lsum) : -INFINITY;
+    if (w.partial >= 0) {
+      p.partial_o[((int64_t)w.partial * kDecodeRows + row) * D + d] = val;
+      if (d == 0) p.partial_lse[w.partial * kDecodeRows + row] = lse2;
+    } else {
+      const int tok = w.q_row0 + row / p.G;
+      const int head = w.hk * p.G + row % p.G;
+      p.out[(int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head + d] = __float2bfloat16_rn(val);
+      if (d == 0 && p.lse != nullptr) p.lse[(int64_t)head * p.total_q + tok] = lse2 * kLn2;
     }
   }
-  return true;
+  named_bar_sync(1, kConsumerThreads);
+  // the borrowed V stage goes back to the producer (generic writes before the next async copy)
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0 && merge_stage >= 0) mbar_arrive(&B.empty_v[merge_stage]);
+  return !any_bad;
 }
 
 // ------------------------------------------------------------------ fp8-cache tiles (warp MMA, f16)
@@ -1021,13 +1003,12 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
   using L = Layout<128, true, PF>;
   constexpr int D = 128;
   constexpr int NT = KPW / 8;
-  constexpr bool kDecodeTile = (KPW != kKvTile);
   const int lane = threadIdx.x & 31;
   const int cw = (threadIdx.x >> 5) - 2;
   const int ctid = threadIdx.x - 64;
   const int g = lane >> 2, t = lane & 3;
-  const int row_blk = kDecodeTile ? 0 : cw;
-  const int kw0 = kDecodeTile ? cw * KPW : 0;
+  const int row_blk = 0;    // a decode unit is at most 16 rows: one MMA row block
+  const int kw0 = cw * KPW;  // this warp's keys of each tile
   const int R = w.n_q * p.G;
   const int r0 = row_blk * 16 + g, r1 = r0 + 8;
   auto limit_of = [&](int r) {
@@ -1174,7 +1155,7 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
         }
       }
     }
-    if (kDecodeTile && t0 + kKvTile >= w.kv_end) {
+    if (t0 + kKvTile >= w.kv_end) {
       merge_stage = rv.stage;  // released after the merge below, which uses it as scratch
     } else {
       __syncwarp();
@@ -1190,153 +1171,125 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  if constexpr (kDecodeTile) {
-    if (num_tiles(w) == 0) {
-      // no key at all: every row is 0 with LSE -inf (a split-KV chunk that a
-      // dynamic plan's current length left empty gives such a partial)
-      for (int idx = ctid; idx < R * D; idx += kConsumerThreads) {
-        const int row = idx / D, dd = idx % D;
-        if (w.partial >= 0) {
-          p.partial_o[((int64_t)w.partial * kDecodeRows + row) * D + dd] = 0.f;
-          if (dd == 0) p.partial_lse[w.partial * kDecodeRows + row] = -INFINITY;
-          continue;
-        }
-        const int tok = w.q_row0 + row / p.G;
-        const int head = w.hk * p.G + row % p.G;
-        p.out[(int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head + dd] = __float2bfloat16_rn(0.f);
-        if (dd == 0 && p.lse != nullptr) p.lse[(int64_t)head * p.total_q + tok] = -INFINITY;
+  if (num_tiles(w) == 0) {
+    // no key at all: every row is 0 with LSE -inf (a split-KV chunk that a
+    // dynamic plan's current length left empty gives such a partial)
+    for (int idx = ctid; idx < R * D; idx += kConsumerThreads) {
+      const int row = idx / D, dd = idx % D;
+      if (w.partial >= 0) {
+        p.partial_o[((int64_t)w.partial * kDecodeRows + row) * D + dd] = 0.f;
+        if (dd == 0) p.partial_lse[w.partial * kDecodeRows + row] = -INFINITY;
+        continue;
       }
-      return true;
+      const int tok = w.q_row0 + row / p.G;
+      const int head = w.hk * p.G + row % p.G;
+      p.out[(int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head + dd] = __float2bfloat16_rn(0.f);
+      if (dd == 0 && p.lse != nullptr) p.lse[(int64_t)head * p.total_q + tok] = -INFINITY;
     }
-    // Merge of the four warps' partial results in the borrowed 16 KB V stage:
-    // fragments are added in fragment order (all warps share the layout),
-    // warps 2,3 into 0,1, then warp 1 into warp 0, which writes the rows.
-    float* ml = reinterpret_cast<float*>(smem + L::kMlOff);
-    float4* buf = reinterpret_cast<float4*>(smem + L::kVOff + merge_stage * L::kTileBytes);  // [2][16][32] float4
-    int* bad = reinterpret_cast<int*>(ml + kConsumerWarps * kDecodeRows * 2);  // [warp]: its waits failed
-    if (t == 0) {
-      ml[(cw * 16 + g) * 2 + 0] = m0;
-      ml[(cw * 16 + g) * 2 + 1] = l0;
-      ml[(cw * 16 + g + 8) * 2 + 0] = m1;
-      ml[(cw * 16 + g + 8) * 2 + 1] = l1;
-    }
-    if (lane == 0) bad[cw] = failed ? 1 : 0;
-    if (failed && lane == 0) *abort_flag = 1;
-    named_bar_sync(1, kConsumerThreads);
-    const bool any_bad = (bad[0] | bad[1] | bad[2] | bad[3]) != 0;
-    float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
+    return true;
+  }
+  // Merge of the four warps' partial results in the borrowed 16 KB V stage:
+  // fragments are added in fragment order (all warps share the layout),
+  // warps 2,3 into 0,1, then warp 1 into warp 0, which writes the rows.
+  float* ml = reinterpret_cast<float*>(smem + L::kMlOff);
+  float4* buf = reinterpret_cast<float4*>(smem + L::kVOff + merge_stage * L::kTileBytes);  // [2][16][32] float4
+  int* bad = reinterpret_cast<int*>(ml + kConsumerWarps * kDecodeRows * 2);  // [warp]: its waits failed
+  if (t == 0) {
+    ml[(cw * 16 + g) * 2 + 0] = m0;
+    ml[(cw * 16 + g) * 2 + 1] = l0;
+    ml[(cw * 16 + g + 8) * 2 + 0] = m1;
+    ml[(cw * 16 + g + 8) * 2 + 1] = l1;
+  }
+  if (lane == 0) bad[cw] = failed ? 1 : 0;
+  if (failed && lane == 0) *abort_flag = 1;
+  named_bar_sync(1, kConsumerThreads);
+  const bool any_bad = (bad[0] | bad[1] | bad[2] | bad[3]) != 0;
+  float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
 #pragma unroll
-    for (int ww = 0; ww < kConsumerWarps; ++ww) {
-      M0 = fmaxf(M0, ml[(ww * 16 + g) * 2]);
-      M1 = fmaxf(M1, ml[(ww * 16 + g + 8) * 2]);
-    }
-    const float Mu0 = M0 == -INFINITY ? 0.f : M0, Mu1 = M1 == -INFINITY ? 0.f : M1;
+  for (int ww = 0; ww < kConsumerWarps; ++ww) {
+    M0 = fmaxf(M0, ml[(ww * 16 + g) * 2]);
+    M1 = fmaxf(M1, ml[(ww * 16 + g + 8) * 2]);
+  }
+  const float Mu0 = M0 == -INFINITY ? 0.f : M0, Mu1 = M1 == -INFINITY ? 0.f : M1;
 #pragma unroll
-    for (int ww = 0; ww < kConsumerWarps; ++ww) {
-      L0 += ml[(ww * 16 + g) * 2 + 1] * ex2(ml[(ww * 16 + g) * 2] - Mu0);
-      L1 += ml[(ww * 16 + g + 8) * 2 + 1] * ex2(ml[(ww * 16 + g + 8) * 2] - Mu1);
-    }
-    const float f0 = ex2(m0 - Mu0), f1 = ex2(m1 - Mu1);
+  for (int ww = 0; ww < kConsumerWarps; ++ww) {
+    L0 += ml[(ww * 16 + g) * 2 + 1] * ex2(ml[(ww * 16 + g) * 2] - Mu0);
+    L1 += ml[(ww * 16 + g + 8) * 2 + 1] * ex2(ml[(ww * 16 + g + 8) * 2] - Mu1);
+  }
+  const float f0 = ex2(m0 - Mu0), f1 = ex2(m1 - Mu1);
+#pragma unroll
+  for (int n = 0; n < 16; ++n) {
+    o[n][0] *= f0;
+    o[n][1] *= f0;
+    o[n][2] *= f1;
+    o[n][3] *= f1;
+  }
+  auto put = [&](int slot) {
+#pragma unroll
+    for (int n = 0; n < 16; ++n) buf[(slot * 16 + n) * 32 + lane] = make_float4(o[n][0], o[n][1], o[n][2], o[n][3]);
+  };
+  auto add = [&](int slot) {
 #pragma unroll
     for (int n = 0; n < 16; ++n) {
-      o[n][0] *= f0;
-      o[n][1] *= f0;
-      o[n][2] *= f1;
-      o[n][3] *= f1;
+      const float4 v = buf[(slot * 16 + n) * 32 + lane];
+      o[n][0] += v.x;
+      o[n][1] += v.y;
+      o[n][2] += v.z;
+      o[n][3] += v.w;
     }
-    auto put = [&](int slot) {
-#pragma unroll
-      for (int n = 0; n < 16; ++n) buf[(slot * 16 + n) * 32 + lane] = make_float4(o[n][0], o[n][1], o[n][2], o[n][3]);
-    };
-    auto add = [&](int slot) {
-#pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        const float4 v = buf[(slot * 16 + n) * 32 + lane];
-        o[n][0] += v.x;
-        o[n][1] += v.y;
-        o[n][2] += v.z;
-        o[n][3] += v.w;
-      }
-    };
-    if (!any_bad && cw >= 2) put(cw - 2);
-    named_bar_sync(1, kConsumerThreads);
-    if (!any_bad && cw < 2) add(cw);
-    named_bar_sync(1, kConsumerThreads);
-    if (!any_bad && cw == 1) put(0);
-    named_bar_sync(1, kConsumerThreads);
-    if (!any_bad && cw == 0) {
-      add(0);
-      // O tile 4db+2h+par, column c holds d = 32db + 16h + 2c + par: a thread's
-      // (even, odd) tile pair covers d = 32db + 16h + 4t + {0,1,2,3}
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int row = half ? r1 : r0;
-        if (row >= R) continue;
-        const float Ls = half ? L1 : L0;
-        const float inv = Ls > 0.f ? vscale / Ls : 0.f;
-        const float lse2 = Ls > 0.f ? (half ? Mu1 : Mu0) + __log2f(Ls) : -INFINITY;
-        const int tok = w.q_row0 + row / p.G;
-        const int head = w.hk * p.G + row % p.G;
-#pragma unroll
-        for (int db = 0; db < 4; ++db)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const float* e = o[4 * db + 2 * h];
-            const float* d = o[4 * db + 2 * h + 1];
-            const int col = 32 * db + 16 * h + 4 * t;
-            const float4 v = make_float4(e[2 * half] * inv, d[2 * half] * inv, e[2 * half + 1] * inv,
-                                         d[2 * half + 1] * inv);
-            if (w.partial >= 0) {
-              *reinterpret_cast<float4*>(p.partial_o + ((int64_t)w.partial * kDecodeRows + row) * D + col) = v;
-            } else {
-              uint2 pk2;
-              pk2.x = pack_bf16(v.x, v.y);
-              pk2.y = pack_bf16(v.z, v.w);
-              *reinterpret_cast<uint2*>(p.out + (int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head + col) =
-                  pk2;
-            }
-          }
-        if (t == 0) {
-          if (w.partial >= 0)
-            p.partial_lse[w.partial * kDecodeRows + row] = lse2;
-          else if (p.lse != nullptr)
-            p.lse[(int64_t)head * p.total_q + tok] = lse2 * kLn2;
-        }
-      }
-    }
-    named_bar_sync(1, kConsumerThreads);
-    // the borrowed V stage goes back to the producer (generic writes before the next async copy)
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0 && merge_stage >= 0) mbar_arrive(&B.empty_v[merge_stage]);
-    if (any_bad) return false;
-  } else {
+  };
+  if (!any_bad && cw >= 2) put(cw - 2);
+  named_bar_sync(1, kConsumerThreads);
+  if (!any_bad && cw < 2) add(cw);
+  named_bar_sync(1, kConsumerThreads);
+  if (!any_bad && cw == 1) put(0);
+  named_bar_sync(1, kConsumerThreads);
+  if (!any_bad && cw == 0) {
+    add(0);
+    // O tile 4db+2h+par, column c holds d = 32db + 16h + 2c + par: a thread's
+    // (even, odd) tile pair covers d = 32db + 16h + 4t + {0,1,2,3}
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-      const int r = half ? r1 : r0;
-      if (r >= R) continue;
-      const float l = half ? l1 : l0;
-      const float m = half ? m1 : m0;
-      const float inv = l > 0.f ? vscale / l : 0.f;
-      const int tok = w.q_row0 + r / p.G;
-      const int head = w.hk * p.G + r % p.G;
-      __nv_bfloat16* dst = p.out + (int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head;
+      const int row = half ? r1 : r0;
+      if (row >= R) continue;
+      const float Ls = half ? L1 : L0;
+      const float inv = Ls > 0.f ? vscale / Ls : 0.f;
+      const float lse2 = Ls > 0.f ? (half ? Mu1 : Mu0) + __log2f(Ls) : -INFINITY;
+      const int tok = w.q_row0 + row / p.G;
+      const int head = w.hk * p.G + row % p.G;
 #pragma unroll
       for (int db = 0; db < 4; ++db)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const float* e = o[4 * db + 2 * h];
           const float* d = o[4 * db + 2 * h + 1];
-          uint2 v;
-          v.x = pack_bf16(e[half * 2] * inv, d[half * 2] * inv);
-          v.y = pack_bf16(e[half * 2 + 1] * inv, d[half * 2 + 1] * inv);
-          *reinterpret_cast<uint2*>(dst + 32 * db + 16 * h + 4 * t) = v;
+          const int col = 32 * db + 16 * h + 4 * t;
+          const float4 v = make_float4(e[2 * half] * inv, d[2 * half] * inv, e[2 * half + 1] * inv,
+                                       d[2 * half + 1] * inv);
+          if (w.partial >= 0) {
+            *reinterpret_cast<float4*>(p.partial_o + ((int64_t)w.partial * kDecodeRows + row) * D + col) = v;
+          } else {
+            uint2 pk2;
+            pk2.x = pack_bf16(v.x, v.y);
+            pk2.y = pack_bf16(v.z, v.w);
+            *reinterpret_cast<uint2*>(p.out + (int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head + col) =
+                pk2;
+          }
         }
-      if (t == 0 && p.lse != nullptr)
-        p.lse[(int64_t)head * p.total_q + tok] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+      if (t == 0) {
+        if (w.partial >= 0)
+          p.partial_lse[w.partial * kDecodeRows + row] = lse2;
+        else if (p.lse != nullptr)
+          p.lse[(int64_t)head * p.total_q + tok] = lse2 * kLn2;
+      }
     }
   }
-  return true;
+  named_bar_sync(1, kConsumerThreads);
+  // the borrowed V stage goes back to the producer (generic writes before the next async copy)
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0 && merge_stage >= 0) mbar_arrive(&B.empty_v[merge_stage]);
+  return !any_bad;
 }
 
 template <int D, bool FP8, bool PF>
