@@ -248,6 +248,16 @@ def attend(q: np.ndarray, K: np.ndarray, V: np.ndarray, causal: bool, scale: flo
     return (o, lse, w_all) if return_weights else (o, lse)
 
 
+def query_values(case, rows: np.ndarray) -> np.ndarray:
+    """Query rows as attended: the bf16 values, or -- when the call quantises Q
+    for the fp8 Q.K^T (``case.q_scale``; the fp8 "QKV" models of the vLLM page's
+    feature list and lm-eval notes) -- their e4m3 codes with the same encode as
+    the cache (one fp32 RN multiply by fp32(1/scale)), decoded times the scale."""
+    if getattr(case, "q_scale", None) is None:
+        return bf16_to_f64(rows)
+    return e4m3_decode(fp8_quantize(rows, case.q_scale)) * float(np.float32(case.q_scale))
+
+
 def forward(case, *, k_cache=None, v_cache=None):
     """The whole call: append the new K/V (if any), then attend every sequence.
 
@@ -270,7 +280,7 @@ def forward(case, *, k_cache=None, v_cache=None):
             continue
         K = gather_sequence(spec, kc, case.block_table, b, lk, case.k_scale)
         V = gather_sequence(spec, vc, case.block_table, b, lk, case.v_scale)
-        q = bf16_to_f64(case.q[cu_q[b]:cu_q[b] + lq])
+        q = query_values(case, case.q[cu_q[b]:cu_q[b] + lq])
         o, l = attend(q, K, V, spec.causal, spec.softmax_scale)
         out[cu_q[b]:cu_q[b] + lq] = o
         lse[:, cu_q[b]:cu_q[b] + lq] = l
@@ -300,7 +310,7 @@ def forward_rows(case, k_cache_after, v_cache_after, rows: Iterable[tuple[int, i
         # query i is row i of a length-lq block; keep its causal horizon exact
         horizon = i + (lk - lq) + 1 if spec.causal else lk
         horizon = max(0, min(lk, horizon))
-        q = bf16_to_f64(case.q[cu_q[b] + i:cu_q[b] + i + 1])
+        q = query_values(case, case.q[cu_q[b] + i:cu_q[b] + i + 1])
         oi, li = attend(q, K[:horizon], V[:horizon], False, spec.softmax_scale)
         if horizon == 0:
             oi[:] = 0.0

@@ -138,6 +138,7 @@ class Case:
     prefix_v: Optional[np.ndarray] = None
     k_scale: float = 1.0                 # fp32 per-tensor scales (fp8 only)
     v_scale: float = 1.0
+    q_scale: Optional[float] = None      # fp8 only: Q quantised to e4m3 for Q K^T with this scale
     sentinel: str = "finite"             # "finite" | "nan" fill of unused slots
     extra: dict = field(default_factory=dict)
 

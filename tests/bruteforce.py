@@ -114,6 +114,11 @@ def run(case):
             for h in range(Hq):
                 hk = h // G
                 qv = [bf16(x) for x in case.q[t0 + i][h]]
+                if getattr(case, "q_scale", None) is not None:  # Q quantised for Q K^T
+                    np_ = __import__("numpy")
+                    inv_q = float(np_.float32(1.0) / np_.float32(case.q_scale))
+                    qs = float(np_.float32(case.q_scale))
+                    qv = [fp8_value(fp8_nearest(f32mul(x, inv_q))) * qs for x in qv]
                 scores = []
                 for j in range(lk):
                     if spec.causal and j > i + lk - lq:

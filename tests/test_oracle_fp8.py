@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 
 import oracle
+import synth
 from tests import bruteforce
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -105,3 +106,42 @@ def test_quantize_uses_single_fp32_multiply():
     x = (x_bits.astype(np.uint32) << 16).view(np.float32)
     want = oracle.e4m3_encode((x * inv).astype(np.float32))
     assert np.array_equal(oracle.fp8_quantize(x_bits, scale), want)
+
+
+# ---------------------------------------------------------------------------
+# quantised queries (Q . K^T on fp8): the same encode as the cache
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("seed", range(12))
+def test_quantised_queries_against_bruteforce(seed):
+    """Oracle with q_scale vs the brute force's own nearest-code encode of Q."""
+    import dataclasses
+    from tests import bruteforce
+    case = synth.random_case(500 + seed, cache_dtype="fp8")
+    amax = float(np.abs(synth.bf16_bits_to_f32(case.q)).max())
+    case = dataclasses.replace(case, q_scale=float(np.float32(max(amax, 1e-3) / 448.0)))
+    ref = oracle.forward(case)
+    out, lse, _, _ = bruteforce.run(case)
+    np.testing.assert_allclose(ref["out"], np.array(out, dtype=np.float64).reshape(ref["out"].shape), rtol=0,
+                               atol=1e-12)
+    lse_b = np.array(lse, dtype=np.float64).reshape(ref["lse"].shape)
+    assert np.array_equal(np.isfinite(ref["lse"]), np.isfinite(lse_b))
+    fin = np.isfinite(lse_b)
+    np.testing.assert_allclose(ref["lse"][fin], lse_b[fin], rtol=0, atol=1e-12)
+
+
+def test_quantised_queries_identity_on_representable_values():
+    """Queries that are e4m3 codes times the scale quantise to themselves: the
+    call with q_scale then equals the plain call."""
+    import dataclasses
+    case = synth.random_case(77, cache_dtype="fp8", batch=3)
+    q_scale = float(np.float32(0.03125))           # a power of two: code * scale is exact in bf16
+    rng = np.random.default_rng(3)
+    codes = rng.integers(0, 0x7E, size=case.q.shape, dtype=np.int64).astype(np.uint8)
+    codes[rng.random(case.q.shape) < 0.5] |= 0x80
+    vals = (oracle.e4m3_decode(codes) * q_scale).astype(np.float32)
+    q_bits = synth.f32_to_bf16_bits(vals)
+    assert np.array_equal(synth.bf16_bits_to_f32(q_bits), vals)   # exactly representable
+    plain = dataclasses.replace(case, q=q_bits)
+    quant = dataclasses.replace(plain, q_scale=q_scale)
+    a, b = oracle.forward(plain), oracle.forward(quant)
+    assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["lse"], b["lse"])
