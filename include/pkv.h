@@ -114,6 +114,14 @@ typedef struct {
                                     pages): sequence b's pages are block_table[
                                     page_indptr[b] + i], i < page_indptr[b+1] -
                                     page_indptr[b]; block_table_stride is ignored.  */
+  const float* q_scale;          /* nullable; fp8 cache only.  Q is quantised to e4m3
+                                    with this per-tensor scale (the cache's encode:
+                                    code = e4m3_rn_satfinite(q * fp32(1/scale))) and
+                                    Q.K^T runs on fp8 tensor cores, as for the fp8
+                                    "QKV" models of the vLLM PR "[Kernel][Triton][FP8]
+                                    ..." (feature list, lm-eval notes); P.V stays f16.
+                                    Decode tiles only: a plan with prefill tiles
+                                    returns PKV_ERR_UNSUPPORTED.                     */
 } pkv_fwd_args;
 
 typedef struct pkv_plan_s* pkv_plan_t;

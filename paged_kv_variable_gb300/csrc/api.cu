@@ -238,6 +238,8 @@ extern "C" pkv_status pkv_attn_varlen_kvcache_fwd(const pkv_problem* problem, co
     return fail(PKV_ERR_INVALID_ARG, "the plan appends %d tokens but k_new / v_new are NULL", plan->total_new);
   if (plan->total_new == 0 && has_new)
     return fail(PKV_ERR_INVALID_ARG, "k_new given but the plan was made with no new tokens");
+  if (args->q_scale && (pr.cache_dtype != PKV_FP8_E4M3 || plan->num_prefill_items > 0))
+    return fail(PKV_ERR_UNSUPPORTED, "q_scale (fp8 Q.K^T) needs an fp8 cache and a plan of decode tiles only");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   int* status = reinterpret_cast<int*>(ws + plan->layout.status);
@@ -281,6 +283,7 @@ extern "C" pkv_status pkv_attn_varlen_kvcache_fwd(const pkv_problem* problem, co
   p.causal = pr.causal;
   p.scale_log2 = pr.softmax_scale * 1.4426950408889634f;
   p.k_scale = args->k_scale;
+  p.q_scale = args->q_scale;
   p.v_scale = args->v_scale;
   p.items = reinterpret_cast<const WorkItem*>(ws + plan->layout.items);
   p.cta_begin = reinterpret_cast<const int32_t*>(ws + plan->layout.cta_begin);

@@ -997,7 +997,13 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
 // V: ldmatrix.trans on byte pairs gives a thread (key 2t, 2t+1) x (d 2g, 2g+1);
 // a byte permute splits that into the fragment of column d = 2g (even O tile)
 // and of d = 2g+1 (odd O tile); the epilogue puts O columns back in order.
-template <bool PF, int KPW>
+//
+// QF8 (q_scale given): Q is quantised to e4m3 and S = Q K^T runs as
+// m16n8k32 e4m3 MMAs straight on the cached K bytes (no K conversion).  The
+// same d permutation serves both operands: for k-step ks = 2G+h, thread t's
+// k slots 4t..4t+3 and 16+4t..16+4t+3 are dims 16(4G+t) + 8h + {0..3 | 4..7},
+// i.e. words 2h and 2h+1 of the 16-byte chunk 4G+t of a key row.
+template <bool PF, int KPW, bool QF8>
 __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* smem, const Bars& B,
                              volatile int* abort_flag, Ring& rk, Ring& rv, float sl2, float vscale) {
   using L = Layout<128, true, PF>;
@@ -1019,7 +1025,7 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
   };
   const int lim0 = limit_of(r0), lim1 = limit_of(r1);
 
-  uint32_t qa[8][4];
+  uint32_t qa[8][4];  // f16 fragments (8 k-steps of 16), or e4m3 ones (QF8: 4 k-steps of 32)
   {
     const __nv_bfloat16* q0 = nullptr;
     const __nv_bfloat16* q1 = nullptr;
@@ -1027,13 +1033,35 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
       q0 = p.q + (int64_t)(w.q_row0 + r0 / p.G) * p.q_stride_tok + (int64_t)(w.hk * p.G + r0 % p.G) * p.q_stride_head;
     if (r1 < R)
       q1 = p.q + (int64_t)(w.q_row0 + r1 / p.G) * p.q_stride_tok + (int64_t)(w.hk * p.G + r1 % p.G) * p.q_stride_head;
+    if constexpr (QF8) {
+      // the cache's encode: one IEEE reciprocal, an RN multiply per value, RN satfinite to e4m3
+      const float inv_q = __frcp_rn(__ldg(p.q_scale));
+      auto quant4 = [&](uint32_t w0, uint32_t w1) -> uint32_t {
+        auto lo = [](uint32_t v) { return __uint_as_float(v << 16); };
+        auto hi = [](uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); };
+        const uint32_t a = f32x2_to_e4m3x2(__fmul_rn(lo(w0), inv_q), __fmul_rn(hi(w0), inv_q));
+        const uint32_t b = f32x2_to_e4m3x2(__fmul_rn(lo(w1), inv_q), __fmul_rn(hi(w1), inv_q));
+        return a | (b << 16);
+      };
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const int d0 = 64 * (ks >> 2) + 16 * t + 4 * (ks & 3);
-      qa[ks][0] = q0 ? bf16x2_to_f16x2(ld_u32(q0 + d0)) : 0u;
-      qa[ks][1] = q1 ? bf16x2_to_f16x2(ld_u32(q1 + d0)) : 0u;
-      qa[ks][2] = q0 ? bf16x2_to_f16x2(ld_u32(q0 + d0 + 2)) : 0u;
-      qa[ks][3] = q1 ? bf16x2_to_f16x2(ld_u32(q1 + d0 + 2)) : 0u;
+      for (int ks = 0; ks < 4; ++ks) {
+        const int d0 = 16 * (4 * (ks >> 1) + t) + 8 * (ks & 1);
+        const uint4 v0 = q0 ? __ldg(reinterpret_cast<const uint4*>(q0 + d0)) : make_uint4(0, 0, 0, 0);
+        const uint4 v1 = q1 ? __ldg(reinterpret_cast<const uint4*>(q1 + d0)) : make_uint4(0, 0, 0, 0);
+        qa[ks][0] = quant4(v0.x, v0.y);
+        qa[ks][1] = quant4(v1.x, v1.y);
+        qa[ks][2] = quant4(v0.z, v0.w);
+        qa[ks][3] = quant4(v1.z, v1.w);
+      }
+    } else {
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const int d0 = 64 * (ks >> 2) + 16 * t + 4 * (ks & 3);
+        qa[ks][0] = q0 ? bf16x2_to_f16x2(ld_u32(q0 + d0)) : 0u;
+        qa[ks][1] = q1 ? bf16x2_to_f16x2(ld_u32(q1 + d0)) : 0u;
+        qa[ks][2] = q0 ? bf16x2_to_f16x2(ld_u32(q0 + d0 + 2)) : 0u;
+        qa[ks][3] = q1 ? bf16x2_to_f16x2(ld_u32(q1 + d0 + 2)) : 0u;
+      }
     }
   }
 
@@ -1063,11 +1091,16 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
       for (int G = 0; G < 2; ++G) {
         const uint4 kv = lds_u128(kraw + key * 128 + ((((4 * G + t) ^ (key & 7))) << 4));
         const uint32_t wd[4] = {kv.x, kv.y, kv.z, kv.w};
+        if constexpr (QF8) {
+          mma_e4m3(s[nt], qa[2 * G][0], qa[2 * G][1], qa[2 * G][2], qa[2 * G][3], wd[0], wd[1]);
+          mma_e4m3(s[nt], qa[2 * G + 1][0], qa[2 * G + 1][1], qa[2 * G + 1][2], qa[2 * G + 1][3], wd[2], wd[3]);
+        } else {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int ks = 4 * G + u;
-          mma_f16(s[nt], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], e4m3x2_to_f16x2(wd[u]),
-                  e4m3x2_to_f16x2(wd[u] >> 16));
+          for (int u = 0; u < 4; ++u) {
+            const int ks = 4 * G + u;
+            mma_f16(s[nt], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], e4m3x2_to_f16x2(wd[u]),
+                    e4m3x2_to_f16x2(wd[u] >> 16));
+          }
         }
       }
     }
@@ -1292,7 +1325,7 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
   return !any_bad;
 }
 
-template <int D, bool FP8, bool PF>
+template <int D, bool FP8, bool PF, bool QF8>
 __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, volatile int* abort_flag, uint32_t tmem,
                          int it0, int it1) {
   using L = Layout<D, FP8, PF>;
@@ -1307,6 +1340,8 @@ __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
   const float kscale = FP8 ? __ldg(p.k_scale) : 1.f;
   const float vscale = FP8 ? __ldg(p.v_scale) : 1.f;
   const float sl2 = p.scale_log2 * kscale;
+  // quantised queries: S = codes(Q) . codes(K), times q_scale and k_scale
+  const float sl2q = (FP8 && p.q_scale) ? sl2 * __ldg(p.q_scale) : sl2;
   Ring rk, rv;
   uint32_t pt = 0;
   for (int it = it0; it < it1; ++it) {
@@ -1315,7 +1350,8 @@ __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
     if (w.kind == kDecode) {
       if (mma_consumer) {
         if constexpr (FP8)
-          ok = run_item_fp8<PF, kKvTile / kConsumerWarps>(p, w, smem, B, abort_flag, rk, rv, sl2, vscale);
+          ok = run_item_fp8<PF, kKvTile / kConsumerWarps, QF8>(p, w, smem, B, abort_flag, rk, rv, QF8 ? sl2q : sl2,
+                                                                vscale);
         else
           ok = run_item<D, FP8, PF, kKvTile / kConsumerWarps>(p, w, smem, B, abort_flag, rk, rv, sl2, vscale);
       } else {
@@ -1336,7 +1372,7 @@ __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
   return true;
 }
 
-template <int D, bool FP8, bool PF>
+template <int D, bool FP8, bool PF, bool QF8>
 __global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
     attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q) {
@@ -1446,7 +1482,7 @@ __global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
       __syncwarp();
     }
   } else {
-    consumer<D, FP8, PF>(p, smem, B, abort_flag, tmem, it0, it1);
+    consumer<D, FP8, PF, QF8>(p, smem, B, abort_flag, tmem, it0, it1);
   }
   // warps 1..5: every tensor-memory access is done before warp 1 frees it
   tc_fence_before();
@@ -1455,7 +1491,7 @@ __global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
   if (L::kTc && warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int D, bool FP8, bool PF>
+template <int D, bool FP8, bool PF, bool QF8 = false>
 cudaError_t launch_t(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
                      int num_ctas, bool overlap_prev, cudaStream_t s) {
   using L = Layout<D, FP8, PF>;
@@ -1467,7 +1503,7 @@ cudaError_t launch_t(const AttnParams& p, const CUtensorMap& tk, const CUtensorM
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(configured.load() & bit)) {
-    e = cudaFuncSetAttribute(attn_kernel<D, FP8, PF>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    e = cudaFuncSetAttribute(attn_kernel<D, FP8, PF, QF8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
@@ -1481,7 +1517,7 @@ cudaError_t launch_t(const AttnParams& p, const CUtensorMap& tk, const CUtensorM
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = overlap_prev ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, attn_kernel<D, FP8, PF>, p, tk, tv, tq);
+  return cudaLaunchKernelEx(&cfg, attn_kernel<D, FP8, PF, QF8>, p, tk, tv, tq);
 }
 
 }  // namespace
@@ -1492,7 +1528,8 @@ cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tm_k, const
   if (num_ctas == 0) return cudaSuccess;
   const bool o = overlap_prev;
   if (fp8)
-    return has_prefill ? launch_t<128, true, true>(p, tm_k, tm_v, tm_q, num_ctas, o, stream)
+    return has_prefill  ? launch_t<128, true, true>(p, tm_k, tm_v, tm_q, num_ctas, o, stream)
+           : p.q_scale ? launch_t<128, true, false, true>(p, tm_k, tm_v, tm_q, num_ctas, o, stream)
                        : launch_t<128, true, false>(p, tm_k, tm_v, tm_q, num_ctas, o, stream);
   if (head_dim == 128)
     return has_prefill ? launch_t<128, false, true>(p, tm_k, tm_v, tm_q, num_ctas, o, stream)

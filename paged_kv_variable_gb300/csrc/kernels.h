@@ -65,6 +65,7 @@ struct AttnParams {
   float scale_log2;    // softmax_scale * log2(e)
   const float* k_scale;
   const float* v_scale;
+  const float* q_scale;  // nullable (fp8 cache, decode tiles): Q quantised to e4m3 for Q K^T
   const WorkItem* items;
   const int32_t* cta_begin;
   float* partial_o;

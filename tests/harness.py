@@ -69,6 +69,8 @@ class GpuCase:
                     if with_lse else None)
         self.k_scale = torch.tensor([case.k_scale], dtype=torch.float32, device=device)
         self.v_scale = torch.tensor([case.v_scale], dtype=torch.float32, device=device)
+        self.q_scale = (None if getattr(case, "q_scale", None) is None else
+                        torch.tensor([case.q_scale], dtype=torch.float32, device=device))
         num_pages = case.num_pages if spec.paged else spec.batch
         self.problem = pkv.make_problem(batch=spec.batch, num_heads_q=spec.hq, num_heads_kv=spec.hkv,
                                         head_dim=spec.d, page_size=spec.page_size, cache_capacity=spec.capacity,
@@ -89,7 +91,7 @@ class GpuCase:
             k_new=self.k_new if with_new else None, v_new=self.v_new if with_new else None,
             cu_seqlens_knew=self.cu_new if with_new else None, block_table=self.block_table,
             k_scale=self.k_scale if spec.cache_dtype == "fp8" else None,
-            v_scale=self.v_scale if spec.cache_dtype == "fp8" else None)
+            v_scale=self.v_scale if spec.cache_dtype == "fp8" else None, q_scale=self.q_scale)
 
     def write_prefix(self):
         """fp8 cases: write the cached prefix with the library's own append."""

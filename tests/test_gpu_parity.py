@@ -469,3 +469,25 @@ def test_small_pages_decode(P, cache_dtype):
     ref = oracle.forward(case)
     H.compare_out(g.out, ref["out"], H.FP8_TOL if cache_dtype == "fp8" else H.BF16_TOL)
     H.compare_lse(g.lse, ref["lse"])
+
+
+@pytest.mark.parametrize("P,G,split", [(16, 4, False), (16, 4, True), (0, 8, False), (8, 1, True)])
+def test_fp8_quantised_queries_decode(P, G, split):
+    """fp8 cache with q_scale: Q quantised to e4m3 and Q.K^T on fp8 tensor cores
+    (decode tiles), against the oracle's quantised-query reading."""
+    import dataclasses
+    rng = np.random.default_rng(160 + P + G)
+    spec = synth.uniform_spec("fp8-q8-decode", 5, 1, 1800 if split else 400, hq=2 * G, hkv=2, d=128, page_size=P,
+                              cache_dtype="fp8")
+    case = synth.make_case(spec, rng)
+    amax = float(np.abs(synth.bf16_bits_to_f32(case.q)).max())
+    case = dataclasses.replace(case, q_scale=float(np.float32(amax / 448.0)))
+    g = H.GpuCase(case, num_sms=4 if split else 152)
+    assert (g.plan.stats()["num_split_units"] > 0) == split
+    g.write_prefix()
+    g.run()                                          # q_scale goes in with the other arguments
+    assert g.status() == 0
+    ref = oracle.forward(case)
+    H.compare_out(g.out, ref["out"], H.FP8_TOL)
+    H.compare_lse(g.lse, ref["lse"])
+
