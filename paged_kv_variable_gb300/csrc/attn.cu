@@ -4,7 +4,8 @@
 // "[Refactor] Uniform PoDAttention API with Horizontal Fusion SMs Schedule",
 // Key Changes 2: prefill and decode work share one persistent launch).
 //
-// Warp roles (224 threads; 352 with the fp8 converters):
+// Warp roles (224 threads without prefill tiles; 256 with them, 384 for an
+// fp8 cache):
 //   warps 0, 6  TMA producers (K and Q; V): tiles of 128 keys, boxes of up to
 //               128 rows per (page, 128-byte column chunk), page numbers read from
 //               block_table or a ragged page list (vLLM PR "[Kernel][Triton][FP8]
@@ -15,9 +16,10 @@
 //               into rings of shared-memory stages (that PR's cached-KV
 //               prefetch); plus the 128-row Q tile of a prefill item.  Pages of
 //               1, 2 or 4 tokens are gathered row by row with cp.async.
-//   warp 1      owns tensor memory and issues the tcgen05 MMAs of prefill
-//               tiles: S = Q K^T into TMEM (two buffers), O += P V into TMEM
-//               with P read from TMEM.
+//   warp 1      owns tensor memory and issues S = Q K^T of prefill tiles into
+//               TMEM (three buffers).
+//   last warp   (with prefill tiles) issues O += P V into TMEM, P read from
+//               TMEM where the softmax wrote it over S.
 //   warps 2..5  consumers.  Prefill tile: one query row per thread, masked
 //               online softmax on S read from TMEM, P written back to TMEM for
 //               the next MMA, O rescaled in TMEM, epilogue.  Decode tile
@@ -44,24 +46,27 @@ namespace {
 constexpr int kConsumerWarps = 4;                  // warp-MMA consumers (decode, fp8 prefill): warps 2..5
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr float kLn2 = 0.693147180559945309f;
-// Tensor memory: S buffers [0,128) and [128,256) (fp32), O [256, 256+D) (fp32),
-// P buffers [384,448) and [448,512) (bf16 pairs: 128 keys in 64 columns).
+// Tensor memory: S buffers [0,128), [128,256), [256,384) (fp32), O [384, 384+D)
+// (fp32).  P of a tile (bf16 or f16 pairs: 128 keys in 64 columns) overwrites
+// the first 64 columns of its own S buffer once the softmax has read S, so a
+// buffer is free again when P V of its tile has completed.
 constexpr uint32_t kTmemCols = 512;
-constexpr int kSBufs = 2;             // S = Q K^T of tile j+2 is issued before P V of tile j
-constexpr uint32_t kTmemO = 256;
-constexpr uint32_t kTmemP = 384;
+constexpr int kSBufs = 3;             // S of tile T+3 waits only for P V of tile T
+constexpr uint32_t kTmemO = 384;
 
 template <int D, bool FP8, bool PF>
 struct Layout {
-  // Warp roles: 0 K/Q producer, 1 MMA issuer, 2..5 consumers (softmax of
-  // prefill tiles, warp-MMA decode tiles), 6 V producer, and for an fp8 cache
-  // 7..10 converters (e4m3 K/V tiles and the bf16 Q tile to f16 MMA operands).
+  // Warp roles: 0 K/Q producer, 1 S = Q K^T issuer, 2..5 consumers (softmax
+  // of prefill tiles, warp-MMA decode tiles), 6 V producer, for an fp8 cache
+  // 7..10 converters (e4m3 K/V tiles and the bf16 Q tile to f16 MMA
+  // operands), and with prefill tiles a last warp issuing O += P V.
   static constexpr bool kTc = PF;                           // prefill tiles (on tcgen05) in the plan
   static constexpr int kSoftmaxWarps = kConsumerWarps;      // one per TMEM lane quarter
   static constexpr int kVProducerWarp = 2 + kSoftmaxWarps;
   static constexpr int kConvWarp0 = kVProducerWarp + 1;
   static constexpr int kConvWarps = (FP8 && PF) ? 4 : 0;
-  static constexpr int kThreads = 32 * (3 + kSoftmaxWarps + kConvWarps);
+  static constexpr int kPvWarp = kConvWarp0 + kConvWarps;
+  static constexpr int kThreads = 32 * (3 + kSoftmaxWarps + kConvWarps + (PF ? 1 : 0));
   static constexpr int kEsize = FP8 ? 1 : 2;
   // decode-only plans give all shared memory to the rings
   static constexpr int kStagesK = PF ? (FP8 ? 2 : (D == 128 ? 3 : 4)) : (FP8 || D == 64 ? 6 : 4);
@@ -77,7 +82,7 @@ struct Layout {
   // decode merge scratch: the item's last V stage, borrowed before it is released
   static constexpr int kMlOff = kVcOff + (kConvWarps ? 2 * kConvTile : 0);  // float[4][16][2] (m, l), int[4]
   static constexpr int kBarOff = kMlOff + kConsumerWarps * kDecodeRows * 2 * 4 + 16;  // + failed-wait flags
-  static constexpr int kNumBars = 2 * kStagesK + 2 * kStagesV + 3 + 2 * kSBufs + 4 + 9;
+  static constexpr int kNumBars = 2 * kStagesK + 2 * kStagesV + 3 + 3 * kSBufs + 9 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;     // tmem base, abort flag
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes;                       // base is 1024-aligned (checked in the kernel)
@@ -90,10 +95,10 @@ struct Bars {
   uint64_t* empty_v;
   uint64_t* q_full;
   uint64_t* q_empty;
-  uint64_t* s_full;   // [kSBufs] S of a tile is in TMEM
-  uint64_t* s_free;   // [kSBufs] the softmax has read it
-  uint64_t* p_full;   // [2] P of a tile is in shared memory (and O rescaled)
-  uint64_t* o_done;   // [2] P V of a tile has completed
+  // per S buffer (tile T uses T % kSBufs)
+  uint64_t* s_full;   // S of the tile is in TMEM
+  uint64_t* p_full;   // P of the tile is in TMEM (and O rescaled, V rows past the sequence zeroed)
+  uint64_t* o_done;   // P V of the tile has completed: the buffer is free
   uint64_t* drain;    // MMA completion before tensor memory is freed after an abort
   // fp8 cache only
   uint64_t* qc_full;   // the Q tile is f16
@@ -101,6 +106,7 @@ struct Bars {
   uint64_t* kc_empty;  // [2] S of the tile using it has completed
   uint64_t* vc_full;   // [2] converted V tile ready
   uint64_t* vc_empty;  // [2] P V of the tile using it has completed
+  uint64_t* drain_pv;  // P V MMA completion before tensor memory is freed after an abort
 };
 
 // Byte offset of 16-byte chunk c of row r in a bf16 tile stored as
@@ -330,128 +336,108 @@ __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CU
   if (!dep_done) grid_dep_wait();
 }
 
-// ------------------------------------------------------------------ MMA issuer (prefill tiles)
-// Order per item with n tiles: S_0, S_1, then for each j: S_{j+2}, P_j V_j.
-// S_{j+2} needs S buffer j % 2 read by the softmax of tile j; P_j V_j needs
-// P_j (tensor-memory buffer j % 2, written by the softmax) and V_j.  With an
-// fp8 cache the K and V operands are the converted f16 tiles (buffer T % 2)
-// and Q is f16 too.
+// ------------------------------------------------------------------ MMA issuers (prefill tiles)
+// Two threads issue the tcgen05 MMAs of prefill tiles, each queue in order:
+// warp 1 S_j = Q K_j^T (needs K_j, and S buffer j % 3 free: P V of tile j-3
+// completed), the P V warp O += P_j V_j (needs P_j, written by the softmax
+// into S buffer j % 3, and V_j).  An MMA issue does not return while the
+// tensor pipe is busy with the ones before it, so with one thread per queue
+// the waits and bookkeeping of one overlap the other's MMAs.  With an fp8
+// cache the K and V operands are the converted f16 tiles (buffer T % 2) and Q
+// is f16 too.
 template <int D, bool FP8, bool PF>
-__device__ bool mma_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, volatile int* abort_flag,
-                           uint32_t tmem, int it0, int it1) {
+__device__ bool s_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, volatile int* abort_flag, uint32_t tmem,
+                         int it0, int it1) {
   using L = Layout<D, FP8, PF>;
   constexpr int kAB = FP8 ? 0 : 1;  // operand type: f16 or bf16
   constexpr uint32_t kIdescQK = idesc_f16(kAB, 0, 128, 128);
-  constexpr uint32_t kIdescPV = idesc_f16(kAB, 1, 128, D);
   const uint32_t q_base = smem_u32(smem + L::kQOff);
-  Ring rk, rv;
+  Ring rk;
   uint32_t pt = 0, pi = 0;
-
-  auto issue_s = [&](uint32_t T) -> bool {
-    const uint32_t b = T % kSBufs, use = T / kSBufs;
-    uint32_t k_base;
-    if constexpr (FP8) {
-      if (!mbar_wait(&B.kc_full[T & 1], (T >> 1) & 1, abort_flag)) return false;
-      k_base = smem_u32(smem + L::kKcOff + (T & 1) * L::kConvTile);
-    } else {
-      if (!mbar_wait(&B.full_k[rk.stage], rk.phase, abort_flag)) return false;
-      k_base = smem_u32(smem + L::kKOff + rk.stage * L::kTileBytes);
-    }
-    if (use >= 1 && !mbar_wait(&B.s_free[b], (use - 1) & 1, abort_flag)) return false;
-    tc_fence_after();
-#pragma unroll
-    for (int k = 0; k < D / 16; ++k) {
-      const uint32_t off = (k >> 2) * (kKvTile * 128) + (k & 3) * 32;
-      umma_ss(tmem + b * 128, sdesc_sw128(q_base + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024), kIdescQK,
-              k > 0 ? 1u : 0u);
-    }
-    umma_commit(&B.s_full[b]);  // bf16: the softmax warps release the K stage once they have seen S complete
-    if constexpr (FP8) umma_commit(&B.kc_empty[T & 1]);
-    rk.advance<L::kStagesK>();
-    return true;
-  };
-  auto issue_pv = [&](uint32_t T, bool first) -> bool {
-    if (!mbar_wait(&B.p_full[T & 1], (T >> 1) & 1, abort_flag)) return false;
-    uint32_t v_base;
-    if constexpr (FP8) {
-      if (!mbar_wait(&B.vc_full[T & 1], (T >> 1) & 1, abort_flag)) return false;
-      v_base = smem_u32(smem + L::kVcOff + (T & 1) * L::kConvTile);
-    } else {
-      if (!mbar_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
-      v_base = smem_u32(smem + L::kVOff + rv.stage * L::kTileBytes);
-    }
-    tc_fence_after();
-    const uint32_t p_tmem = tmem + kTmemP + (T & 1) * 64;
-#pragma unroll
-    for (int k = 0; k < kKvTile / 16; ++k) {
-      const uint64_t bd = sdesc_sw128(v_base + k * 16 * 128, kKvTile * 128, 1024);
-      umma_ts(tmem + kTmemO, p_tmem + k * 8, bd, kIdescPV, (first && k == 0) ? 0u : 1u);
-    }
-    umma_commit(&B.o_done[T & 1]);
-    if constexpr (FP8) {
-      umma_commit(&B.vc_empty[T & 1]);
-    } else {
-      // the V stage barrier expects one arrival per consumer warp (as the decode
-      // warps give): all but one now, the last when these MMAs complete
-      mbar_arrive_cnt(&B.empty_v[rv.stage], kConsumerWarps - 1);
-      umma_commit(&B.empty_v[rv.stage]);
-    }
-    rv.advance<L::kStagesV>();
-    return true;
-  };
-
   for (int it = it0; it < it1; ++it) {
     const WorkItem w = load_item(p, it);
     const int n = num_tiles(w);
     if (w.kind != kPrefill) {
       rk.advance<L::kStagesK>(n);
-      rv.advance<L::kStagesV>(n);
       continue;
     }
     if (n == 0) continue;
     if (!mbar_wait(FP8 ? B.qc_full : B.q_full, pi & 1, abort_flag)) return false;
-    {
-      // Two queues, each in order: S_j (K_j loaded -- converted, for an fp8
-      // cache -- and S buffer j % 2 read by the softmax of tile j-2) and P_j V_j
-      // (P_j written, V_j loaded).  Whichever head is ready is issued, so a K
-      // tile still in flight does not hold up a P V whose completion the
-      // softmax is waiting for.
-      int ns = 0, npv = 0;
-      uint64_t t_last = globaltimer_ns();
-      while (npv < n) {
-        bool progressed = false;
-        if (npv < ns) {
-          const uint32_t T = pt + npv;
-          const bool v_ready = FP8 ? mbar_test_wait(&B.vc_full[T & 1], (T >> 1) & 1)
-                                   : mbar_test_wait(&B.full_v[rv.stage], rv.phase);
-          if (mbar_test_wait(&B.p_full[T & 1], (T >> 1) & 1) && v_ready) {
-            if (!issue_pv(T, npv == 0)) return false;  // its waits are already satisfied
-            ++npv;
-            progressed = true;
-          }
-        }
-        if (ns < n && ns < npv + 3) {  // S runs up to two tiles ahead of P V
-          const uint32_t T = pt + ns, b = T % kSBufs, use = T / kSBufs;
-          const bool k_ready = FP8 ? mbar_test_wait(&B.kc_full[T & 1], (T >> 1) & 1)
-                                   : mbar_test_wait(&B.full_k[rk.stage], rk.phase);
-          if (k_ready && (use == 0 || mbar_test_wait(&B.s_free[b], (use - 1) & 1))) {
-            if (!issue_s(T)) return false;
-            if (ns == n - 1) umma_commit(B.q_empty);
-            ++ns;
-            progressed = true;
-          }
-        }
-        if (progressed) {
-          t_last = globaltimer_ns();
-        } else {
-          if (*abort_flag) return false;
-          if (globaltimer_ns() - t_last > kWaitLimitNs) return false;
-          __nanosleep(32);
-        }
+    for (int j = 0; j < n; ++j) {
+      const uint32_t T = pt + j, b = T % kSBufs, use = T / kSBufs;
+      uint32_t k_base;
+      if constexpr (FP8) {
+        if (!mbar_wait(&B.kc_full[T & 1], (T >> 1) & 1, abort_flag)) return false;
+        k_base = smem_u32(smem + L::kKcOff + (T & 1) * L::kConvTile);
+      } else {
+        if (!mbar_wait(&B.full_k[rk.stage], rk.phase, abort_flag)) return false;
+        k_base = smem_u32(smem + L::kKOff + rk.stage * L::kTileBytes);
       }
+      // the buffer last held S and P of tile T - kSBufs: P V of that tile has completed
+      if (use >= 1 && !mbar_wait(&B.o_done[b], (use - 1) & 1, abort_flag)) return false;
+      tc_fence_after();
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = (k >> 2) * (kKvTile * 128) + (k & 3) * 32;
+        umma_ss(tmem + b * 128, sdesc_sw128(q_base + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024), kIdescQK,
+                k > 0 ? 1u : 0u);
+      }
+      umma_commit(&B.s_full[b]);  // bf16: the softmax warps release the K stage once they have seen S complete
+      if constexpr (FP8) umma_commit(&B.kc_empty[T & 1]);
+      rk.advance<L::kStagesK>();
     }
+    umma_commit(B.q_empty);
     pt += n;
     ++pi;
+  }
+  return true;
+}
+
+template <int D, bool FP8, bool PF>
+__device__ bool pv_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, volatile int* abort_flag, uint32_t tmem,
+                          int it0, int it1) {
+  using L = Layout<D, FP8, PF>;
+  constexpr int kAB = FP8 ? 0 : 1;
+  constexpr uint32_t kIdescPV = idesc_f16(kAB, 1, 128, D);
+  Ring rv;
+  uint32_t pt = 0;
+  for (int it = it0; it < it1; ++it) {
+    const WorkItem w = load_item(p, it);
+    const int n = num_tiles(w);
+    if (w.kind != kPrefill) {
+      rv.advance<L::kStagesV>(n);
+      continue;
+    }
+    for (int j = 0; j < n; ++j) {
+      const uint32_t T = pt + j, b = T % kSBufs;
+      if (!mbar_wait(&B.p_full[b], (T / kSBufs) & 1, abort_flag)) return false;
+      uint32_t v_base;
+      if constexpr (FP8) {
+        if (!mbar_wait(&B.vc_full[T & 1], (T >> 1) & 1, abort_flag)) return false;
+        v_base = smem_u32(smem + L::kVcOff + (T & 1) * L::kConvTile);
+      } else {
+        if (!mbar_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
+        v_base = smem_u32(smem + L::kVOff + rv.stage * L::kTileBytes);
+      }
+      tc_fence_after();
+      const uint32_t p_tmem = tmem + b * 128;  // P over the first 64 columns of the tile's S buffer
+#pragma unroll
+      for (int k = 0; k < kKvTile / 16; ++k) {
+        const uint64_t bd = sdesc_sw128(v_base + k * 16 * 128, kKvTile * 128, 1024);
+        umma_ts(tmem + kTmemO, p_tmem + k * 8, bd, kIdescPV, (j == 0 && k == 0) ? 0u : 1u);
+      }
+      umma_commit(&B.o_done[b]);
+      if constexpr (FP8) {
+        umma_commit(&B.vc_empty[T & 1]);
+      } else {
+        // the V stage barrier expects one arrival per consumer warp (as the decode
+        // warps give): all but one now, the last when these MMAs complete
+        mbar_arrive_cnt(&B.empty_v[rv.stage], kConsumerWarps - 1);
+        umma_commit(&B.empty_v[rv.stage]);
+      }
+      rv.advance<L::kStagesV>();
+    }
+    pt += n;
   }
   return true;
 }
@@ -544,9 +530,10 @@ __device__ bool converter(const AttnParams& p, uint8_t* smem, const Bars& B, vol
 
 // ------------------------------------------------------------------ prefill tile softmax (tcgen05 path)
 // Four warps, one query row per thread (TMEM lane), all 128 keys of a tile.
-// P of tile T goes to tensor-memory buffer T % 2, so it only waits for P V of
-// tile T-2; O is rescaled (which needs P V of tile T-1 done) only when a row's
-// running max moves.  bf16 cache: P is bf16, this warp releases the K stage
+// P of tile T overwrites the S it was computed from (its S buffer is only
+// reused once P V of the tile has completed), so the softmax never waits for
+// a P buffer; O is rescaled (which needs P V of tile T-1 done) only when a
+// row's running max moves.  bf16 cache: P is bf16, this warp releases the K stage
 // and zeroes V rows past the sequence.  fp8 cache: P is f16 (the MMA runs on
 // f16), the converter warps own the raw stages and the zeroing, S is read in
 // two 64-column passes (fewer live registers in the larger block), and the
@@ -593,13 +580,9 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
       for (int c = 0; c < kPass / 32; ++c) tmem_ld32(t_lane + s_col + h * kPass + c * 32, s + c * 32);
       tmem_wait_ld();
       if constexpr (!FP8) {
-        // all of S is in registers now: release the S buffer and the K stage
-        tc_fence_before();
+        // S of this tile is complete: its K stage is free
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&B.s_free[sb]);
-          mbar_arrive(&B.empty_k[rk.stage]);  // S of this tile is complete: its K stage is free
-        }
+        if (lane == 0) mbar_arrive(&B.empty_k[rk.stage]);
       }
       if (need_mask) {
 #pragma unroll
@@ -624,9 +607,6 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
     const float alpha = bump ? ex2(m - mu) : 1.f;
     m = m_new;
 
-    // P buffer T % 2 is free once P V of tile T-2 has completed
-    if (j >= 2 && !warp_wait(&B.o_done[T & 1], ((T - 2) >> 1) & 1, abort_flag)) return false;
-    tc_fence_after();
     // probabilities two at a time: one packed FMA for the scaled logits, one
     // packed add into the row sum
     const uint64_t sl2x2 = f32x2(sl2, sl2), nmu2 = f32x2(-mu, -mu);
@@ -655,12 +635,7 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
       }
 #pragma unroll
       for (int c = 0; c < kPass / 64; ++c)
-        tmem_st32(t_lane + kTmemP + (T & 1) * 64 + h * (kPass / 2) + c * 32, pk + c * 32);
-    }
-    if constexpr (FP8) {
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&B.s_free[sb]);
+        tmem_st32(t_lane + s_col + h * (kPass / 2) + c * 32, pk + c * 32);
     }
     float q0, q1, q2, q3;
     f32x2_split(sum2[0], q0, q1);
@@ -680,7 +655,7 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
     }
     if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
       // O must hold P V of tile T-1 before it is rescaled
-      if (!warp_wait(&B.o_done[(T - 1) & 1], ((T - 1) >> 1) & 1, abort_flag)) return false;
+      if (!warp_wait(&B.o_done[(T - 1) % kSBufs], ((T - 1) / kSBufs) & 1, abort_flag)) return false;
       tc_fence_after();
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -696,7 +671,7 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
     fence_proxy_async_smem();  // the zeroed V rows (generic stores) before the MMA reads them
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&B.p_full[T & 1]);
+    if (lane == 0) mbar_arrive(&B.p_full[sb]);
     rk.advance<L::kStagesK>();
     rv.advance<L::kStagesV>();
   }
@@ -705,7 +680,7 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
   __nv_bfloat16* dst = p.out + (int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head;
   if (n > 0) {
     const uint32_t T = pt + n - 1;
-    if (!warp_wait(&B.o_done[T & 1], (T >> 1) & 1, abort_flag)) return false;
+    if (!warp_wait(&B.o_done[T % kSBufs], (T / kSBufs) & 1, abort_flag)) return false;
     tc_fence_after();
     const float inv = l > 0.f ? vscale / l : 0.f;
 #pragma unroll
@@ -1394,14 +1369,14 @@ __global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
   B.q_empty = B.q_full + 1;
   B.drain = B.q_full + 2;
   B.s_full = B.q_full + 3;
-  B.s_free = B.s_full + kSBufs;
-  B.p_full = B.s_free + kSBufs;
-  B.o_done = B.p_full + 2;
-  B.qc_full = B.o_done + 2;
+  B.p_full = B.s_full + kSBufs;
+  B.o_done = B.p_full + kSBufs;
+  B.qc_full = B.o_done + kSBufs;
   B.kc_full = B.qc_full + 1;
   B.kc_empty = B.kc_full + 2;
   B.vc_full = B.kc_empty + 2;
   B.vc_empty = B.vc_full + 2;
+  B.drain_pv = B.vc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1421,9 +1396,6 @@ __global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
     mbar_init(B.q_empty, 1);
     for (int i = 0; i < kSBufs; ++i) {
       mbar_init(&B.s_full[i], 1);
-      mbar_init(&B.s_free[i], L::kSoftmaxWarps);
-    }
-    for (int i = 0; i < 2; ++i) {
       mbar_init(&B.p_full[i], L::kSoftmaxWarps);
       mbar_init(&B.o_done[i], 1);
     }
@@ -1437,6 +1409,7 @@ __global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
       }
     }
     mbar_init(B.drain, 1);
+    mbar_init(B.drain_pv, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -1459,7 +1432,7 @@ __global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
     return;
   }
   if constexpr (L::kConvWarps > 0) {
-    if (warp >= L::kConvWarp0) {
+    if (warp >= L::kConvWarp0 && warp < L::kConvWarp0 + L::kConvWarps) {
       if (!converter<D, PF>(p, smem, B, abort_flag, it0, it1)) {
         if (lane == 0) record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, -2);
         *abort_flag = 1;
@@ -1467,16 +1440,18 @@ __global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
       return;
     }
   }
-  if (warp == 1) {
+  if (warp == 1 || (L::kTc && warp == L::kPvWarp)) {
     if constexpr (L::kTc) {
       if (lane == 0) {
-        if (!mma_issuer<D, FP8, PF>(p, smem, B, abort_flag, tmem, it0, it1)) {
-          record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, -1);
+        const bool pv = warp == L::kPvWarp;
+        if (!(pv ? pv_issuer<D, FP8, PF>(p, smem, B, abort_flag, tmem, it0, it1)
+                 : s_issuer<D, FP8, PF>(p, smem, B, abort_flag, tmem, it0, it1))) {
+          record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, pv ? -3 : -1);
           *abort_flag = 1;
-          // wait (bounded) for the MMAs already issued before the memory is freed
+          // wait (bounded) for this thread's MMAs already issued before the memory is freed
           int zero = 0;
-          umma_commit(B.drain);
-          mbar_wait(B.drain, 0, &zero);
+          umma_commit(pv ? B.drain_pv : B.drain);
+          mbar_wait(pv ? B.drain_pv : B.drain, 0, &zero);
         }
       }
       __syncwarp();
@@ -1484,9 +1459,9 @@ __global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
   } else {
     consumer<D, FP8, PF, QF8>(p, smem, B, abort_flag, tmem, it0, it1);
   }
-  // warps 1..5: every tensor-memory access is done before warp 1 frees it
+  // warps 1..5 and the P V warp: every tensor-memory access is done before warp 1 frees it
   tc_fence_before();
-  named_bar_sync(2, 32 * (1 + L::kSoftmaxWarps));
+  named_bar_sync(2, 32 * (1 + L::kSoftmaxWarps + (L::kTc ? 1 : 0)));
   tc_fence_after();
   if (L::kTc && warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
