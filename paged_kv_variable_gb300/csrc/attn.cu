@@ -642,7 +642,8 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
     f32x2_split(sum2[1], q2, q3);
     l = l * alpha + ((q0 + q2) + (q1 + q3));
 
-    if (!FP8 && t0 + kKvTile > w.lk) {
+    const bool zero_v = !FP8 && t0 + kKvTile > w.lk;
+    if (zero_v) {
       // rows past the sequence may hold anything (even NaN): zero them in V
       if (!warp_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
       if (t0 + r >= w.lk) {
@@ -668,7 +669,7 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
       }
     }
     tmem_wait_st();
-    fence_proxy_async_smem();  // the zeroed V rows (generic stores) before the MMA reads them
+    if (zero_v) fence_proxy_async_smem();  // the zeroed V rows (generic stores) before the MMA reads them
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&B.p_full[sb]);
