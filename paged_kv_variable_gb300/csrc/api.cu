@@ -271,6 +271,8 @@ extern "C" pkv_status pkv_attn_varlen_kvcache_fwd(const pkv_problem* problem, co
   p.out = static_cast<__nv_bfloat16*>(args->out);
   p.o_stride_tok = args->o_stride_tok;
   p.o_stride_head = args->o_stride_head;
+  p.out_v8 = (reinterpret_cast<uintptr_t>(args->out) % 32 == 0) && (args->o_stride_tok % 16 == 0) &&
+             (args->o_stride_head % 16 == 0);
   p.lse = args->lse;
   p.total_q = plan->total_q;
   p.block_table = args->block_table;

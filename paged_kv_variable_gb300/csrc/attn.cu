@@ -690,14 +690,22 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
       tmem_ld32(t_lane + kTmemO + c * 32, o);
       tmem_wait_ld();
       if (valid) {
+        uint4 v[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          uint4 v;
-          v.x = pack_bf16(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
-          v.y = pack_bf16(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
-          v.z = pack_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
-          v.w = pack_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
-          *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) = v;
+          v[q].x = pack_bf16(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+          v[q].y = pack_bf16(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+          v[q].z = pack_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+          v[q].w = pack_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+        }
+        // a row is written in 32-byte pieces where it is aligned for them (whole
+        // sectors, half the store instructions), else in 16-byte ones
+        if (p.out_v8) {
+          st_global_v8(dst + c * 32, v[0], v[1]);
+          st_global_v8(dst + c * 32 + 16, v[2], v[3]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) = v[q];
         }
       }
     }
@@ -1322,6 +1330,11 @@ __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
   uint32_t pt = 0;
   for (int it = it0; it < it1; ++it) {
     const WorkItem w = load_item(p, it);
+    if (it + 1 < it1) {
+      // the next descriptor is in L1 when this item ends
+      prefetch_l1(p.items + it + 1);
+      prefetch_l1(reinterpret_cast<const char*>(p.items + it + 2) - 1);
+    }
     bool ok = true;
     if (w.kind == kDecode) {
       if (mma_consumer) {

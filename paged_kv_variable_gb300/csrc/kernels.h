@@ -48,6 +48,7 @@ struct AttnParams {
   int64_t q_stride_tok, q_stride_head;
   __nv_bfloat16* out;
   int64_t o_stride_tok, o_stride_head;
+  int32_t out_v8;      // every output row starts on 32 bytes: prefill rows are written 32 bytes per store
   float* lse;
   int32_t total_q;
   const int32_t* block_table;

@@ -57,6 +57,33 @@ def test_random_fp8(seed):
     run_full(H.gpu_random_case(100 + seed, cache_dtype="fp8", sentinel="nan" if seed % 2 else "finite"))
 
 
+@pytest.mark.parametrize("layout", ["head_pad", "base_offset"])
+@pytest.mark.parametrize("cache_dtype", ["bf16", "fp8"])
+def test_output_rows_not_32_byte_aligned(layout, cache_dtype):
+    """Output rows on 16 but not 32 bytes (a padded head stride, or a base 16
+    bytes past a 32-byte boundary): the 16-byte store path, same results."""
+    import torch
+    case = synth.random_case(7, batch=3, hq=8, hkv=2, d=128, page_size=16, causal=True, cache_dtype=cache_dtype,
+                             max_cache=300, max_new=200, allow_zero=False)
+    spec = case.spec
+    g = H.GpuCase(case)
+    g.write_prefix()
+    shape = (spec.total_q, spec.hq, spec.d)
+    if layout == "head_pad":
+        big = torch.full((spec.total_q, spec.hq, spec.d + 8), float("nan"), dtype=torch.bfloat16, device="cuda")
+        g.out = big[:, :, :spec.d]
+        assert (g.out.stride(1) * 2) % 32 == 16
+    else:
+        big = torch.full((spec.total_q * spec.hq * spec.d + 8,), float("nan"), dtype=torch.bfloat16, device="cuda")
+        g.out = big[8:].view(shape)
+        assert g.out.data_ptr() % 32 == 16
+    g.run()
+    assert g.status() == 0, g.pkv.last_error()
+    ref = oracle.forward(case)
+    H.compare_out(g.out.contiguous(), ref["out"], tol_for(case))
+    H.compare_lse(g.lse, ref["lse"])
+
+
 @pytest.mark.parametrize("seed", range(8))
 def test_cache_only_and_ragged_queries(seed):
     # no new K/V (cache-only attention) and query lengths unrelated to new lengths
