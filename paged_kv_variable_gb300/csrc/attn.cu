@@ -528,6 +528,57 @@ __device__ bool converter(const AttnParams& p, uint8_t* smem, const Bars& B, vol
   return true;
 }
 
+// ------------------------------------------------------------------ prefill epilogue
+// The epilogue of a prefill item (O / l to bf16 rows, the LSE) is deferred:
+// it runs inside the next prefill item's first tile, once that tile's P is in
+// tensor memory and before the softmax lets P V of the tile (which starts O
+// afresh) be issued, or at the end of the CTA's work.  So the softmax warps do
+// not wait for the item's last P V to complete: by then it has, and the S of
+// the next item's tiles are already in tensor memory.
+struct PendingEpi {
+  bool has = false;                // warp-uniform
+  uint32_t T = 0;                  // the item's last tile: O is final once its P V has completed
+  float inv = 0.f;                 // scale of the output (v_scale / l, or 0)
+  float lse = 0.f;                 // natural-log LSE of the row
+  __nv_bfloat16* dst = nullptr;    // this thread's output row (null: none)
+  float* lse_dst = nullptr;
+};
+
+// Writes the pending item's rows (waits for its last P V), 32 columns at a time
+template <int D>
+__device__ __forceinline__ bool epi_run(const AttnParams& p, const Bars& B, const PendingEpi& e, uint32_t t_lane,
+                                        volatile int* abort_flag) {
+  if (!warp_wait(&B.o_done[e.T % kSBufs], (e.T / kSBufs) & 1, abort_flag)) return false;
+  tc_fence_after();
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t o[32];
+    tmem_ld32(t_lane + kTmemO + c * 32, o);
+    tmem_wait_ld();
+    if (e.dst != nullptr) {
+      uint4 v[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        v[q].x = pack_bf16(__uint_as_float(o[8 * q + 0]) * e.inv, __uint_as_float(o[8 * q + 1]) * e.inv);
+        v[q].y = pack_bf16(__uint_as_float(o[8 * q + 2]) * e.inv, __uint_as_float(o[8 * q + 3]) * e.inv);
+        v[q].z = pack_bf16(__uint_as_float(o[8 * q + 4]) * e.inv, __uint_as_float(o[8 * q + 5]) * e.inv);
+        v[q].w = pack_bf16(__uint_as_float(o[8 * q + 6]) * e.inv, __uint_as_float(o[8 * q + 7]) * e.inv);
+      }
+      // a row is written in 32-byte pieces where it is aligned for them (whole
+      // sectors, half the store instructions), else in 16-byte ones
+      if (p.out_v8) {
+        st_global_v8(e.dst + c * 32, v[0], v[1]);
+        st_global_v8(e.dst + c * 32 + 16, v[2], v[3]);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(e.dst + c * 32 + q * 8) = v[q];
+      }
+    }
+  }
+  if (e.lse_dst != nullptr) *e.lse_dst = e.lse;
+  return true;
+}
+
 // ------------------------------------------------------------------ prefill tile softmax (tcgen05 path)
 // Four warps, one query row per thread (TMEM lane), all 128 keys of a tile.
 // P of tile T overwrites the S it was computed from (its S buffer is only
@@ -541,7 +592,7 @@ __device__ bool converter(const AttnParams& p, uint8_t* smem, const Bars& B, vol
 template <int D, bool FP8, bool PF>
 __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, const Bars& B,
                              volatile int* abort_flag, uint32_t tmem, Ring& rk, Ring& rv, uint32_t& pt, float sl2,
-                             float vscale) {
+                             float vscale, PendingEpi& pend) {
   using L = Layout<D, FP8, PF>;
   constexpr int kPass = FP8 ? 64 : 128;      // S columns held in registers at a time
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -668,6 +719,13 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
         tmem_st32(t_lane + kTmemO + c * 32, o);
       }
     }
+    // the previous item's O is written out before P V of this item's first tile
+    // may replace it (bf16 cache; with an fp8 cache the register budget of the
+    // larger block keeps the epilogue at the end of its own item)
+    if (!FP8 && j == 0 && pend.has) {
+      if (!epi_run<D>(p, B, pend, t_lane, abort_flag)) return false;
+      pend.has = false;
+    }
     tmem_wait_st();
     if (zero_v) fence_proxy_async_smem();  // the zeroed V rows (generic stores) before the MMA reads them
     tc_fence_before();
@@ -677,45 +735,30 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
     rv.advance<L::kStagesV>();
   }
 
-  // epilogue: O / l -> bf16 rows, natural-log LSE
+  // epilogue: O / l -> bf16 rows and the natural-log LSE, deferred to the next
+  // prefill item's first tile (or the end of the CTA's work)
   __nv_bfloat16* dst = p.out + (int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head;
+  float* lse_dst = (valid && p.lse != nullptr) ? p.lse + (int64_t)head * p.total_q + tok : nullptr;
+  const float lse = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
   if (n > 0) {
-    const uint32_t T = pt + n - 1;
-    if (!warp_wait(&B.o_done[T % kSBufs], (T / kSBufs) & 1, abort_flag)) return false;
-    tc_fence_after();
-    const float inv = l > 0.f ? vscale / l : 0.f;
-#pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t o[32];
-      tmem_ld32(t_lane + kTmemO + c * 32, o);
-      tmem_wait_ld();
-      if (valid) {
-        uint4 v[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          v[q].x = pack_bf16(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
-          v[q].y = pack_bf16(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
-          v[q].z = pack_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
-          v[q].w = pack_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
-        }
-        // a row is written in 32-byte pieces where it is aligned for them (whole
-        // sectors, half the store instructions), else in 16-byte ones
-        if (p.out_v8) {
-          st_global_v8(dst + c * 32, v[0], v[1]);
-          st_global_v8(dst + c * 32 + 16, v[2], v[3]);
-        } else {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) = v[q];
-        }
-      }
+    pend.has = true;
+    pend.T = pt + n - 1;
+    pend.inv = l > 0.f ? vscale / l : 0.f;
+    pend.lse = lse;
+    pend.dst = valid ? dst : nullptr;
+    pend.lse_dst = lse_dst;
+    if constexpr (FP8) {
+      if (!epi_run<D>(p, B, pend, t_lane, abort_flag)) return false;
+      tc_fence_before();
+      pend.has = false;
     }
-    tc_fence_before();
-  } else if (valid) {
+  } else {
+    if (valid) {
 #pragma unroll
-    for (int c = 0; c < D / 8; ++c) *reinterpret_cast<uint4*>(dst + c * 8) = make_uint4(0, 0, 0, 0);
+      for (int c = 0; c < D / 8; ++c) *reinterpret_cast<uint4*>(dst + c * 8) = make_uint4(0, 0, 0, 0);
+    }
+    if (lse_dst != nullptr) *lse_dst = lse;
   }
-  if (valid && p.lse != nullptr)
-    p.lse[(int64_t)head * p.total_q + tok] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
   pt += n;
   return true;
 }
@@ -1328,6 +1371,7 @@ __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
   const float sl2q = (FP8 && p.q_scale) ? sl2 * __ldg(p.q_scale) : sl2;
   Ring rk, rv;
   uint32_t pt = 0;
+  PendingEpi pend;
   for (int it = it0; it < it1; ++it) {
     const WorkItem w = load_item(p, it);
     if (it + 1 < it1) {
@@ -1348,7 +1392,7 @@ __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
         rv.advance<L::kStagesV>(num_tiles(w));
       }
     } else if constexpr (PF) {
-      ok = softmax_item<D, FP8, PF>(p, w, smem, B, abort_flag, tmem, rk, rv, pt, sl2, vscale);
+      ok = softmax_item<D, FP8, PF>(p, w, smem, B, abort_flag, tmem, rk, rv, pt, sl2, vscale, pend);
     } else {
       ok = false;  // a decode-only launch never receives prefill tiles
     }
@@ -1356,6 +1400,18 @@ __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
       record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, it);
       *abort_flag = 1;
       return false;
+    }
+  }
+  if constexpr (PF && !FP8) {
+    if (pend.has) {
+      // the last prefill item's epilogue
+      const int qw = (threadIdx.x >> 5) & 3;
+      if (!epi_run<D>(p, B, pend, tmem + ((uint32_t)(qw * 32) << 16), abort_flag)) {
+        record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, it1);
+        *abort_flag = 1;
+        return false;
+      }
+      tc_fence_before();
     }
   }
   return true;
