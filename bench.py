@@ -287,11 +287,12 @@ def e2e_decode(case, steps, warmup, device, mode="graph"):
     cu_seqlens), the call, and the device -> host copy of the output, then a
     stream synchronisation, all inside the timed region.
 
-    mode="graph": the serving-loop form -- a decode plan for the lengths made
-    once (pkv_plan_decode_dynamic, which reads the lengths on the device) and
-    the call captured once in a CUDA graph; each step copies its inputs in and
-    replays the graph.  mode="host_plan": each step also makes the plan on the
-    host and uploads it before an eager call."""
+    mode="graph": the serving-loop form -- a plan made once and the call
+    captured once in a CUDA graph; each step copies its inputs in and replays
+    the graph.  For a decode batch the plan is pkv_plan_decode_dynamic's (the
+    lengths are read on the device at every call); a batch with prefill rows
+    takes a plan for its own lengths.  mode="host_plan": each step also makes
+    the plan on the host and uploads it before an eager call."""
     import torch
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from tests import harness as H
@@ -314,7 +315,11 @@ def e2e_decode(case, steps, warmup, device, mode="graph"):
     stream = torch.cuda.current_stream()
 
     if mode == "graph":
-        pl = pkv.plan_decode_dynamic(g.problem, spec.q_lens, spec.cache_lens, spec.new_lens, nsms)
+        decode_only = bool(np.all(spec.q_lens * (spec.hq // spec.hkv) <= 16))
+        if decode_only:
+            pl = pkv.plan_decode_dynamic(g.problem, spec.q_lens, spec.cache_lens, spec.new_lens, nsms)
+        else:
+            pl = pkv.plan(g.problem, spec.q_lens, spec.cache_lens, spec.new_lens, nsms)
         ws = pkv.workspace_tensor(pl.workspace_bytes, device)
         pl.upload(ws)
         args = g.args()
@@ -504,8 +509,9 @@ def gpu_arm(args):
             "cpu_baseline": cpu_base,
             "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 4),
-                    "form": "host buffers -> copies in, replay of the captured call (decode plan made once with "
-                            "pkv_plan_decode_dynamic), copy out, synchronise; wall clock",
+                    "form": "host buffers -> copies in, replay of the captured call (plan made once: "
+                            "pkv_plan_decode_dynamic for a decode batch, else a plan for its lengths), copy out, "
+                            "synchronise; wall clock",
                     "host_plan_each_step": {
                         "value": round(main.work["bytes"] * world / (e2e_hp_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                         "ms_per_step": round(e2e_hp_ms, 4), "h2d_bytes_per_step": int(h2d_hp)}},
