@@ -281,6 +281,18 @@ def flush_l2(bufs):
     bufs[1].sum()
 
 
+# what each --workload runs (the default is the headline decode batch; the
+# others exist for profiler captures)
+WORKLOAD_NAMES = {
+    "decode": "decode: B=64, 1 query + 1 appended token each, Hq=32, Hkv=8, D=128, bf16 paged cache page 16 "
+              "(seeded permutation), cache lens U[512,4096]",
+    "decode-small": "decode: 16 sequences of the B=64 decode batch (profiler captures)",
+    "prefill": "prefill: B=8, 512 new tokens on a 1536-token cached prefix, Hq=32, Hkv=8, D=128, bf16 "
+               "contiguous cache, causal (profiler captures)",
+    "fp8-decode": "decode at kv length 2048 on the fp8 cache of the B=64 fp8 prefill (profiler captures)",
+}
+
+
 def e2e_decode(case, steps, warmup, device, mode="graph"):
     """The same step through the public API from HOST buffers, wall-clock timed:
     pinned-host -> device copies of the step's inputs (q, new K/V, lengths,
@@ -493,8 +505,7 @@ def gpu_arm(args):
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(t_step, 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": "decode: B=64, 1 query + 1 appended token each, Hq=32, Hkv=8, D=128, bf16 "
-                                   "paged cache page 16 (seeded permutation), cache lens U[512,4096]",
+            "config": {"workload": WORKLOAD_NAMES.get(args.workload, args.workload),
                        "step": "kv append + persistent attention + split-KV combine (one library call)",
                        "launch": "CUDA graph replay of the captured library call, one per step",
                        "l2": "flushed before every timed step (256 MB write, then a 256 MB read of another "
