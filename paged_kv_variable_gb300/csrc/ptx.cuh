@@ -88,6 +88,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 // lane then observes the completed phase itself (acquire).  All lanes of the
 // warp must call it; they all leave with the same result.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  // common case first: the phase has completed and every lane sees it at once
+  // (a non-blocking test, which acquires like the wait)
+  if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
   int ok = 1;
   if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
