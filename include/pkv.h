@@ -120,8 +120,9 @@ typedef struct {
                                     Q.K^T runs on fp8 tensor cores, as for the fp8
                                     "QKV" models of the vLLM PR "[Kernel][Triton][FP8]
                                     ..." (feature list, lm-eval notes); P.V stays f16.
-                                    Decode tiles only: a plan with prefill tiles
-                                    returns PKV_ERR_UNSUPPORTED.                     */
+                                    Decode tiles use warp-level e4m3 MMAs, prefill
+                                    tiles tcgen05 kind::f8f6f4 on the raw cache tile.
+                                    A bf16 cache returns PKV_ERR_UNSUPPORTED.        */
 } pkv_fwd_args;
 
 typedef struct pkv_plan_s* pkv_plan_t;

@@ -238,8 +238,8 @@ extern "C" pkv_status pkv_attn_varlen_kvcache_fwd(const pkv_problem* problem, co
     return fail(PKV_ERR_INVALID_ARG, "the plan appends %d tokens but k_new / v_new are NULL", plan->total_new);
   if (plan->total_new == 0 && has_new)
     return fail(PKV_ERR_INVALID_ARG, "k_new given but the plan was made with no new tokens");
-  if (args->q_scale && (pr.cache_dtype != PKV_FP8_E4M3 || plan->num_prefill_items > 0))
-    return fail(PKV_ERR_UNSUPPORTED, "q_scale (fp8 Q.K^T) needs an fp8 cache and a plan of decode tiles only");
+  if (args->q_scale && pr.cache_dtype != PKV_FP8_E4M3)
+    return fail(PKV_ERR_UNSUPPORTED, "q_scale (fp8 Q.K^T) needs an fp8 cache");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   int* status = reinterpret_cast<int*>(ws + plan->layout.status);

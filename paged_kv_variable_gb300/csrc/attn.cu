@@ -345,13 +345,17 @@ __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CU
 // the waits and bookkeeping of one overlap the other's MMAs.  With an fp8
 // cache the K and V operands are the converted f16 tiles (buffer T % 2) and Q
 // is f16 too.
-template <int D, bool FP8, bool PF>
+// QF8 (fp8 cache with q_scale): the converter warps quantise Q to e4m3 (into
+// the first converted-K buffer) and S = Q K^T runs as kind::f8f6f4 MMAs on the
+// raw e4m3 K stage, which this thread releases when the MMAs have completed;
+// the converters then turn only V into f16.
+template <int D, bool FP8, bool PF, bool QF8>
 __device__ bool s_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, volatile int* abort_flag, uint32_t tmem,
                          int it0, int it1) {
   using L = Layout<D, FP8, PF>;
-  constexpr int kAB = FP8 ? 0 : 1;  // operand type: f16 or bf16
+  constexpr int kAB = FP8 ? 0 : 1;  // operand type: f16 or bf16 (e4m3 for QF8: the same code)
   constexpr uint32_t kIdescQK = idesc_f16(kAB, 0, 128, 128);
-  const uint32_t q_base = smem_u32(smem + L::kQOff);
+  const uint32_t q_base = smem_u32(smem + (QF8 ? L::kKcOff : L::kQOff));
   Ring rk;
   uint32_t pt = 0, pi = 0;
   for (int it = it0; it < it1; ++it) {
@@ -366,7 +370,7 @@ __device__ bool s_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
     for (int j = 0; j < n; ++j) {
       const uint32_t T = pt + j, b = T % kSBufs, use = T / kSBufs;
       uint32_t k_base;
-      if constexpr (FP8) {
+      if constexpr (FP8 && !QF8) {
         if (!mbar_wait(&B.kc_full[T & 1], (T >> 1) & 1, abort_flag)) return false;
         k_base = smem_u32(smem + L::kKcOff + (T & 1) * L::kConvTile);
       } else {
@@ -376,14 +380,29 @@ __device__ bool s_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
       // the buffer last held S and P of tile T - kSBufs: P V of that tile has completed
       if (use >= 1 && !mbar_wait(&B.o_done[b], (use - 1) & 1, abort_flag)) return false;
       tc_fence_after();
+      if constexpr (QF8) {
+        // e4m3 rows of 128 bytes (one swizzle atom wide): K=32 per MMA, 32 bytes apart
 #pragma unroll
-      for (int k = 0; k < D / 16; ++k) {
-        const uint32_t off = (k >> 2) * (kKvTile * 128) + (k & 3) * 32;
-        umma_ss(tmem + b * 128, sdesc_sw128(q_base + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024), kIdescQK,
-                k > 0 ? 1u : 0u);
+        for (int k = 0; k < D / 32; ++k)
+          umma_ss_e4m3(tmem + b * 128, sdesc_sw128(q_base + k * 32, 16, 1024),
+                       sdesc_sw128(k_base + k * 32, 16, 1024), kIdescQK, k > 0 ? 1u : 0u);
+      } else {
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * (kKvTile * 128) + (k & 3) * 32;
+          umma_ss(tmem + b * 128, sdesc_sw128(q_base + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024),
+                  kIdescQK, k > 0 ? 1u : 0u);
+        }
       }
       umma_commit(&B.s_full[b]);  // bf16: the softmax warps release the K stage once they have seen S complete
-      if constexpr (FP8) umma_commit(&B.kc_empty[T & 1]);
+      if constexpr (QF8) {
+        // the raw K stage barrier expects one arrival per consumer warp: all but
+        // one now, the last when these MMAs complete
+        mbar_arrive_cnt(&B.empty_k[rk.stage], kConsumerWarps - 1);
+        umma_commit(&B.empty_k[rk.stage]);
+      } else if constexpr (FP8) {
+        umma_commit(&B.kc_empty[T & 1]);
+      }
       rk.advance<L::kStagesK>();
     }
     umma_commit(B.q_empty);
@@ -466,7 +485,7 @@ __device__ __forceinline__ void convert_tile(const uint8_t* raw, uint8_t* conv, 
   }
 }
 
-template <int D, bool PF>
+template <int D, bool PF, bool QF8>
 __device__ bool converter(const AttnParams& p, uint8_t* smem, const Bars& B, volatile int* abort_flag, int it0,
                           int it1) {
   using L = Layout<D, true, PF>;
@@ -483,14 +502,40 @@ __device__ bool converter(const AttnParams& p, uint8_t* smem, const Bars& B, vol
       continue;
     }
     if (n == 0) continue;
-    // Q: bf16 -> f16 in place (elementwise, so the swizzle does not matter)
     if (!warp_wait(B.q_full, pi & 1, abort_flag)) return false;
-    uint4* q = reinterpret_cast<uint4*>(smem + L::kQOff);
+    if constexpr (QF8) {
+      // Q: bf16 -> e4m3 with the cache's encode (one IEEE reciprocal of q_scale,
+      // an RN multiply per value, RN satfinite), into the first converted-K
+      // buffer as [128 rows][128 B] swizzled: the 16 values of e4m3 chunk c of
+      // row r come from bf16 chunks 2c and 2c+1 of that row
+      const float inv_q = __frcp_rn(__ldg(p.q_scale));
+      auto quant4 = [&](uint32_t w0, uint32_t w1) -> uint32_t {
+        auto lo = [](uint32_t v) { return __uint_as_float(v << 16); };
+        auto hi = [](uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); };
+        const uint32_t a = f32x2_to_e4m3x2(__fmul_rn(lo(w0), inv_q), __fmul_rn(hi(w0), inv_q));
+        const uint32_t b = f32x2_to_e4m3x2(__fmul_rn(lo(w1), inv_q), __fmul_rn(hi(w1), inv_q));
+        return a | (b << 16);
+      };
+      const uint8_t* qb = smem + L::kQOff;
+      uint8_t* q8 = smem + L::kKcOff;
+#pragma unroll 2
+      for (int k = 0; k < 8; ++k) {
+        const int u = ct + 128 * k;
+        const int r = u >> 3, c = u & 7;
+        const uint4 a = *reinterpret_cast<const uint4*>(qb + tile_off(r, 2 * c));
+        const uint4 b = *reinterpret_cast<const uint4*>(qb + tile_off(r, 2 * c + 1));
+        *reinterpret_cast<uint4*>(q8 + r * 128 + ((c ^ (r & 7)) << 4)) =
+            make_uint4(quant4(a.x, a.y), quant4(a.z, a.w), quant4(b.x, b.y), quant4(b.z, b.w));
+      }
+    } else {
+      // Q: bf16 -> f16 in place (elementwise, so the swizzle does not matter)
+      uint4* q = reinterpret_cast<uint4*>(smem + L::kQOff);
 #pragma unroll 4
-    for (int k = 0; k < kKvTile * D * 2 / 16 / 128; ++k) {
-      uint4 v = q[ct + 128 * k];
-      v = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
-      q[ct + 128 * k] = v;
+      for (int k = 0; k < kKvTile * D * 2 / 16 / 128; ++k) {
+        uint4 v = q[ct + 128 * k];
+        v = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+        q[ct + 128 * k] = v;
+      }
     }
     fence_proxy_async_smem();
     __syncwarp();
@@ -499,15 +544,17 @@ __device__ bool converter(const AttnParams& p, uint8_t* smem, const Bars& B, vol
     for (int j = 0; j < n; ++j) {
       const uint32_t T = pt + j;
       const int t0 = w.kv_begin + j * kKvTile;
-      if (!warp_wait(&B.full_k[rk.stage], rk.phase, abort_flag)) return false;
-      if (T >= 2 && !warp_wait(&B.kc_empty[T & 1], ((T >> 1) - 1) & 1, abort_flag)) return false;
-      convert_tile(smem + L::kKOff + rk.stage * L::kTileBytes, smem + L::kKcOff + (T & 1) * L::kConvTile, ct,
-                   kKvTile);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&B.kc_full[T & 1]);
-        mbar_arrive(&B.empty_k[rk.stage]);
+      if constexpr (!QF8) {
+        if (!warp_wait(&B.full_k[rk.stage], rk.phase, abort_flag)) return false;
+        if (T >= 2 && !warp_wait(&B.kc_empty[T & 1], ((T >> 1) - 1) & 1, abort_flag)) return false;
+        convert_tile(smem + L::kKOff + rk.stage * L::kTileBytes, smem + L::kKcOff + (T & 1) * L::kConvTile, ct,
+                     kKvTile);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&B.kc_full[T & 1]);
+          mbar_arrive(&B.empty_k[rk.stage]);
+        }
       }
       if (!warp_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
       if (T >= 2 && !warp_wait(&B.vc_empty[T & 1], ((T >> 1) - 1) & 1, abort_flag)) return false;
@@ -1392,7 +1439,7 @@ __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
         rv.advance<L::kStagesV>(num_tiles(w));
       }
     } else if constexpr (PF) {
-      ok = softmax_item<D, FP8, PF>(p, w, smem, B, abort_flag, tmem, rk, rv, pt, sl2, vscale, pend);
+      ok = softmax_item<D, FP8, PF>(p, w, smem, B, abort_flag, tmem, rk, rv, pt, QF8 ? sl2q : sl2, vscale, pend);
     } else {
       ok = false;  // a decode-only launch never receives prefill tiles
     }
@@ -1503,7 +1550,7 @@ __global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
   }
   if constexpr (L::kConvWarps > 0) {
     if (warp >= L::kConvWarp0 && warp < L::kConvWarp0 + L::kConvWarps) {
-      if (!converter<D, PF>(p, smem, B, abort_flag, it0, it1)) {
+      if (!converter<D, PF, QF8>(p, smem, B, abort_flag, it0, it1)) {
         if (lane == 0) record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, -2);
         *abort_flag = 1;
       }
@@ -1515,7 +1562,7 @@ __global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
       if (lane == 0) {
         const bool pv = warp == L::kPvWarp;
         if (!(pv ? pv_issuer<D, FP8, PF>(p, smem, B, abort_flag, tmem, it0, it1)
-                 : s_issuer<D, FP8, PF>(p, smem, B, abort_flag, tmem, it0, it1))) {
+                 : s_issuer<D, FP8, PF, QF8>(p, smem, B, abort_flag, tmem, it0, it1))) {
           record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, pv ? -3 : -1);
           *abort_flag = 1;
           // wait (bounded) for this thread's MMAs already issued before the memory is freed
@@ -1573,7 +1620,8 @@ cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tm_k, const
   if (num_ctas == 0) return cudaSuccess;
   const bool o = overlap_prev;
   if (fp8)
-    return has_prefill  ? launch_t<128, true, true>(p, tm_k, tm_v, tm_q, num_ctas, o, stream)
+    return has_prefill  ? (p.q_scale ? launch_t<128, true, true, true>(p, tm_k, tm_v, tm_q, num_ctas, o, stream)
+                                     : launch_t<128, true, true>(p, tm_k, tm_v, tm_q, num_ctas, o, stream))
            : p.q_scale ? launch_t<128, true, false, true>(p, tm_k, tm_v, tm_q, num_ctas, o, stream)
                        : launch_t<128, true, false>(p, tm_k, tm_v, tm_q, num_ctas, o, stream);
   if (head_dim == 128)

@@ -39,6 +39,20 @@ __device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t adesc, uint64_
       : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f8f6f4 with both operands e4m3 (type
+// code 0 in the instruction descriptor's A and B fields, the code of f16 for
+// kind::f16, so idesc_f16(0, ...) describes it): K=32 per MMA, i.e. the same
+// 32 bytes of a 128-byte K-major row as one kind::f16 MMA.
+__device__ __forceinline__ void umma_ss_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16.  A sits in tensor memory, one
 // row per lane, two 16-bit elements per 32-bit column (K-major): the K=16
 // elements of one MMA occupy 8 consecutive columns.

@@ -518,3 +518,33 @@ def test_fp8_quantised_queries_decode(P, G, split):
     H.compare_out(g.out, ref["out"], H.FP8_TOL)
     H.compare_lse(g.lse, ref["lse"])
 
+
+@pytest.mark.parametrize("P,G,causal,mixed", [(16, 4, True, False), (0, 4, False, False), (16, 8, True, True),
+                                              (32, 2, True, False)])
+def test_fp8_quantised_queries_prefill(P, G, causal, mixed):
+    """fp8 cache with q_scale on prefill tiles: Q quantised to e4m3 and Q.K^T as
+    tcgen05 kind::f8f6f4 MMAs on the raw cache tiles (P.V in f16), against the
+    oracle's quantised-query reading; ragged lengths leave partial tiles."""
+    import dataclasses
+    rng = np.random.default_rng(300 + P + G + int(mixed))
+    if mixed:
+        spec = synth.Spec(batch=4, hq=2 * G, hkv=2, d=128, page_size=P, causal=causal,
+                          softmax_scale=float(np.float32(1.0 / np.sqrt(128))), cache_dtype="fp8",
+                          q_lens=np.array([1, 300, 1, 77], np.int32), cache_lens=np.array([900, 150, 40, 0], np.int32),
+                          new_lens=np.array([1, 300, 1, 77], np.int32), capacity=1216, name="fp8-q8-mixed")
+    else:
+        spec = synth.uniform_spec("fp8-q8-prefill", 3, 200, 333, hq=2 * G, hkv=2, d=128, page_size=P,
+                                  causal=causal, cache_dtype="fp8")
+    case = synth.make_case(spec, rng)
+    amax = float(np.abs(synth.bf16_bits_to_f32(case.q)).max())
+    case = dataclasses.replace(case, q_scale=float(np.float32(amax / 448.0)))
+    g = H.GpuCase(case)
+    assert g.plan.stats()["num_prefill_items"] > 0
+    g.write_prefix()
+    g.run()
+    assert g.status() == 0, g.pkv.last_error()
+    ref = oracle.forward(case)
+    H.compare_out(g.out, ref["out"], H.FP8_TOL)
+    H.compare_lse(g.lse, ref["lse"])
+    assert np.array_equal(H.to_numpy_bits(g.k_cache), ref["k_cache"]), "k cache differs"
+
