@@ -53,16 +53,47 @@ def _peaks():
 
 
 # --------------------------------------------------------------------------- ncu traffic
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source without comments, trailing blanks and empty lines
+    (string and character literals are kept as they are)."""
+    out, i, n, quote = [], 0, len(text), None
+    while i < n:
+        c = text[i]
+        if quote:
+            out.append(c)
+            if c == "\\" and i + 1 < n:
+                out.append(text[i + 1])
+                i += 2
+                continue
+            if c == quote:
+                quote = None
+            i += 1
+        elif c in "\"'":
+            quote = c
+            out.append(c)
+            i += 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(l.rstrip() for l in "".join(out).splitlines() if l.strip())
+
+
 def kernel_source_hash() -> str:
-    """Hash of the CUDA sources: a stored ncu traffic figure is used only for the
-    kernel it was measured on."""
+    """Hash of the CUDA sources' code (comments and blank lines left out): a
+    stored ncu traffic figure is used only for the kernel it was measured on."""
     import hashlib
     csrc = os.path.join(ROOT, "paged_kv_variable_gb300", "csrc")
     h = hashlib.sha256()
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh", ".h", ".cpp")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+                h.update(f.encode() + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

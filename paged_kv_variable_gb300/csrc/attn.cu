@@ -26,7 +26,9 @@
 //               (<= 16 rows): warp-level MMAs, the four warps split the keys
 //               of each tile and merge at the end of the item.
 //   warps 7..10 (fp8 cache with prefill tiles) convert e4m3 K/V tiles and the
-//               bf16 Q tile into f16 MMA operands in shared memory.
+//               bf16 Q tile into f16 MMA operands in shared memory (with
+//               q_scale: Q into e4m3 for kind::f8f6f4 MMAs on the raw K
+//               tiles, and V alone into f16).
 //
 // fp8 caches (vLLM PR, 8-bit KV cache): decode tiles convert e4m3 to f16 in
 // registers, straight into MMA fragments (exact); k_scale is folded into the
