@@ -16,7 +16,6 @@
 #include <cstring>
 #include <functional>
 #include <new>
-#include <queue>
 #include <vector>
 
 #include "internal.h"
@@ -122,7 +121,15 @@ pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const 
     chunk = std::max<int64_t>(512, (chunk + kKvTile - 1) / kKvTile * kKvTile);
   }
 
+  int64_t num_tiles_est = 0;
+  for (int b = 0; b < B; ++b) {
+    const int lq = h_q_lens[b], lk = h_cache_lens[b] + (h_new_lens ? h_new_lens[b] : 0);
+    if (lq == 0) continue;
+    num_tiles_est += (int64_t)p.num_heads_kv *
+                     (lq * G <= kDecodeRows ? (lk <= chunk ? 1 : (lk + chunk - 1) / chunk) : (lq + tq_prefill - 1) / tq_prefill);
+  }
   std::vector<Tile> tiles;
+  tiles.reserve((size_t)num_tiles_est);
   std::vector<CombineItem> combines;
   int32_t num_slots = 0, n_dec = 0, n_pre = 0;
   int64_t q_row = 0;
@@ -189,31 +196,41 @@ pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const 
     q_row += lq;
   }
 
-  // longest processing time first onto the least-loaded CTA
+  // longest processing time first onto the least-loaded CTA (ties: the lowest
+  // CTA index), found with a tournament tree over the CTAs' (load, index)
+  // pairs; each CTA keeps its items in the order they were assigned
   const int num_items = (int)tiles.size();
   const int num_ctas = std::max(1, std::min(num_sms, num_items));
+  std::vector<double> costs(num_items);
+  for (int i = 0; i < num_items; ++i) costs[i] = tiles[i].cost;
   std::vector<int> order(num_items);
   for (int i = 0; i < num_items; ++i) order[i] = i;
-  std::stable_sort(order.begin(), order.end(), [&](int a, int c) { return tiles[a].cost > tiles[c].cost; });
+  std::stable_sort(order.begin(), order.end(), [&](int a, int c) { return costs[a] > costs[c]; });
   using Load = std::pair<double, int>;
-  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
-  for (int c = 0; c < num_ctas; ++c) heap.push({0.0, c});
-  std::vector<std::vector<int>> per_cta(num_ctas);
+  int leaves = 1;
+  while (leaves < num_ctas) leaves *= 2;
+  const Load none{HUGE_VAL, INT32_MAX};
+  std::vector<Load> tree(2 * (size_t)leaves, none);  // node i: the lesser of nodes 2i and 2i+1
+  for (int c = 0; c < num_ctas; ++c) tree[leaves + c] = {0.0, c};
+  for (int i = leaves - 1; i >= 1; --i) tree[i] = std::min(tree[2 * i], tree[2 * i + 1]);
+  std::vector<int> cta_of(num_items), cta_count(num_ctas, 0);
   for (int idx : order) {
-    Load l = heap.top();
-    heap.pop();
-    per_cta[l.second].push_back(idx);
-    l.first += tiles[idx].cost;
-    heap.push(l);
+    const int c = tree[1].second;
+    cta_of[idx] = c;
+    ++cta_count[c];
+    int i = leaves + c;
+    tree[i].first += costs[idx];
+    for (i >>= 1; i >= 1; i >>= 1) tree[i] = std::min(tree[2 * i], tree[2 * i + 1]);
   }
   double max_cost = 0, sum_cost = 0;
   int max_items = 0;
-  while (!heap.empty()) {
-    max_cost = std::max(max_cost, heap.top().first);
-    sum_cost += heap.top().first;
-    heap.pop();
+  std::vector<Load> loads(tree.begin() + leaves, tree.begin() + leaves + num_ctas);
+  std::sort(loads.begin(), loads.end());  // summed lightest first
+  for (const Load& l : loads) {
+    max_cost = std::max(max_cost, l.first);
+    sum_cost += l.first;
   }
-  for (auto& v : per_cta) max_items = std::max<int>(max_items, (int)v.size());
+  for (int c = 0; c < num_ctas; ++c) max_items = std::max(max_items, cta_count[c]);
 
   // workspace layout
   WorkspaceLayout L{};
@@ -261,12 +278,10 @@ pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const 
 
   WorkItem* items = (WorkItem*)(plan->image + L.items);
   int32_t* cta_begin = (int32_t*)(plan->image + L.cta_begin);
-  int k = 0;
-  for (int c = 0; c < num_ctas; ++c) {
-    cta_begin[c] = k;
-    for (int idx : per_cta[c]) items[k++] = tiles[idx].item;
-  }
-  cta_begin[num_ctas] = k;
+  cta_begin[0] = 0;
+  for (int c = 0; c < num_ctas; ++c) cta_begin[c + 1] = cta_begin[c] + cta_count[c];
+  std::vector<int32_t> fill(cta_begin, cta_begin + num_ctas);
+  for (int idx : order) items[fill[cta_of[idx]]++] = tiles[idx].item;
   if (!combines.empty()) memcpy(plan->image + L.combine, combines.data(), combines.size() * sizeof(CombineItem));
   int32_t* lc = (int32_t*)(plan->image + L.plan_lc);
   for (int b = 0; b < B; ++b) lc[b] = h_cache_lens[b];
