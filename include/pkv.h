@@ -205,6 +205,8 @@ typedef struct {
   int32_t kind;         /* 0 decode tile, 1 prefill tile                     */
   int32_t partial_slot; /* -1: writes the output; else split-KV partial slot */
   int32_t cta;          /* persistent CTA that runs it                       */
+  double cost;          /* the plan's cost model of the tile (model units): the
+                           longest-first assignment sorts and balances by it */
 } pkv_work_item;
 
 /* Copies up to `capacity` tiles, in CTA order, into h_items (host memory);
@@ -243,13 +245,26 @@ pkv_status pkv_attn_varlen_kvcache_fwd(const pkv_problem* problem, const pkv_fwd
  *    before any stream capture.
  *  - A plan needing more than 32 MiB of workspace is rejected with
  *    PKV_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ *  - Every host-side check (problem, plan, cache, q / out, new tokens, size)
+ *    runs before the array is touched: a rejected call copies nothing.
  *  - Every call on a device shares the one array: calls that overlap on the
  *    GPU (other streams, other host threads) race and must be serialised by
- *    the caller.  Each call rewrites what it reads, including the status word.
- *  - The device status word of these calls is not readable by pkv_get_status.
+ *    the caller.  Each call rewrites what it reads, including the status word,
+ *    which it clears; pkv_get_status_noalloc reads it.
  */
 pkv_status pkv_attn_varlen_kvcache_fwd_noalloc(const pkv_problem* problem, const pkv_fwd_args* args,
                                                pkv_plan_t plan, void* stream);
+
+/*
+ * pkv_get_status_noalloc -- pkv_get_status for the calls above: synchronises
+ * `stream`, reads the device status word that the last
+ * pkv_attn_varlen_kvcache_fwd_noalloc on the current device left in the fixed
+ * array into *device_status (a pkv_status; a bad block_table entry gives
+ * PKV_ERR_DEVICE_BOUNDS, a length past a dynamic plan's bound
+ * PKV_ERR_PLAN_MISMATCH) and resets it to PKV_OK.  Allocates nothing.  (No
+ * counterpart on the pages, like the entry point it reads for.)
+ */
+pkv_status pkv_get_status_noalloc(void* stream, int32_t* device_status);
 
 /*
  * pkv_kv_append -- in-place append alone (flash-attention PR, Usage: "kv cache

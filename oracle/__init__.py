@@ -9,7 +9,8 @@ input generators in ``synth``, which hold none of the method's arithmetic.
 Every pinned function is checked in ``tests/test_oracle_*.py`` against things
 other than itself: a pure-Python brute force, PyTorch's fp64
 ``scaled_dot_product_attention``, hand-derived golden values, closed forms and
-invariants.  No function in this package is "parity unpinned".
+invariants; ``forward_rows`` (the per-row form the full-size parity tests
+use) is checked row by row against ``forward``.
 """
 from .reference import (  # noqa: F401
     bf16_to_f64,

@@ -26,7 +26,7 @@ STATUS_NAMES = {
 # every symbol the header declares
 EXPORTED = ["pkv_plan", "pkv_plan_upload", "pkv_plan_get_stats", "pkv_plan_get_items", "pkv_attn_varlen_kvcache_fwd", "pkv_kv_append",
             "pkv_get_status", "pkv_plan_destroy", "pkv_last_error", "pkv_version", "pkv_set_profile_events",
-            "pkv_attn_varlen_kvcache_fwd_noalloc", "pkv_plan_decode_dynamic"]
+            "pkv_attn_varlen_kvcache_fwd_noalloc", "pkv_plan_decode_dynamic", "pkv_get_status_noalloc"]
 
 
 class PkvError(RuntimeError):
@@ -57,7 +57,8 @@ class FwdArgs(ctypes.Structure):
 
 class WorkItemInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("seq", "kv_head", "q_row0", "q_index0", "n_q", "q_len", "kv_len",
-                                               "kv_begin", "kv_end", "kind", "partial_slot", "cta")]
+                                               "kv_begin", "kv_end", "kind", "partial_slot", "cta")] + [
+        ("cost", ctypes.c_double)]
 
 
 class PlanStats(ctypes.Structure):
@@ -90,13 +91,14 @@ def lib() -> ctypes.CDLL:
         L.pkv_get_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
         L.pkv_set_profile_events.argtypes = [vp, vp]
         L.pkv_attn_varlen_kvcache_fwd_noalloc.argtypes = [ctypes.POINTER(Problem), ctypes.POINTER(FwdArgs), vp, vp]
+        L.pkv_get_status_noalloc.argtypes = [vp, ctypes.POINTER(i32)]
         L.pkv_plan_destroy.argtypes = [vp]
         L.pkv_plan_destroy.restype = None
         L.pkv_last_error.restype = ctypes.c_char_p
         L.pkv_version.restype = ctypes.c_char_p
         for name in ("pkv_plan", "pkv_plan_upload", "pkv_plan_get_stats", "pkv_plan_get_items", "pkv_attn_varlen_kvcache_fwd",
                      "pkv_kv_append", "pkv_get_status", "pkv_set_profile_events",
-                     "pkv_attn_varlen_kvcache_fwd_noalloc"):
+                     "pkv_attn_varlen_kvcache_fwd_noalloc", "pkv_get_status_noalloc"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -236,6 +238,13 @@ def attn_varlen_kvcache_fwd_noalloc(problem: Problem, args: FwdArgs, plan_: Plan
     allocate device memory); uses the library's fixed 32 MiB device scratch."""
     _check(lib().pkv_attn_varlen_kvcache_fwd_noalloc(ctypes.byref(problem), ctypes.byref(args), plan_.handle,
                                                      _stream_handle(stream)))
+
+
+def get_status_noalloc(stream=None) -> int:
+    """Device status word left by the last no-workspace call on this device (then reset)."""
+    st = ctypes.c_int32()
+    _check(lib().pkv_get_status_noalloc(_stream_handle(stream), ctypes.byref(st)))
+    return int(st.value)
 
 
 def kv_append(problem: Problem, args: FwdArgs, total_new: int, device_status=None, stream=None) -> None:

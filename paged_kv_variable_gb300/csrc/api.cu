@@ -209,17 +209,16 @@ extern "C" pkv_status pkv_kv_append(const pkv_problem* problem, const pkv_fwd_ar
   return PKV_OK;
 }
 
-extern "C" pkv_status pkv_attn_varlen_kvcache_fwd(const pkv_problem* problem, const pkv_fwd_args* args,
-                                                  pkv_plan_t plan, void* workspace, size_t workspace_bytes,
-                                                  void* stream) {
+namespace pkv {
+
+// Every host-side check of an attention call that does not involve the
+// workspace: the problem, the plan it must match, the cache, q / out and the
+// new-token arguments.  Nothing is launched or copied before these pass.
+pkv_status validate_call(const pkv_problem* problem, const pkv_fwd_args* args, pkv_plan_t plan) {
   pkv_status st = validate_problem(problem);
   if (st != PKV_OK) return st;
   if (!plan) return fail(PKV_ERR_INVALID_ARG, "plan is NULL");
   if (!same_problem(*problem, plan->problem)) return fail(PKV_ERR_INVALID_ARG, "problem differs from the plan's");
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
-    return fail(PKV_ERR_INVALID_ARG, "workspace must be non-NULL and 256-byte aligned");
-  if (workspace_bytes < plan->layout.total)
-    return fail(PKV_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu required", workspace_bytes, plan->layout.total);
   st = validate_cache_args(*problem, args);
   if (st != PKV_OK) return st;
   const pkv_problem& pr = *problem;
@@ -238,15 +237,32 @@ extern "C" pkv_status pkv_attn_varlen_kvcache_fwd(const pkv_problem* problem, co
     return fail(PKV_ERR_INVALID_ARG, "the plan appends %d tokens but k_new / v_new are NULL", plan->total_new);
   if (plan->total_new == 0 && has_new)
     return fail(PKV_ERR_INVALID_ARG, "k_new given but the plan was made with no new tokens");
+  if (plan->total_new > 0) {
+    st = validate_new_args(pr, args);
+    if (st != PKV_OK) return st;
+  }
   if (args->q_scale && pr.cache_dtype != PKV_FP8_E4M3)
     return fail(PKV_ERR_UNSUPPORTED, "q_scale (fp8 Q.K^T) needs an fp8 cache");
+  return PKV_OK;
+}
+
+}  // namespace pkv
+
+extern "C" pkv_status pkv_attn_varlen_kvcache_fwd(const pkv_problem* problem, const pkv_fwd_args* args,
+                                                  pkv_plan_t plan, void* workspace, size_t workspace_bytes,
+                                                  void* stream) {
+  pkv_status st = validate_call(problem, args, plan);
+  if (st != PKV_OK) return st;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+    return fail(PKV_ERR_INVALID_ARG, "workspace must be non-NULL and 256-byte aligned");
+  if (workspace_bytes < plan->layout.total)
+    return fail(PKV_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu required", workspace_bytes, plan->layout.total);
+  const pkv_problem& pr = *problem;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   int* status = reinterpret_cast<int*>(ws + plan->layout.status);
 
   if (plan->total_new > 0) {
-    st = validate_new_args(pr, args);
-    if (st != PKV_OK) return st;
     AppendParams ap = append_params(pr, args, plan->total_new, status);
     cudaError_t e = launch_kv_append(ap, pr.head_dim, pr.cache_dtype == PKV_FP8_E4M3, s);
     if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");

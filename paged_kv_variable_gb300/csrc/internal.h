@@ -89,9 +89,12 @@ struct pkv_plan_s {
   int32_t num_items;
   int32_t num_combine;
   int32_t dynamic;  // cache lengths read on the device; plan_lc holds their bounds
+  double* item_cost;  // [num_items] model cost of each item, in work-list order
 };
 
 namespace pkv {
 // thread-local error message helpers (api.cu)
 pkv_status fail(pkv_status st, const char* fmt, ...);
+// host checks of an attention call other than its workspace (api.cu)
+pkv_status validate_call(const pkv_problem* problem, const pkv_fwd_args* args, pkv_plan_t plan);
 }  // namespace pkv

@@ -50,16 +50,27 @@ using namespace pkv;
 
 extern "C" pkv_status pkv_attn_varlen_kvcache_fwd_noalloc(const pkv_problem* problem, const pkv_fwd_args* args,
                                                           pkv_plan_t plan, void* stream) {
-  if (!plan) return fail(PKV_ERR_INVALID_ARG, "plan is NULL");
+  // every host check first: a rejected call leaves the shared scratch alone
+  pkv_status st = validate_call(problem, args, plan);
+  if (st != PKV_OK) return st;
   if (plan->layout.total > kStaticScratchBytes)
     return fail(PKV_ERR_WORKSPACE_TOO_SMALL,
                 "this plan needs %zu bytes of scratch but the fixed scratch holds %zu bytes; use "
                 "pkv_attn_varlen_kvcache_fwd with a caller workspace",
                 plan->layout.total, kStaticScratchBytes);
   void* scratch = nullptr;
-  pkv_status st = scratch_address(&scratch);
+  st = scratch_address(&scratch);
   if (st != PKV_OK) return st;
   st = pkv_plan_upload(plan, scratch, kStaticScratchBytes, stream);
   if (st != PKV_OK) return st;
   return pkv_attn_varlen_kvcache_fwd(problem, args, plan, scratch, kStaticScratchBytes, stream);
+}
+
+extern "C" pkv_status pkv_get_status_noalloc(void* stream, int32_t* device_status) {
+  if (!device_status) return fail(PKV_ERR_INVALID_ARG, "NULL output");
+  void* scratch = nullptr;
+  pkv_status st = scratch_address(&scratch);
+  if (st != PKV_OK) return st;
+  // the status word sits at the head of every plan's workspace layout
+  return pkv_get_status(scratch, stream, device_status);
 }

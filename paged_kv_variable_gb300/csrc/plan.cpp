@@ -255,7 +255,10 @@ pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const 
   pkv_plan_s* plan = new (std::nothrow) pkv_plan_s();
   if (!plan) return fail(PKV_ERR_INVALID_ARG, "out of host memory");
   plan->image = (unsigned char*)calloc(1, image_bytes);
-  if (!plan->image) {
+  plan->item_cost = (double*)calloc((size_t)std::max(1, num_items), sizeof(double));
+  if (!plan->image || !plan->item_cost) {
+    free(plan->image);
+    free(plan->item_cost);
     delete plan;
     return fail(PKV_ERR_INVALID_ARG, "out of host memory");
   }
@@ -281,7 +284,11 @@ pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const 
   cta_begin[0] = 0;
   for (int c = 0; c < num_ctas; ++c) cta_begin[c + 1] = cta_begin[c] + cta_count[c];
   std::vector<int32_t> fill(cta_begin, cta_begin + num_ctas);
-  for (int idx : order) items[fill[cta_of[idx]]++] = tiles[idx].item;
+  for (int idx : order) {
+    const int k = fill[cta_of[idx]]++;
+    items[k] = tiles[idx].item;
+    plan->item_cost[k] = costs[idx];
+  }
   if (!combines.empty()) memcpy(plan->image + L.combine, combines.data(), combines.size() * sizeof(CombineItem));
   int32_t* lc = (int32_t*)(plan->image + L.plan_lc);
   for (int b = 0; b < B; ++b) lc[b] = h_cache_lens[b];
@@ -346,6 +353,7 @@ extern "C" pkv_status pkv_plan_get_items(pkv_plan_t plan, pkv_work_item* h_items
       o.kind = w.kind;
       o.partial_slot = w.partial;
       o.cta = c;
+      o.cost = plan->item_cost[k];
     }
   }
   return PKV_OK;
@@ -354,5 +362,6 @@ extern "C" pkv_status pkv_plan_get_items(pkv_plan_t plan, pkv_work_item* h_items
 extern "C" void pkv_plan_destroy(pkv_plan_t plan) {
   if (!plan) return;
   free(plan->image);
+  free(plan->item_cost);
   delete plan;
 }

@@ -228,3 +228,82 @@ def test_fwd_validation_before_any_launch(pkv):
     with pytest.raises(pkv.PkvError) as e:
         pkv.kv_append(fp8, pkv.make_args(**good), 4, None, stream=0)   # no scales
     assert e.value.status == 1
+
+
+# ------------------------------------------------------------------ longest-processing-time assignment
+def _lpt_heap(items, num_ctas):
+    """Reference assignment with heapq: tiles in the plan's generation order
+    (sequence, kv head, query tile, key chunk), stably sorted longest first,
+    each given to the least-loaded CTA (ties: the lowest index); a CTA runs
+    its tiles in the order it received them."""
+    import heapq
+    key = lambda it: (it["seq"], it["kv_head"], it["q_index0"], it["kv_begin"])
+    gen = sorted(items, key=key)
+    order = sorted(range(len(gen)), key=lambda k: -gen[k]["cost"])   # sorted() is stable
+    heap = [(0.0, c) for c in range(num_ctas)]
+    heapq.heapify(heap)
+    lists = [[] for _ in range(num_ctas)]
+    for k in order:
+        load, c = heapq.heappop(heap)
+        lists[c].append(key(gen[k]))
+        heapq.heappush(heap, (load + gen[k]["cost"], c))
+    return lists
+
+
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("sms", [1, 13, 152])
+def test_plan_assignment_is_lpt(pkv, seed, sms):
+    """The work list equals a heapq LPT over the plan's own tile costs, CTA by
+    CTA and item by item (random mixed batches: decode units, split chunks,
+    prefill tiles, zero lengths)."""
+    rng = np.random.default_rng(seed)
+    B = int(rng.integers(3, 40))
+    lq = np.where(rng.random(B) < 0.7, 1, rng.integers(0, 700, B)).astype(np.int32)
+    lc = rng.integers(0, 6000, B).astype(np.int32)
+    cap = int((lc + lq).max() + 16) // 16 * 16 + 16
+    prob = pkv.make_problem(batch=B, num_heads_q=8 * int(rng.choice([1, 2, 4])), num_heads_kv=8, head_dim=128,
+                            page_size=16, cache_capacity=cap, num_pages=100000, cache_dtype="bf16", causal=True,
+                            softmax_scale=0.088)
+    pl = pkv.plan(prob, lq, lc, lq, num_sms=sms)
+    items = pl.items()
+    n_ctas = pl.stats()["num_ctas"]
+    assert n_ctas == min(sms, len(items))
+    got = [[] for _ in range(n_ctas)]
+    for it in items:
+        got[it["cta"]].append((it["seq"], it["kv_head"], it["q_index0"], it["kv_begin"]))
+    assert got == _lpt_heap(items, n_ctas)
+
+
+# ------------------------------------------------------------------ no-workspace entry point (host checks)
+def test_noalloc_rejects_before_touching_its_scratch(pkv):
+    """Host checks of the workspace-free call run before its fixed device
+    array is resolved or written: a bad argument, or a plan needing more than
+    the array's 32 MiB, is refused with no CUDA call at all (this test runs
+    without a GPU)."""
+    B, hkv, lk = 64, 8, 8191
+    prob = pkv.make_problem(batch=B, num_heads_q=32, num_heads_kv=hkv, head_dim=128, page_size=16,
+                            cache_capacity=8192, num_pages=B * 512, cache_dtype="bf16", causal=True,
+                            softmax_scale=0.088)
+    ones = np.ones(B, np.int32)
+    big = pkv.plan(prob, ones, np.full(B, lk, np.int32), ones, num_sms=4096)   # 512-key chunks: many partials
+    assert big.workspace_bytes > 32 << 20
+    q = _FakeTensor(1 << 20, (B, 32, 128))
+    kc = _FakeTensor(1 << 24, (B * 512, 16, hkv, 128))
+    i32 = _FakeTensor(1 << 16, (B + 1,), esize=4)
+    bt = _FakeTensor(1 << 17, (B, 512), esize=4)
+    kn = _FakeTensor(1 << 18, (B, hkv, 128))
+    good = dict(q=q, out=q, cu_seqlens_q=i32, max_seqlen_q=1, k_cache=kc, v_cache=kc, cache_seqlens=i32,
+                k_new=kn, v_new=kn, cu_seqlens_knew=i32, block_table=bt)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.attn_varlen_kvcache_fwd_noalloc(prob, pkv.make_args(**good), big, stream=0)
+    assert e.value.status == 3 and "fixed scratch" in pkv.last_error()
+    small = pkv.plan(prob, ones, np.full(B, 100, np.int32), ones, num_sms=152)
+    assert small.workspace_bytes <= 32 << 20
+    bad = dict(good, block_table=None)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.attn_varlen_kvcache_fwd_noalloc(prob, pkv.make_args(**bad), small, stream=0)
+    assert e.value.status == 1 and "block_table" in pkv.last_error()
+    with pytest.raises(pkv.PkvError) as e:       # new tokens missing: caught before any copy
+        pkv.attn_varlen_kvcache_fwd_noalloc(prob, pkv.make_args(**dict(good, k_new=None, v_new=None)), small,
+                                            stream=0)
+    assert e.value.status == 1

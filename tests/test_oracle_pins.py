@@ -296,3 +296,99 @@ def test_algorithmic_work_closed_forms():
     spec = synth.config2(draw_values=False).spec
     w = oracle.algorithmic_work(spec)
     assert w["kv_bytes"] == int(spec.kv_lens.sum()) * 8 * 128 * 2 * 2
+
+
+# ---------------------------------------------------------------------------
+# forward_rows: the per-row oracle the full-size parity tests sample from
+# ---------------------------------------------------------------------------
+def _rows_equal_forward(case):
+    """forward_rows over EVERY query row equals forward() row by row: its own
+    causal horizon, per-sequence gather and empty-row handling against the
+    whole-sequence masked softmax."""
+    spec = case.spec
+    ref = oracle.forward(case)
+    rows = [(b, i) for b in range(spec.batch) for i in range(int(spec.q_lens[b]))]
+    if not rows:
+        return
+    # visit the rows in a shuffled order: the gather cache of forward_rows
+    # must not depend on the rows of one sequence arriving together
+    order = np.random.default_rng(len(rows)).permutation(len(rows))
+    rows = [rows[k] for k in order]
+    o, lse = oracle.forward_rows(case, ref["k_cache"], ref["v_cache"], rows)
+    idx = [int(spec.cu_q[b]) + i for b, i in rows]
+    np.testing.assert_allclose(o, ref["out"][idx], rtol=0, atol=1e-13)
+    want = ref["lse"][:, idx]
+    fin = np.isfinite(want)
+    assert np.array_equal(np.isfinite(lse), fin)
+    assert np.all(np.isneginf(lse[~fin]))
+    np.testing.assert_allclose(lse[fin], want[fin], rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_forward_rows_equals_forward_random(seed):
+    # causal and non-causal, Lq != Ln (and Lq > Lk: rows with an empty causal
+    # horizon), zero lengths, paged / contiguous, bf16 / fp8, GQA group sizes
+    case = synth.random_case(4000 + seed, causal=(seed % 2 == 0), cache_dtype="fp8" if seed % 5 == 4 else "bf16",
+                             with_new=(seed % 7 != 6), q_equals_new=(seed % 3 != 0), max_cache=50, max_new=12)
+    _rows_equal_forward(case)
+
+
+def test_forward_rows_equals_forward_config1():
+    _rows_equal_forward(synth.config1())
+    _rows_equal_forward(synth.config1(sentinel="nan"))
+
+
+def test_forward_rows_empty_horizons():
+    """Rows that see no key: Lk = 0, and causal Lq > Lk (the first Lq - Lk rows)."""
+    spec = synth.Spec(batch=3, hq=4, hkv=2, d=16, page_size=4, causal=True, softmax_scale=0.25,
+                      cache_dtype="bf16", q_lens=np.array([3, 5, 2], np.int32),
+                      cache_lens=np.array([0, 1, 6], np.int32), new_lens=np.array([0, 1, 2], np.int32),
+                      capacity=8, name="empty-horizons")
+    case = synth.make_case(spec, np.random.default_rng(9))
+    ref = oracle.forward(case)
+    assert np.all(ref["out"][:3] == 0) and np.all(np.isneginf(ref["lse"][:, :3]))   # Lk = 0
+    assert np.all(ref["out"][3:6] == 0) and np.all(np.isfinite(ref["lse"][:, 6:8]))  # Lq 5 on Lk 2
+    _rows_equal_forward(case)
+
+
+def test_forward_rows_equals_forward_mixed_subset():
+    """Sequences of the mixed in-flight batch: a 2048-token prefill request on
+    its cached prefix and three long decode requests."""
+    full = synth.config4()
+    pre = [b for b in range(full.spec.batch) if full.spec.q_lens[b] > 1][0]
+    dec = [b for b in range(full.spec.batch) if full.spec.q_lens[b] == 1][:3]
+    _rows_equal_forward(synth.subset_case(full, [dec[0], pre, dec[1], dec[2]]))
+
+
+# ---------------------------------------------------------------------------
+# byte and flop counts behind the roofline numbers, counted by hand
+# ---------------------------------------------------------------------------
+def test_algorithmic_work_hand_count_config1():
+    """The tiny paged workload counted by hand: B=2, Hq=4, Hkv=2, D=64, page
+    16, cache lengths {37, 5}, new tokens = queries {3, 1}, so Lk = {40, 6}."""
+    import bench
+    spec = synth.config1().spec
+    kv_read = (40 + 6) * 2 * 64 * 2 * 2       # keys x kv heads x D x (K, V) x 2 bytes
+    q_read_o_write = (3 + 1) * 4 * 64 * 2 * 2  # query rows x q heads x D x 2 bytes x (read q, write out)
+    new_kv = (3 + 1) * 2 * 64 * 2 * (2 + 2)   # new tokens x kv heads x D x (K, V) x (read bf16 + write bf16)
+    table = (3 + 1) * 4                        # pages used: ceil(40/16) + ceil(6/16), 4 bytes each
+    assert (kv_read, q_read_o_write, new_kv, table) == (23552, 4096, 4096, 16)
+    # causal pairs: sequence 0 rows see 38, 39, 40 keys; sequence 1's row sees 6
+    pairs = 38 + 39 + 40 + 6
+    w = oracle.algorithmic_work(spec)
+    assert w["kv_bytes"] == kv_read
+    assert w["bytes"] == kv_read + q_read_o_write + new_kv + table == 31760
+    assert w["pairs"] == pairs == 123
+    assert w["flops"] == 4 * 64 * 4 * pairs
+    sw = bench.step_work(spec)
+    assert sw["attn_bytes"] == kv_read + q_read_o_write + table == 27664
+    assert sw["append_bytes"] == new_kv
+    assert sw["bytes"] == w["bytes"] and sw["flops"] == w["flops"]
+    # fp8 cache: K/V are read and written one byte each, new K/V still read as bf16
+    fspec = synth.Spec(**{**spec.__dict__, "cache_dtype": "fp8"})
+    fw = oracle.algorithmic_work(fspec)
+    assert fw["bytes"] == (40 + 6) * 2 * 64 * 2 * 1 + q_read_o_write + (3 + 1) * 2 * 64 * 2 * (2 + 1) + table
+    assert bench.step_work(fspec)["bytes"] == fw["bytes"]
+    # non-causal: every query row sees every key of its sequence
+    nspec = synth.Spec(**{**spec.__dict__, "causal": False})
+    assert oracle.algorithmic_work(nspec)["pairs"] == 3 * 40 + 1 * 6 == bench.step_work(nspec)["flops"] // (4 * 64 * 4)

@@ -48,4 +48,23 @@ def test_noalloc_matches_workspace_entry_point(idx):
         g.out.fill_(float("nan"))
         g.pkv.attn_varlen_kvcache_fwd_noalloc(g.problem, g.args(), g.plan)
         torch.cuda.synchronize()
+        assert g.pkv.get_status_noalloc() == 0, g.pkv.last_error()
         H.compare_out(g.out, H.bf16_to_f64(want), H.BF16_TOL, what="noalloc out")
+
+
+def test_noalloc_device_status_is_readable():
+    """A device-side error of a workspace-free call (a block_table entry past
+    the page pool, which the kernels skip instead of reading) shows in the
+    status word of the fixed scratch; the next good call clears it."""
+    case = synth.config1()
+    g = H.GpuCase(case)
+    bad = g.block_table.clone()
+    bad[0, 1] = 10_000
+    good_table = g.block_table
+    g.block_table = bad
+    g.pkv.attn_varlen_kvcache_fwd_noalloc(g.problem, g.args(), g.plan)
+    assert g.pkv.get_status_noalloc() == 6      # PKV_ERR_DEVICE_BOUNDS
+    assert g.pkv.get_status_noalloc() == 0      # reading resets it
+    g.block_table = good_table
+    g.pkv.attn_varlen_kvcache_fwd_noalloc(g.problem, g.args(), g.plan)
+    assert g.pkv.get_status_noalloc() == 0
