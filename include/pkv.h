@@ -147,9 +147,12 @@ typedef struct {
  * pkv_plan -- host scheduling step (flashinfer PR "Uniform PoDAttention API",
  * Key Changes 2: partition by KV-cache load; Limitations: classifier on the
  * query length).  Validates the shape, classifies every (sequence, kv head)
- * as decode work (Lq*G <= 16 rows) or prefill work (128-row query tiles),
- * cuts long decode units into KV chunks (split-KV, flash-attention PR,
- * Limitation), and assigns all tiles to num_sms persistent CTAs longest first.
+ * as decode work (Lq*G <= 16 rows: warp-MMA tiles) or tensor-core work
+ * (tiles of 128 rows = 128/G query tokens x the G heads of the group; a group
+ * of more than 128 heads is cut into sub-groups of 128, so any G >= 1 is
+ * served), cuts long units whose queries fit one tile (decode steps, short
+ * query runs) into KV chunks (split-KV, flash-attention PR, Limitation), and
+ * assigns all tiles to num_sms persistent CTAs longest first.
  * h_q_lens / h_cache_lens / h_new_lens: host int32 [B]; h_new_lens may be NULL
  * when the call appends nothing.  Zero lengths are accepted.  On success
  * *out_plan owns a host work list and *out_workspace_bytes is the device
@@ -171,8 +174,9 @@ pkv_status pkv_plan(const pkv_problem* problem, const int32_t* h_q_lens,
  * every call made with the plan; q lengths and new-token lengths are fixed by
  * it.  Work is split and scheduled for the bounds; at run time each work
  * item's key range is cut at the sequence's current key count (split-KV
- * chunks past it contribute nothing).  Every request must be a decode unit
- * (q_len * Hq/Hkv <= 16), else PKV_ERR_UNSUPPORTED.  A call whose
+ * chunks past it contribute nothing).  Every request's queries must fit one
+ * tile (q_len * Hq/Hkv <= 16, or q_len <= 128 / min(Hq/Hkv, 128)), else
+ * PKV_ERR_UNSUPPORTED.  A call whose
  * cache_seqlens[b] exceeds its bound records PKV_ERR_PLAN_MISMATCH in the
  * device status and attends at most the bound.  Pure host code.
  */
@@ -191,7 +195,8 @@ pkv_status pkv_plan_upload(pkv_plan_t plan, void* workspace, size_t workspace_by
 pkv_status pkv_plan_get_stats(pkv_plan_t plan, pkv_plan_stats* stats);
 
 /* One scheduled tile as the plan made it (diagnostics and tests).  Rows of a
- * tile are (query token, head of the group) pairs, row = token * G + g. */
+ * tile are (query token, head of the tile's heads) pairs, row = token *
+ * num_heads + g, query head = kv_head * G + head0 + g. */
 typedef struct {
   int32_t seq;          /* sequence b                                        */
   int32_t kv_head;      /* kv head                                           */
@@ -203,8 +208,11 @@ typedef struct {
   int32_t kv_begin;     /* keys [kv_begin, kv_end) handled by this tile      */
   int32_t kv_end;
   int32_t kind;         /* 0 decode tile, 1 prefill tile                     */
-  int32_t partial_slot; /* -1: writes the output; else split-KV partial slot */
+  int32_t partial_slot; /* -1: writes the output; else its first split-KV
+                           partial slot (16 rows per slot)                   */
   int32_t cta;          /* persistent CTA that runs it                       */
+  int32_t head0;        /* first query head of the group in the tile         */
+  int32_t num_heads;    /* query heads of the group in the tile              */
   double cost;          /* the plan's cost model of the tile (model units): the
                            longest-first assignment sorts and balances by it */
 } pkv_work_item;

@@ -57,7 +57,8 @@ class FwdArgs(ctypes.Structure):
 
 class WorkItemInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("seq", "kv_head", "q_row0", "q_index0", "n_q", "q_len", "kv_len",
-                                               "kv_begin", "kv_end", "kind", "partial_slot", "cta")] + [
+                                               "kv_begin", "kv_end", "kind", "partial_slot", "cta",
+                                               "head0", "num_heads")] + [
         ("cost", ctypes.c_double)]
 
 

@@ -86,15 +86,15 @@ pkv_status make_cache_map(CUtensorMap* map, const pkv_problem& pr, const pkv_fwd
   return PKV_OK;
 }
 
-// 3-D map over q (D, Hq, total_q): a box of G heads x 128/G tokens is the
-// 128-row Q tile of one kv head's prefill item (row = token * G + g).
+// 3-D map over q (D, Hq, total_q): a box of nh heads x 128/nh tokens (nh = G,
+// at most 128) is the Q tile of one tensor-core item (row = token * nh + g).
 pkv_status make_q_map(CUtensorMap* map, const pkv_problem& pr, const pkv_fwd_args& a, int total_q) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  const int g = pr.num_heads_q / pr.num_heads_kv;
+  const int nh = tc_group_heads(pr.num_heads_q / pr.num_heads_kv);
   cuuint64_t dims[3] = {(cuuint64_t)pr.head_dim, (cuuint64_t)pr.num_heads_q, (cuuint64_t)(total_q > 0 ? total_q : 1)};
   cuuint64_t strides[2] = {(cuuint64_t)a.q_stride_head * 2, (cuuint64_t)a.q_stride_tok * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)g, (cuuint32_t)(kPrefillRowsTc / g)};
+  cuuint32_t box[3] = {64, (cuuint32_t)nh, (cuuint32_t)(kPrefillRowsTc / nh)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -17,6 +17,8 @@
 
 namespace pkv {
 
+constexpr int kCombineThreads = 256;
+
 // One warp per (new token, kv head) row; lane l moves elements [l*E, l*E+E).
 template <int D, bool FP8>
 __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
@@ -85,43 +87,48 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
   }
 }
 
-// One block per split unit; thread t owns row t / (D/8) and 8 consecutive
-// columns.  Partials are normalised outputs with log2-domain LSEs; the merge
-// order over chunks is fixed (deterministic).
+// One block per split unit; a thread owns 8 consecutive columns of a row and
+// walks the unit's rows (up to 128: a tensor-core tile of a wide head group).
+// Partials are normalised outputs with log2-domain LSEs; chunk s of the unit
+// wrote slot0 + s * slot_stride; the merge order over chunks is fixed
+// (deterministic).
 template <int D>
-__global__ void __launch_bounds__(kDecodeRows * D / 8) combine_kernel(const CombineParams p) {
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p) {
   const CombineItem ci = p.items[blockIdx.x];
-  const int row = threadIdx.x / (D / 8);
-  const int d0 = (threadIdx.x % (D / 8)) * 8;
-  if (row >= ci.n_q * p.G) return;
+  constexpr int kPerRow = D / 8;
+  const int d0 = (threadIdx.x % kPerRow) * 8;
+  const int rows = ci.n_q * ci.nh;
   grid_dep_wait();  // the partials come from the attention kernel launched just before
   constexpr float kLn2 = 0.693147180559945309f;
-  const float* lse = p.partial_lse + (int64_t)ci.slot0 * kDecodeRows + row;
-  float m = -INFINITY;
-  for (int s = 0; s < ci.nsplit; ++s) m = fmaxf(m, __ldg(lse + s * kDecodeRows));
-  const float m_use = m == -INFINITY ? 0.f : m;
-  float wsum = 0.f;
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  const float* po = p.partial_o + ((int64_t)ci.slot0 * kDecodeRows + row) * D + d0;
-  for (int s = 0; s < ci.nsplit; ++s) {
-    const float w = ex2(__ldg(lse + s * kDecodeRows) - m_use);
-    const float4 a = __ldg(reinterpret_cast<const float4*>(po + (int64_t)s * kDecodeRows * D));
-    const float4 b = __ldg(reinterpret_cast<const float4*>(po + (int64_t)s * kDecodeRows * D + 4));
-    wsum += w;
-    acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
-    acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
+  const int64_t chunk_rows = (int64_t)ci.slot_stride * kDecodeRows;
+  for (int row = threadIdx.x / kPerRow; row < rows; row += kCombineThreads / kPerRow) {
+    const float* lse = p.partial_lse + (int64_t)ci.slot0 * kDecodeRows + row;
+    float m = -INFINITY;
+    for (int s = 0; s < ci.nsplit; ++s) m = fmaxf(m, __ldg(lse + s * chunk_rows));
+    const float m_use = m == -INFINITY ? 0.f : m;
+    float wsum = 0.f;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const float* po = p.partial_o + ((int64_t)ci.slot0 * kDecodeRows + row) * D + d0;
+    for (int s = 0; s < ci.nsplit; ++s) {
+      const float w = ex2(__ldg(lse + s * chunk_rows) - m_use);
+      const float4 a = __ldg(reinterpret_cast<const float4*>(po + s * chunk_rows * D));
+      const float4 b = __ldg(reinterpret_cast<const float4*>(po + s * chunk_rows * D + 4));
+      wsum += w;
+      acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
+      acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const int tok = ci.q_row0 + row / ci.nh;
+    const int head = ci.hk * p.G + ci.h0 + row % ci.nh;
+    uint4 v;
+    v.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+    v.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+    v.z = pack_bf16(acc[4] * inv, acc[5] * inv);
+    v.w = pack_bf16(acc[6] * inv, acc[7] * inv);
+    *reinterpret_cast<uint4*>(p.out + (int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head + d0) = v;
+    if (p.lse != nullptr && d0 == 0)
+      p.lse[(int64_t)head * p.total_q + tok] = wsum > 0.f ? (m_use + __log2f(wsum)) * kLn2 : -INFINITY;
   }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  const int tok = ci.q_row0 + row / p.G;
-  const int head = ci.hk * p.G + row % p.G;
-  uint4 v;
-  v.x = pack_bf16(acc[0] * inv, acc[1] * inv);
-  v.y = pack_bf16(acc[2] * inv, acc[3] * inv);
-  v.z = pack_bf16(acc[4] * inv, acc[5] * inv);
-  v.w = pack_bf16(acc[6] * inv, acc[7] * inv);
-  *reinterpret_cast<uint4*>(p.out + (int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head + d0) = v;
-  if (p.lse != nullptr && d0 == 0)
-    p.lse[(int64_t)head * p.total_q + tok] = wsum > 0.f ? (m_use + __log2f(wsum)) * kLn2 : -INFINITY;
 }
 
 cudaError_t launch_kv_append(const AppendParams& p, int head_dim, bool fp8, cudaStream_t stream) {
@@ -148,7 +155,7 @@ cudaError_t launch_combine(const CombineParams& p, int num_items, int head_dim, 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)num_items);
-  cfg.blockDim = dim3((unsigned)(kDecodeRows * head_dim / 8));
+  cfg.blockDim = dim3((unsigned)kCombineThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cfg.attrs = attr;

@@ -257,12 +257,14 @@ __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CU
       }
       if (lane == 0) {
         if (pi == 0) tma_prefetch_desc(tm_q);
-        const int tq = kPrefillRowsTc / p.G;
-        mbar_arrive_expect_tx(B.q_full, (uint32_t)((D / 64) * p.G * tq * 128));
+        // the box: nh_tc heads x (128 / nh_tc) tokens, every byte credited (zero fill included)
+        const int nh_tc = tc_group_heads(p.G);
+        mbar_arrive_expect_tx(B.q_full, (uint32_t)((D / 64) * nh_tc * (kPrefillRowsTc / nh_tc) * 128));
       }
       __syncwarp();
       if (lane < D / 64)
-        tma_load_3d(smem + L::kQOff + lane * (kKvTile * 128), tm_q, B.q_full, lane * 64, w.hk * p.G, w.q_row0);
+        tma_load_3d(smem + L::kQOff + lane * (kKvTile * 128), tm_q, B.q_full, lane * 64, w.hk * p.G + w.h0,
+                    w.q_row0);
       ++pi;
     }
     int q = 0;  // tile of the current page group
@@ -588,8 +590,9 @@ struct PendingEpi {
   bool has = false;                // warp-uniform
   uint32_t T = 0;                  // the item's last tile: O is final once its P V has completed
   float inv = 0.f;                 // scale of the output (v_scale / l, or 0)
-  float lse = 0.f;                 // natural-log LSE of the row
+  float lse = 0.f;                 // natural-log LSE of the row (log2 for a split-KV partial)
   __nv_bfloat16* dst = nullptr;    // this thread's output row (null: none)
+  float* pdst = nullptr;           // or its fp32 split-KV partial row
   float* lse_dst = nullptr;
 };
 
@@ -604,7 +607,7 @@ __device__ __forceinline__ bool epi_run(const AttnParams& p, const Bars& B, cons
     uint32_t o[32];
     tmem_ld32(t_lane + kTmemO + c * 32, o);
     tmem_wait_ld();
-    if (e.dst != nullptr) {
+    if (e.dst != nullptr || e.pdst != nullptr) {
       uint4 v[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -615,7 +618,19 @@ __device__ __forceinline__ bool epi_run(const AttnParams& p, const Bars& B, cons
       }
       // a row is written in 32-byte pieces where it is aligned for them (whole
       // sectors, half the store instructions), else in 16-byte ones
-      if (p.out_v8) {
+      if (e.pdst != nullptr) {
+        // split-KV partial: the normalised fp32 row (512-byte rows of the workspace)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float f[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) f[k] = __uint_as_float(o[8 * q + k]) * e.inv;
+          st_global_v8(e.pdst + c * 32 + q * 8, make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
+                                                           __float_as_uint(f[2]), __float_as_uint(f[3])),
+                       make_uint4(__float_as_uint(f[4]), __float_as_uint(f[5]), __float_as_uint(f[6]),
+                                  __float_as_uint(f[7])));
+        }
+      } else if (p.out_v8) {
         st_global_v8(e.dst + c * 32, v[0], v[1]);
         st_global_v8(e.dst + c * 32 + 16, v[2], v[3]);
       } else {
@@ -648,14 +663,15 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
   const int qw = warp & 3;                   // TMEM lane quarter this warp may access
   const int r = qw * 32 + lane;              // tile row == TMEM lane
   const uint32_t t_lane = tmem + ((uint32_t)(qw * 32) << 16);
-  const int R = w.n_q * p.G;
+  // rows: token r / nh of the tile, head h0 + r % nh of the group
+  const int R = w.n_q * w.nh;
   const bool valid = r < R;
-  const int tok = w.q_row0 + r / p.G;
-  const int head = w.hk * p.G + r % p.G;
+  const int tok = w.q_row0 + r / w.nh;
+  const int head = w.hk * p.G + w.h0 + r % w.nh;
   int lim = 0;
   if (valid) {
     lim = w.kv_end;
-    if (p.causal) lim = min(lim, w.q_i0 + r / p.G + w.lk - w.lq + 1);
+    if (p.causal) lim = min(lim, w.q_i0 + r / w.nh + w.lk - w.lq + 1);
   }
   const int n = num_tiles(w);
   float m = -INFINITY, l = 0.f;
@@ -784,17 +800,23 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
     rv.advance<L::kStagesV>();
   }
 
-  // epilogue: O / l -> bf16 rows and the natural-log LSE, deferred to the next
-  // prefill item's first tile (or the end of the CTA's work)
+  // epilogue: O / l -> bf16 rows and the natural-log LSE (or, for a split-KV
+  // chunk, fp32 partial rows and log2 LSEs), deferred to the next prefill
+  // item's first tile (or the end of the CTA's work)
+  const bool part = w.partial >= 0;
   __nv_bfloat16* dst = p.out + (int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head;
-  float* lse_dst = (valid && p.lse != nullptr) ? p.lse + (int64_t)head * p.total_q + tok : nullptr;
-  const float lse = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+  float* pdst = p.partial_o + ((int64_t)w.partial * kDecodeRows + r) * D;
+  float* lse_dst = !valid ? nullptr
+                   : part ? p.partial_lse + (int64_t)w.partial * kDecodeRows + r
+                          : (p.lse != nullptr ? p.lse + (int64_t)head * p.total_q + tok : nullptr);
+  const float lse = l > 0.f ? (part ? m + __log2f(l) : (m + __log2f(l)) * kLn2) : -INFINITY;
   if (n > 0) {
     pend.has = true;
     pend.T = pt + n - 1;
     pend.inv = l > 0.f ? vscale / l : 0.f;
     pend.lse = lse;
-    pend.dst = valid ? dst : nullptr;
+    pend.dst = (valid && !part) ? dst : nullptr;
+    pend.pdst = (valid && part) ? pdst : nullptr;
     pend.lse_dst = lse_dst;
     if constexpr (FP8) {
       if (!epi_run<D>(p, B, pend, t_lane, abort_flag)) return false;
@@ -802,7 +824,10 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
       pend.has = false;
     }
   } else {
-    if (valid) {
+    if (valid && part) {
+#pragma unroll
+      for (int c = 0; c < D / 4; ++c) *reinterpret_cast<float4*>(pdst + c * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else if (valid) {
 #pragma unroll
       for (int c = 0; c < D / 8; ++c) *reinterpret_cast<uint4*>(dst + c * 8) = make_uint4(0, 0, 0, 0);
     }

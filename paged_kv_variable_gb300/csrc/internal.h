@@ -29,8 +29,18 @@ inline int cache_box_rows(int page_size, int capacity) {
 
 enum ItemKind : int32_t { kDecode = 0, kPrefill = 1 };
 
+// Heads of one query-head group that a tensor-core tile holds: the whole
+// group up to 128 heads; larger groups are cut into sub-groups of 128.
+#ifdef __CUDACC__
+#define PKV_HOST_DEVICE __host__ __device__
+#else
+#define PKV_HOST_DEVICE
+#endif
+PKV_HOST_DEVICE inline int tc_group_heads(int G) { return G < kPrefillRowsTc ? G : kPrefillRowsTc; }
+
 // One tile of work for one persistent CTA.  Rows of the tile are
-// (query token, head in group) pairs: row r = token * G + g.
+// (query token, head of the tile's head sub-group) pairs: row r = token * nh + g,
+// query head = hk * G + h0 + g.
 struct WorkItem {
   int32_t b;         // sequence
   int32_t hk;        // kv head
@@ -42,19 +52,24 @@ struct WorkItem {
   int32_t kv_begin;  // key range of this item, kv_begin a multiple of kKvTile
   int32_t kv_end;
   int32_t kind;      // ItemKind
-  int32_t partial;   // -1: write the final output; else partial slot
-  int32_t cost;      // model cost (diagnostics)
+  int32_t partial;   // -1: write the final output; else the first partial slot (16 rows each)
+  int32_t h0;        // first query head of the group in this tile
+  int32_t nh;        // heads of the group in this tile (rows = n_q * nh)
+  int32_t pad[3];
 };
-static_assert(sizeof(WorkItem) == 48, "WorkItem layout");
+static_assert(sizeof(WorkItem) == 64, "WorkItem layout");
 
-// A split decode unit merged by the combine kernel: slots slot0 .. slot0+nsplit-1.
+// A unit split into KV chunks, merged by the combine kernel: chunk s wrote
+// rows [0, n_q * nh) starting at partial slot slot0 + s * slot_stride.
 struct CombineItem {
   int32_t q_row0;
   int32_t n_q;
   int32_t hk;
   int32_t nsplit;
   int32_t slot0;
-  int32_t pad[3];
+  int32_t slot_stride;  // 16-row slots per chunk: ceil(n_q * nh / 16)
+  int32_t h0;
+  int32_t nh;
 };
 static_assert(sizeof(CombineItem) == 32, "CombineItem layout");
 

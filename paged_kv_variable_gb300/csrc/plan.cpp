@@ -46,9 +46,7 @@ pkv_status validate_problem(const pkv_problem* p) {
   if (p->num_heads_q % p->num_heads_kv != 0)
     return fail(PKV_ERR_INVALID_ARG, "num_heads_q (%d) %% num_heads_kv (%d) != 0", p->num_heads_q,
                 p->num_heads_kv);
-  int g = p->num_heads_q / p->num_heads_kv;
-  if (g > kDecodeRows)
-    return fail(PKV_ERR_UNSUPPORTED, "group size Hq/Hkv = %d > %d", g, kDecodeRows);
+  // any group size: groups of more than 128 heads are cut into head sub-groups
   if (p->cache_dtype != PKV_BF16 && p->cache_dtype != PKV_FP8_E4M3)
     return fail(PKV_ERR_INVALID_ARG, "cache_dtype %d unknown", p->cache_dtype);
   if (p->head_dim != 64 && p->head_dim != 128)
@@ -94,9 +92,19 @@ pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const 
   const int D = p.head_dim;
   const int esize = p.cache_dtype == PKV_BF16 ? 2 : 1;
   const int prefill_rows = kPrefillRowsTc;
-  const int tq_prefill = prefill_rows / G;  // query tokens per prefill tile
+  // tensor-core tiles: nh_tc heads of a group x tq query tokens (128 rows at
+  // most); a group of more than 128 heads takes n_sub head sub-groups
+  const int nh_tc = tc_group_heads(G);
+  const int n_sub = (G + nh_tc - 1) / nh_tc;
+  const int tq_prefill = prefill_rows / nh_tc;  // query tokens per tensor-core tile
+  // A unit (sequence, kv head[, head sub-group]) is a decode unit (warp-MMA
+  // tile) if its rows fit 16, else tensor-core tiles; units whose queries fit
+  // one tile (decode steps of wide groups, short query runs) can be split
+  // along the keys like decode units.
+  auto is_decode = [&](int lq) { return (int64_t)lq * G <= kDecodeRows; };
+  auto splittable = [&](int lq) { return is_decode(lq) || lq <= tq_prefill; };
 
-  int64_t total_q = 0, total_new = 0, total_decode_keys = 0;
+  int64_t total_q = 0, total_new = 0, total_split_keys = 0;
   for (int b = 0; b < B; ++b) {
     int lq = h_q_lens[b], lc = h_cache_lens[b], ln = h_new_lens ? h_new_lens[b] : 0;
     if (lq < 0 || lc < 0 || ln < 0) return fail(PKV_ERR_INVALID_ARG, "negative length at sequence %d", b);
@@ -105,96 +113,118 @@ pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const 
                   p.cache_capacity);
     total_q += lq;
     total_new += ln;
-    if (dynamic && lq > 0 && (int64_t)lq * G > kDecodeRows)
-      return fail(PKV_ERR_UNSUPPORTED, "dynamic plans take decode requests only (sequence %d: %d query rows > %d)", b,
-                  lq * G, kDecodeRows);
-    if (lq > 0 && (int64_t)lq * G <= kDecodeRows) total_decode_keys += (int64_t)(lc + ln) * p.num_heads_kv;
+    if (dynamic && lq > 0 && !splittable(lq))
+      return fail(PKV_ERR_UNSUPPORTED,
+                  "dynamic plans take requests whose queries fit one tile (sequence %d: %d query tokens > %d)", b, lq,
+                  std::max(tq_prefill, kDecodeRows / G));
+    if (lq > 0 && splittable(lq))
+      total_split_keys += (int64_t)(lc + ln) * p.num_heads_kv * (is_decode(lq) ? 1 : n_sub);
   }
   if (total_q > INT32_MAX / 2 || total_new > INT32_MAX / 2)
     return fail(PKV_ERR_UNSUPPORTED, "total tokens too large");
 
-  // split-KV chunk for decode units: at least 4 decode items per CTA, chunks >= 512 keys
+  // split-KV chunk: at least 4 splittable items per CTA, chunks >= 512 keys
   int64_t chunk = 1 << 30;
-  if (total_decode_keys > 0) {
+  if (total_split_keys > 0) {
     int64_t target = 4LL * num_sms;
-    chunk = (total_decode_keys + target - 1) / target;
+    chunk = (total_split_keys + target - 1) / target;
     chunk = std::max<int64_t>(512, (chunk + kKvTile - 1) / kKvTile * kKvTile);
   }
+  auto nchunks_of = [&](int lk) { return lk <= chunk ? 1 : (int)((lk + chunk - 1) / chunk); };
 
   int64_t num_tiles_est = 0;
   for (int b = 0; b < B; ++b) {
     const int lq = h_q_lens[b], lk = h_cache_lens[b] + (h_new_lens ? h_new_lens[b] : 0);
     if (lq == 0) continue;
-    num_tiles_est += (int64_t)p.num_heads_kv *
-                     (lq * G <= kDecodeRows ? (lk <= chunk ? 1 : (lk + chunk - 1) / chunk) : (lq + tq_prefill - 1) / tq_prefill);
+    num_tiles_est += (int64_t)p.num_heads_kv * (is_decode(lq) ? nchunks_of(lk)
+                                                : (int64_t)n_sub * (splittable(lq) ? nchunks_of(lk)
+                                                                                   : (lq + tq_prefill - 1) / tq_prefill));
   }
   std::vector<Tile> tiles;
   tiles.reserve((size_t)num_tiles_est);
   std::vector<CombineItem> combines;
-  int32_t num_slots = 0, n_dec = 0, n_pre = 0;
+  int64_t num_slots = 0;
+  int32_t n_dec = 0, n_pre = 0;
   int64_t q_row = 0;
   for (int b = 0; b < B; ++b) {
     int lq = h_q_lens[b], lc = h_cache_lens[b], ln = h_new_lens ? h_new_lens[b] : 0;
     int lk = lc + ln;
     if (lq == 0) continue;
     for (int hk = 0; hk < p.num_heads_kv; ++hk) {
-      if (lq * G <= kDecodeRows) {
-        int nchunks = lk <= chunk ? 1 : (int)((lk + chunk - 1) / chunk);
-        int slot0 = nchunks > 1 ? num_slots : -1;
-        for (int c = 0; c < nchunks; ++c) {
-          Tile t{};
-          t.item.b = b;
-          t.item.hk = hk;
-          t.item.q_row0 = (int32_t)q_row;
-          t.item.q_i0 = 0;
-          t.item.n_q = lq;
-          t.item.lq = lq;
-          t.item.lk = lk;
-          t.item.kv_begin = (int32_t)std::min<int64_t>((int64_t)c * chunk, lk);
-          t.item.kv_end = (int32_t)std::min<int64_t>((int64_t)(c + 1) * chunk, lk);
-          t.item.kind = kDecode;
-          t.item.partial = nchunks > 1 ? num_slots + c : -1;
-          t.cost = decode_cost(t.item.kv_end - t.item.kv_begin, D, esize);
-          t.item.cost = (int32_t)std::min(t.cost, 2.0e9);
-          tiles.push_back(t);
-          ++n_dec;
-        }
-        if (nchunks > 1) {
-          CombineItem ci{};
-          ci.q_row0 = (int32_t)q_row;
-          ci.n_q = lq;
-          ci.hk = hk;
-          ci.nsplit = nchunks;
-          ci.slot0 = slot0;
-          combines.push_back(ci);
-          num_slots += nchunks;
-        }
-      } else {
-        for (int i0 = 0; i0 < lq; i0 += tq_prefill) {
-          int n = std::min(tq_prefill, lq - i0);
-          int kv_end = lk;
-          if (p.causal) kv_end = std::max(0, std::min(lk, i0 + n + lk - lq));
-          Tile t{};
-          t.item.b = b;
-          t.item.hk = hk;
-          t.item.q_row0 = (int32_t)(q_row + i0);
-          t.item.q_i0 = i0;
-          t.item.n_q = n;
-          t.item.lq = lq;
-          t.item.lk = lk;
-          t.item.kv_begin = 0;
-          t.item.kv_end = kv_end;
-          t.item.kind = kPrefill;
-          t.item.partial = -1;
-          t.cost = prefill_cost(kv_end, prefill_rows, D);
-          t.item.cost = (int32_t)std::min(t.cost, 2.0e9);
-          tiles.push_back(t);
-          ++n_pre;
+      const bool dec = is_decode(lq);
+      for (int sg = 0; sg < (dec ? 1 : n_sub); ++sg) {
+        const int h0 = dec ? 0 : sg * nh_tc;
+        const int nh = dec ? G : std::min(nh_tc, G - h0);
+        if (splittable(lq)) {
+          // one query tile (all lq tokens), possibly cut into KV chunks
+          const int nchunks = nchunks_of(lk);
+          const int rows = lq * nh;
+          const int stride = (rows + kDecodeRows - 1) / kDecodeRows;  // 16-row partial slots per chunk
+          const int64_t slot0 = nchunks > 1 ? num_slots : -1;
+          for (int c = 0; c < nchunks; ++c) {
+            Tile t{};
+            t.item.b = b;
+            t.item.hk = hk;
+            t.item.q_row0 = (int32_t)q_row;
+            t.item.q_i0 = 0;
+            t.item.n_q = lq;
+            t.item.lq = lq;
+            t.item.lk = lk;
+            t.item.kv_begin = (int32_t)std::min<int64_t>((int64_t)c * chunk, lk);
+            t.item.kv_end = (int32_t)std::min<int64_t>((int64_t)(c + 1) * chunk, lk);
+            t.item.kind = dec ? kDecode : kPrefill;
+            t.item.partial = nchunks > 1 ? (int32_t)(num_slots + (int64_t)c * stride) : -1;
+            t.item.h0 = h0;
+            t.item.nh = nh;
+            const int keys = t.item.kv_end - t.item.kv_begin;
+            t.cost = dec ? decode_cost(keys, D, esize)
+                         : std::max(decode_cost(keys, D, esize), prefill_cost(keys, prefill_rows, D));
+            tiles.push_back(t);
+            if (dec) ++n_dec; else ++n_pre;
+          }
+          if (nchunks > 1) {
+            CombineItem ci{};
+            ci.q_row0 = (int32_t)q_row;
+            ci.n_q = lq;
+            ci.hk = hk;
+            ci.nsplit = nchunks;
+            ci.slot0 = (int32_t)slot0;
+            ci.slot_stride = stride;
+            ci.h0 = h0;
+            ci.nh = nh;
+            combines.push_back(ci);
+            num_slots += (int64_t)nchunks * stride;
+          }
+        } else {
+          for (int i0 = 0; i0 < lq; i0 += tq_prefill) {
+            int n = std::min(tq_prefill, lq - i0);
+            int kv_end = lk;
+            if (p.causal) kv_end = std::max(0, std::min(lk, i0 + n + lk - lq));
+            Tile t{};
+            t.item.b = b;
+            t.item.hk = hk;
+            t.item.q_row0 = (int32_t)(q_row + i0);
+            t.item.q_i0 = i0;
+            t.item.n_q = n;
+            t.item.lq = lq;
+            t.item.lk = lk;
+            t.item.kv_begin = 0;
+            t.item.kv_end = kv_end;
+            t.item.kind = kPrefill;
+            t.item.partial = -1;
+            t.item.h0 = h0;
+            t.item.nh = nh;
+            t.cost = prefill_cost(kv_end, prefill_rows, D);
+            tiles.push_back(t);
+            ++n_pre;
+          }
         }
       }
     }
     q_row += lq;
   }
+  if (num_slots > INT32_MAX / (kDecodeRows * 256))
+    return fail(PKV_ERR_UNSUPPORTED, "too many split-KV partial slots");
 
   // longest processing time first onto the least-loaded CTA (ties: the lowest
   // CTA index), found with a tournament tree over the CTAs' (load, index)
@@ -264,7 +294,7 @@ pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const 
   }
   plan->problem = p;
   plan->num_ctas = num_items > 0 ? num_ctas : 0;
-  plan->num_slots = num_slots;
+  plan->num_slots = (int32_t)num_slots;
   plan->total_q = (int32_t)total_q;
   plan->total_new = (int32_t)total_new;
   plan->max_items_per_cta = max_items;
@@ -353,6 +383,8 @@ extern "C" pkv_status pkv_plan_get_items(pkv_plan_t plan, pkv_work_item* h_items
       o.kind = w.kind;
       o.partial_slot = w.partial;
       o.cta = c;
+      o.head0 = w.h0;
+      o.num_heads = w.nh;
       o.cost = plan->item_cost[k];
     }
   }

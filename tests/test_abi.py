@@ -52,7 +52,6 @@ def _problem(pkv, **kw):
     (dict(page_size=12), 2),
     (dict(page_size=512), 2),
     (dict(cache_dtype="fp8", head_dim=64), 2),
-    (dict(num_heads_q=64, num_heads_kv=2), 2),
     (dict(cache_capacity=0), 1),
     (dict(cache_capacity=40), 1),   # not a multiple of the page size
     (dict(softmax_scale=0.0), 1),
@@ -74,25 +73,29 @@ def test_plan_rejects_overflowing_lengths(pkv):
 
 
 def _coverage(spec, items, num_sms):
-    """Every (seq, kv head, query token) is covered by exactly the tiles whose
-    key ranges tile [0, limit) of that row without overlap."""
+    """Every (seq, query head, query token) is covered by exactly the tiles
+    whose key ranges tile [0, limit) of that row without overlap."""
     G = spec.hq // spec.hkv
     cov = {}
     for it in items:
         b, hk = it["seq"], it["kv_head"]
         assert 0 <= it["cta"] < num_sms
         assert it["kv_begin"] % 128 == 0 or it["kv_begin"] == it["kv_end"]
+        assert 0 <= it["head0"] and it["head0"] + it["num_heads"] <= G
         for t in range(it["n_q"]):
             i = it["q_index0"] + t
-            cov.setdefault((b, hk, i), []).append((it["kv_begin"], it["kv_end"], it["partial_slot"]))
-        rows = it["n_q"] * G
+            for h in range(it["head0"], it["head0"] + it["num_heads"]):
+                cov.setdefault((b, hk * G + h, i), []).append((it["kv_begin"], it["kv_end"], it["partial_slot"]))
+        rows = it["n_q"] * it["num_heads"]
         if it["kind"] == 0:
-            assert rows <= 16
+            assert rows <= 16 and it["num_heads"] == G
+        else:
+            assert rows <= 128 and it["num_heads"] == min(128, G - it["head0"])
     for b in range(spec.batch):
         lq, lk = int(spec.q_lens[b]), int(spec.kv_lens[b])
-        for hk in range(spec.hkv):
+        for hq in range(spec.hq):
             for i in range(lq):
-                ranges = sorted(cov.pop((b, hk, i)))
+                ranges = sorted(cov.pop((b, hq, i)))
                 # ranges are disjoint, start at 0 and reach at least the row's horizon
                 horizon = min(lk, i + lk - lq + 1) if spec.causal else lk
                 pos = 0
@@ -107,9 +110,15 @@ def _coverage(spec, items, num_sms):
     assert not cov
 
 
-@pytest.mark.parametrize("which", ["cfg1", "cfg2", "cfg3", "cfg4", "rand"])
+@pytest.mark.parametrize("which", ["cfg1", "cfg2", "cfg3", "cfg4", "rand", "mqa32", "g48", "g71", "g256", "g6"])
 def test_plan_covers_every_row(pkv, which):
-    if which == "cfg1":
+    wide = {"mqa32": (32, 1), "g48": (96, 2), "g71": (71, 1), "g256": (256, 1), "g6": (12, 2)}
+    if which in wide:
+        hq, hkv = wide[which]
+        rng = np.random.default_rng(hq)
+        case = synth.random_case(hq, batch=6, hq=hq, hkv=hkv, d=128, page_size=16, max_cache=3000, max_new=300,
+                                 causal=True)
+    elif which == "cfg1":
         case = synth.config1()
     elif which == "cfg2":
         case = synth.config2(draw_values=False)
@@ -117,7 +126,7 @@ def test_plan_covers_every_row(pkv, which):
         case = synth.config3(draw_values=False)
     elif which == "cfg4":
         case = synth.config4(draw_values=False)
-    else:
+    elif which == "rand":
         case = synth.random_case(7, batch=5, hq=8, hkv=2, d=128, page_size=16, max_cache=900, max_new=70)
     spec = case.spec
     prob = pkv.make_problem(batch=spec.batch, num_heads_q=spec.hq, num_heads_kv=spec.hkv, head_dim=spec.d,
@@ -147,7 +156,8 @@ def test_plan_accepts_zero_lengths(pkv):
 
 
 def test_dynamic_plan_decode_only(pkv):
-    """A dynamic plan schedules decode units for the bounds and refuses prefill requests."""
+    """A dynamic plan schedules decode units for the bounds and refuses
+    requests whose queries need more than one tile."""
     spec = synth.config2(draw_values=False).spec
     prob = pkv.make_problem(batch=spec.batch, num_heads_q=spec.hq, num_heads_kv=spec.hkv, head_dim=spec.d,
                             page_size=spec.page_size, cache_capacity=spec.capacity, num_pages=100000,
@@ -157,9 +167,12 @@ def test_dynamic_plan_decode_only(pkv):
     fixed = pkv.plan(prob, spec.q_lens, bounds, spec.new_lens, num_sms=152)
     # the same work list as a plan for the bounds themselves
     assert dyn.items() == fixed.items() and dyn.workspace_bytes == fixed.workspace_bytes
+    # queries of one request beyond one tensor-core tile (128 rows / G = 64 tokens at G = 2)
     with pytest.raises(pkv.PkvError) as e:
-        pkv.plan_decode_dynamic(_problem(pkv, batch=2), [1, 9], [3, 3], [1, 9], num_sms=4)
-    assert e.value.status == 2 and "decode" in pkv.last_error()
+        pkv.plan_decode_dynamic(_problem(pkv, batch=2, cache_capacity=256), [1, 65], [3, 3], [1, 65], num_sms=4)
+    assert e.value.status == 2 and "dynamic" in pkv.last_error()
+    # a short query run that fits one tile is accepted
+    pkv.plan_decode_dynamic(_problem(pkv, batch=2, cache_capacity=256), [1, 9], [3, 3], [1, 9], num_sms=4)
 
 
 def test_empty_batch(pkv):
@@ -307,3 +320,28 @@ def test_noalloc_rejects_before_touching_its_scratch(pkv):
         pkv.attn_varlen_kvcache_fwd_noalloc(prob, pkv.make_args(**dict(good, k_new=None, v_new=None)), small,
                                             stream=0)
     assert e.value.status == 1
+
+
+@pytest.mark.parametrize("hq,hkv", [(32, 1), (64, 2), (200, 1), (256, 2)])
+def test_wide_groups_plan(pkv, hq, hkv):
+    """Groups of more than 16 heads: decode steps become tensor-core tiles of
+    the whole group (split along the keys when long); groups of more than 128
+    heads are cut into sub-groups of 128; a dynamic plan accepts them."""
+    G = hq // hkv
+    B = 5
+    prob = pkv.make_problem(batch=B, num_heads_q=hq, num_heads_kv=hkv, head_dim=128, page_size=16,
+                            cache_capacity=16384, num_pages=100000, cache_dtype="bf16", causal=True,
+                            softmax_scale=0.088)
+    ones = np.ones(B, np.int32)
+    lc = np.array([9000, 100, 0, 16000, 3000], np.int32)
+    pl = pkv.plan(prob, ones, lc, ones, num_sms=152)
+    items = pl.items()
+    assert all(it["kind"] == 1 for it in items)
+    subs = {(it["head0"], it["num_heads"]) for it in items}
+    want = {(h0, min(128, G - h0)) for h0 in range(0, G, 128)}
+    assert subs == want
+    assert pl.stats()["num_split_units"] > 0
+    dyn = pkv.plan_decode_dynamic(prob, ones, lc, ones, num_sms=152)
+    assert dyn.items() == items
+    with pytest.raises(pkv.PkvError):   # more query tokens than one tile holds: not a dynamic-plan request
+        pkv.plan_decode_dynamic(prob, np.full(B, 200, np.int32), lc, np.full(B, 200, np.int32), num_sms=152)

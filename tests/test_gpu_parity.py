@@ -109,6 +109,49 @@ def test_group_sizes_decode_and_prefill(g_):
         run_full(synth.make_case(spec, rng))
 
 
+@pytest.mark.parametrize("hq,hkv,lq,lc,P,dtype,sms", [
+    (32, 1, 1, 3000, 16, "bf16", 16),     # MQA decode, split along the keys
+    (32, 1, 200, 500, 16, "bf16", 152),   # MQA prefill: 4 tokens per tile
+    (64, 2, 1, 1500, 0, "bf16", 8),       # G = 32 decode, contiguous cache, split
+    (96, 2, 3, 700, 16, "bf16", 152),     # G = 48: a short query run in one tile
+    (71, 1, 5, 900, 32, "bf16", 4),       # G = 71 (prime): one token per tile, split
+    (256, 1, 2, 600, 16, "bf16", 152),    # G = 256: two head sub-groups of 128
+    (200, 1, 1, 2500, 16, "bf16", 8),     # G = 200: sub-groups of 128 and 72, split
+    (12, 2, 9, 300, 16, "bf16", 152),     # G = 6: 54 rows in one tile
+    (24, 8, 1, 800, 16, "bf16", 152),     # G = 3: a decode tile of 3 rows
+    (32, 1, 1, 2000, 16, "fp8", 16),      # MQA decode on an fp8 cache, split
+    (64, 2, 130, 200, 16, "fp8", 152),    # G = 32 prefill on an fp8 cache
+    (64, 1, 1, 1000, 64, "bf16", 152),    # G = 64 decode, D = 64 below
+])
+def test_wide_and_odd_groups(hq, hkv, lq, lc, P, dtype, sms):
+    """Any group size (MQA and GQA beyond 16 heads per kv head): rows of more
+    than 16 go to tensor-core tiles that hold the whole group (up to 128 heads,
+    larger groups cut into sub-groups), split along the keys when a unit's
+    queries fit one tile; small odd groups stay on decode tiles."""
+    d = 64 if (hq, hkv, lc, P) == (64, 1, 1000, 64) else 128
+    rng = np.random.default_rng(hq * 1000 + lq + lc)
+    spec = synth.uniform_spec(f"g{hq // hkv}", 3, lq, lc, hq=hq, hkv=hkv, d=d, page_size=P, cache_dtype=dtype)
+    case = synth.make_case(spec, rng)
+    g, _ = run_full(case, num_sms=sms)
+    if sms <= 16 and lq == 1:
+        assert g.plan.stats()["num_split_units"] > 0
+
+
+def test_wide_group_mixed_batch_and_quantised_queries():
+    """An MQA batch mixing decode steps, short query runs and long prefills in
+    one launch; then the same on an fp8 cache with quantised queries."""
+    import dataclasses
+    spec = synth.Spec(batch=5, hq=32, hkv=1, d=128, page_size=16, causal=True,
+                      softmax_scale=float(np.float32(1.0 / np.sqrt(128))), cache_dtype="bf16",
+                      q_lens=np.array([1, 300, 1, 4, 37], np.int32), cache_lens=np.array([2500, 100, 0, 900, 0], np.int32),
+                      new_lens=np.array([1, 300, 1, 4, 37], np.int32), capacity=2512, name="mqa-mixed")
+    run_full(synth.make_case(spec, np.random.default_rng(55)), num_sms=24)
+    fspec = dataclasses.replace(spec, cache_dtype="fp8")
+    case = synth.make_case(fspec, np.random.default_rng(56))
+    amax = float(np.abs(synth.bf16_bits_to_f32(case.q)).max())
+    run_full(dataclasses.replace(case, q_scale=float(np.float32(amax / 448.0))), num_sms=24)
+
+
 def test_long_decode_is_split_and_matches():
     rng = np.random.default_rng(11)
     spec = synth.uniform_spec("long", 2, 1, 9000, hq=8, hkv=2, d=128, page_size=64)
@@ -430,17 +473,19 @@ def test_cuda_graph_capture_and_replay(kind):
     H.compare_out(g.out, ref["out"], H.BF16_TOL)
 
 
-@pytest.mark.parametrize("cache_dtype,ragged", [("bf16", False), ("bf16", True), ("fp8", False)])
-def test_dynamic_plan_graph_decode_steps(cache_dtype, ragged):
+@pytest.mark.parametrize("cache_dtype,ragged,hq,hkv", [("bf16", False, 8, 2), ("bf16", True, 8, 2),
+                                                        ("fp8", False, 8, 2), ("bf16", False, 32, 1)])
+def test_dynamic_plan_graph_decode_steps(cache_dtype, ragged, hq, hkv):
     """One dynamic plan and one captured graph serve several decode steps while
     cache_seqlens grows on the device; every step matches the oracle (bf16 and
-    fp8 caches, padded block table or ragged page list)."""
+    fp8 caches, padded block table or ragged page list, GQA and MQA with 32
+    heads per kv head on tensor-core tiles)."""
     import dataclasses
     import math
     import torch
     steps = 5
     rng = np.random.default_rng(91)
-    B, hq, hkv, d, P = 6, 8, 2, 128, 16
+    B, d, P = 6, 128, 16
     base = rng.integers(100, 1500, B).astype(np.int32)
     base[0] = 0                         # a sequence that starts empty
     total = base + steps                # the tokens the steps will append are drawn up front
