@@ -75,7 +75,7 @@ typedef struct {
   int32_t batch;          /* number of sequences B                                   */
   int32_t num_heads_q;    /* Hq                                                      */
   int32_t num_heads_kv;   /* Hkv; Hq % Hkv == 0 (MQA: Hkv = 1)                       */
-  int32_t head_dim;       /* D: 64 or 128 (fp8 cache: 128)                           */
+  int32_t head_dim;       /* D: 64 or 128, either cache dtype                        */
   int32_t page_size;      /* 0 = contiguous cache; else 1, 2, 4 or a multiple of 8,
                              <= 256 (pages under 8 tokens are gathered row by row) */
   int32_t cache_capacity; /* tokens one sequence can hold: contiguous seqlen_cache,

@@ -65,8 +65,9 @@ pkv_status cuda_fail(cudaError_t e, const char* what) {
 }
 
 // 4-D map over a cache (D, Hkv, rows-per-page-or-seq, pages-or-batch); a box
-// is cache_box_rows() rows of one 128-byte column chunk, 128-byte swizzle, zero
-// fill outside the tensor.
+// is cache_box_rows() rows of one 128-byte column chunk with the 128-byte
+// swizzle (an fp8 cache at D = 64: its 64-byte rows with the 64-byte swizzle),
+// zero fill outside the tensor.
 pkv_status make_cache_map(CUtensorMap* map, const pkv_problem& pr, const pkv_fwd_args& a, void* base) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
@@ -77,10 +78,12 @@ pkv_status make_cache_map(CUtensorMap* map, const pkv_problem& pr, const pkv_fwd
   cuuint64_t strides[3] = {(cuuint64_t)a.kc_stride_head * es, (cuuint64_t)a.kc_stride_tok * es,
                            (cuuint64_t)a.kc_stride_page * es};
   cuuint32_t box[4] = {(cuuint32_t)(128 / es), 1, (cuuint32_t)cache_box_rows(pr.page_size, pr.cache_capacity), 1};
-  if (pr.head_dim * es < 128) box[0] = (cuuint32_t)pr.head_dim;
+  const bool narrow = pr.head_dim * es < 128;
+  if (narrow) box[0] = (cuuint32_t)pr.head_dim;
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  narrow ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return PKV_OK;

@@ -70,20 +70,26 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
       *reinterpret_cast<uint32_t*>(vc) = __ldg(reinterpret_cast<const uint32_t*>(vin));
     }
   } else {
-    static_assert(E == 4, "fp8 cache rows are 128 elements");
     // one IEEE reciprocal per call, then an RN multiply per element (no FMA)
     const float inv_k = __frcp_rn(__ldg(p.k_scale));
     const float inv_v = __frcp_rn(__ldg(p.v_scale));
-    const uint2 kr = __ldg(reinterpret_cast<const uint2*>(kin));
-    const uint2 vr = __ldg(reinterpret_cast<const uint2*>(vin));
     auto lo_f = [](uint32_t w) { return __uint_as_float(w << 16); };
     auto hi_f = [](uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); };
-    const uint32_t k01 = f32x2_to_e4m3x2(__fmul_rn(lo_f(kr.x), inv_k), __fmul_rn(hi_f(kr.x), inv_k));
-    const uint32_t k23 = f32x2_to_e4m3x2(__fmul_rn(lo_f(kr.y), inv_k), __fmul_rn(hi_f(kr.y), inv_k));
-    const uint32_t v01 = f32x2_to_e4m3x2(__fmul_rn(lo_f(vr.x), inv_v), __fmul_rn(hi_f(vr.x), inv_v));
-    const uint32_t v23 = f32x2_to_e4m3x2(__fmul_rn(lo_f(vr.y), inv_v), __fmul_rn(hi_f(vr.y), inv_v));
-    *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(p.k_cache) + dst) = k01 | (k23 << 16);
-    *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(p.v_cache) + dst) = v01 | (v23 << 16);
+    auto enc2 = [&](uint32_t w, float inv) -> uint32_t {
+      return f32x2_to_e4m3x2(__fmul_rn(lo_f(w), inv), __fmul_rn(hi_f(w), inv));
+    };
+    uint8_t* kc = reinterpret_cast<uint8_t*>(p.k_cache) + dst;
+    uint8_t* vc = reinterpret_cast<uint8_t*>(p.v_cache) + dst;
+    if constexpr (E == 4) {
+      const uint2 kr = __ldg(reinterpret_cast<const uint2*>(kin));
+      const uint2 vr = __ldg(reinterpret_cast<const uint2*>(vin));
+      *reinterpret_cast<uint32_t*>(kc) = enc2(kr.x, inv_k) | (enc2(kr.y, inv_k) << 16);
+      *reinterpret_cast<uint32_t*>(vc) = enc2(vr.x, inv_v) | (enc2(vr.y, inv_v) << 16);
+    } else {
+      // D = 64: two elements a lane, one 2-byte store each
+      *reinterpret_cast<uint16_t*>(kc) = (uint16_t)enc2(__ldg(reinterpret_cast<const uint32_t*>(kin)), inv_k);
+      *reinterpret_cast<uint16_t*>(vc) = (uint16_t)enc2(__ldg(reinterpret_cast<const uint32_t*>(vin)), inv_v);
+    }
   }
 }
 
@@ -137,8 +143,10 @@ cudaError_t launch_kv_append(const AppendParams& p, int head_dim, bool fp8, cuda
   const int threads = 256;
   const int64_t blocks = (rows * 32 + threads - 1) / threads;
   if (blocks > INT32_MAX) return cudaErrorInvalidValue;
-  if (fp8) {
+  if (fp8 && head_dim == 128) {
     kv_append_kernel<128, true><<<(unsigned)blocks, threads, 0, stream>>>(p);
+  } else if (fp8) {
+    kv_append_kernel<64, true><<<(unsigned)blocks, threads, 0, stream>>>(p);
   } else if (head_dim == 128) {
     kv_append_kernel<128, false><<<(unsigned)blocks, threads, 0, stream>>>(p);
   } else {

@@ -74,7 +74,11 @@ struct Layout {
   static constexpr int kStagesK = PF ? (FP8 ? 2 : (D == 128 ? 3 : 4)) : (FP8 || D == 64 ? 6 : 4);
   static constexpr int kStagesV = PF ? (FP8 ? 2 : (D == 128 ? 3 : 4)) : (FP8 || D == 64 ? 6 : 3);
   static constexpr int kTileBytes = kKvTile * D * kEsize;   // one raw K (or V) tile
-  static constexpr int kChunks = D * kEsize / 128;            // 128-byte column chunks per cache row
+  // A raw tile is [column chunks][128 rows][kRowBytes]: 128-byte chunks with
+  // the 128-byte swizzle, or (an fp8 cache at D = 64) one chunk of 64-byte
+  // rows with the 64-byte swizzle.
+  static constexpr int kRowBytes = D * kEsize < 128 ? D * kEsize : 128;
+  static constexpr int kChunks = D * kEsize / kRowBytes;      // column chunks per cache row
   static constexpr int kKOff = 0;                             // K ring
   static constexpr int kVOff = kStagesK * kTileBytes;         // V ring
   static constexpr int kQOff = kVOff + kStagesV * kTileBytes; // Q tile (128 x D, bf16; f16 after conversion)
@@ -115,6 +119,17 @@ struct Bars {
 // [D/64 column chunks][128 rows][128 B] with the 128-byte TMA swizzle.
 __device__ __forceinline__ uint32_t tile_off(int r, int c) {
   return (uint32_t)((c >> 3) * (kKvTile * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+// Byte offset of 16-byte chunk c of row r in a raw cache tile whose rows are
+// RB bytes (one column chunk): the TMA swizzle of that row width (128 B: the
+// chunk index XOR row % 8; 64 B: XOR (row / 2) % 4, the pattern repeating
+// every 512 bytes).
+template <int RB>
+__device__ __forceinline__ uint32_t raw_off(int r, int c) {
+  static_assert(RB == 128 || RB == 64, "raw tile rows");
+  if constexpr (RB == 128) return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+  return (uint32_t)(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
 }
 
 __device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16* p) {
@@ -180,7 +195,7 @@ __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CU
   const int boxes = kKvTile / p.box_rows;
   const int grp = lane % boxes, chunk = lane / boxes;
   const bool active = chunk < L::kChunks;
-  const int box_off = chunk * (kKvTile * 128) + grp * (p.box_rows * 128);
+  const int box_off = chunk * (kKvTile * L::kRowBytes) + grp * (p.box_rows * L::kRowBytes);
   const bool paged = p.page_size > 0;
   const bool rows = p.row_gather != 0;          // pages of 1, 2 or 4 tokens
   const int per = boxes <= 32 ? 32 / boxes : 1;  // tiles whose page numbers one warp-wide load covers
@@ -225,7 +240,7 @@ __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CU
       }
 #pragma unroll
       for (int c = 0; c < kPieces; ++c)
-        cp_async_16(stage + (c >> 3) * (kKvTile * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4),
+        cp_async_16(stage + (c >> 3) * (kKvTile * L::kRowBytes) + raw_off<L::kRowBytes>(r, c & 7),
                     src + (bytes ? c * 16 : 0), bytes);
     }
     cp_async_commit();
@@ -251,6 +266,15 @@ __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CU
     int t0g = w.kv_begin;
     int gnext = load_pages(w, t0g + per * kKvTile);
     if (!kIsV && L::kTc && w.kind == kPrefill && num_tiles(w) > 0) {
+      // Row gather: the last tile of the previous item is still unmarked (a
+      // tile is marked once the next one has been issued), and the Q buffer
+      // frees only when that tile's S MMAs have run: mark it now, or the two
+      // would wait on each other.
+      if (rows && pend >= 0) {
+        cp_async_wait_group<0>();
+        mark_full(pend);
+        pend = -1;
+      }
       if (!warp_wait(B.q_empty, (pi & 1) ^ 1, abort_flag)) {
         ok = false;
         break;
@@ -385,11 +409,17 @@ __device__ bool s_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
       if (use >= 1 && !mbar_wait(&B.o_done[b], (use - 1) & 1, abort_flag)) return false;
       tc_fence_after();
       if constexpr (QF8) {
-        // e4m3 rows of 128 bytes (one swizzle atom wide): K=32 per MMA, 32 bytes apart
+        // e4m3 rows of D bytes (one swizzle atom wide: 128-byte swizzle at D =
+        // 128, 64-byte at D = 64): K=32 per MMA, 32 bytes apart
 #pragma unroll
-        for (int k = 0; k < D / 32; ++k)
-          umma_ss_e4m3(tmem + b * 128, sdesc_sw128(q_base + k * 32, 16, 1024),
-                       sdesc_sw128(k_base + k * 32, 16, 1024), kIdescQK, k > 0 ? 1u : 0u);
+        for (int k = 0; k < D / 32; ++k) {
+          if constexpr (D == 128)
+            umma_ss_e4m3(tmem + b * 128, sdesc_sw128(q_base + k * 32, 16, 1024),
+                         sdesc_sw128(k_base + k * 32, 16, 1024), kIdescQK, k > 0 ? 1u : 0u);
+          else
+            umma_ss_e4m3(tmem + b * 128, sdesc_sw64(q_base + k * 32, 16, 512), sdesc_sw64(k_base + k * 32, 16, 512),
+                         kIdescQK, k > 0 ? 1u : 0u);
+        }
       } else {
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
@@ -471,14 +501,16 @@ __device__ bool pv_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, vol
 // exactly (every e4m3 value is an f16 value), zeroing V rows past the
 // sequence; and the bf16 Q tile of each item into f16 in place.  Converted
 // tiles are double-buffered (T % 2); raw stages are released after conversion.
+template <int D>
 __device__ __forceinline__ void convert_tile(const uint8_t* raw, uint8_t* conv, int ct, int zero_from) {
+  constexpr int kCpr = D / 16;  // raw 16-byte chunks per row (e4m3 rows of D bytes)
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
+  for (int k = 0; k < kCpr; ++k) {
     const int u = ct + 128 * k;
-    const int r = u >> 3, c = u & 7;  // raw 16-byte chunk c of row r: d = 16c .. 16c+15
+    const int r = u / kCpr, c = u % kCpr;  // raw 16-byte chunk c of row r: d = 16c .. 16c+15
     uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
     if (r < zero_from) {
-      const uint4 w = *reinterpret_cast<const uint4*>(raw + r * 128 + ((c ^ (r & 7)) << 4));
+      const uint4 w = *reinterpret_cast<const uint4*>(raw + raw_off<D>(r, c));
       lo = make_uint4(e4m3x2_to_f16x2(w.x), e4m3x2_to_f16x2(w.x >> 16), e4m3x2_to_f16x2(w.y),
                       e4m3x2_to_f16x2(w.y >> 16));
       hi = make_uint4(e4m3x2_to_f16x2(w.z), e4m3x2_to_f16x2(w.z >> 16), e4m3x2_to_f16x2(w.w),
@@ -522,13 +554,14 @@ __device__ bool converter(const AttnParams& p, uint8_t* smem, const Bars& B, vol
       };
       const uint8_t* qb = smem + L::kQOff;
       uint8_t* q8 = smem + L::kKcOff;
+      constexpr int kCpr = D / 16;  // e4m3 16-byte chunks per row
 #pragma unroll 2
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < kCpr; ++k) {
         const int u = ct + 128 * k;
-        const int r = u >> 3, c = u & 7;
+        const int r = u / kCpr, c = u % kCpr;
         const uint4 a = *reinterpret_cast<const uint4*>(qb + tile_off(r, 2 * c));
         const uint4 b = *reinterpret_cast<const uint4*>(qb + tile_off(r, 2 * c + 1));
-        *reinterpret_cast<uint4*>(q8 + r * 128 + ((c ^ (r & 7)) << 4)) =
+        *reinterpret_cast<uint4*>(q8 + raw_off<D>(r, c)) =
             make_uint4(quant4(a.x, a.y), quant4(a.z, a.w), quant4(b.x, b.y), quant4(b.z, b.w));
       }
     } else {
@@ -551,8 +584,8 @@ __device__ bool converter(const AttnParams& p, uint8_t* smem, const Bars& B, vol
       if constexpr (!QF8) {
         if (!warp_wait(&B.full_k[rk.stage], rk.phase, abort_flag)) return false;
         if (T >= 2 && !warp_wait(&B.kc_empty[T & 1], ((T >> 1) - 1) & 1, abort_flag)) return false;
-        convert_tile(smem + L::kKOff + rk.stage * L::kTileBytes, smem + L::kKcOff + (T & 1) * L::kConvTile, ct,
-                     kKvTile);
+        convert_tile<D>(smem + L::kKOff + rk.stage * L::kTileBytes, smem + L::kKcOff + (T & 1) * L::kConvTile, ct,
+                        kKvTile);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -563,8 +596,8 @@ __device__ bool converter(const AttnParams& p, uint8_t* smem, const Bars& B, vol
       if (!warp_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
       if (T >= 2 && !warp_wait(&B.vc_empty[T & 1], ((T >> 1) - 1) & 1, abort_flag)) return false;
       // rows past the sequence may hold anything (even NaN): they become zeros
-      convert_tile(smem + L::kVOff + rv.stage * L::kTileBytes, smem + L::kVcOff + (T & 1) * L::kConvTile, ct,
-                   w.lk - t0);
+      convert_tile<D>(smem + L::kVOff + rv.stage * L::kTileBytes, smem + L::kVcOff + (T & 1) * L::kConvTile, ct,
+                      w.lk - t0);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -1104,12 +1137,13 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
 // same d permutation serves both operands: for k-step ks = 2G+h, thread t's
 // k slots 4t..4t+3 and 16+4t..16+4t+3 are dims 16(4G+t) + 8h + {0..3 | 4..7},
 // i.e. words 2h and 2h+1 of the 16-byte chunk 4G+t of a key row.
-template <bool PF, int KPW, bool QF8>
+template <int D, bool PF, int KPW, bool QF8>
 __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* smem, const Bars& B,
                              volatile int* abort_flag, Ring& rk, Ring& rv, float sl2, float vscale) {
-  using L = Layout<128, true, PF>;
-  constexpr int D = 128;
+  using L = Layout<D, true, PF>;
   constexpr int NT = KPW / 8;
+  constexpr int NO = D / 8;        // O column tiles
+  constexpr int RB = L::kRowBytes; // raw e4m3 row: D bytes (64-byte swizzle at D = 64)
   const int lane = threadIdx.x & 31;
   const int cw = (threadIdx.x >> 5) - 2;
   const int ctid = threadIdx.x - 64;
@@ -1126,7 +1160,7 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
   };
   const int lim0 = limit_of(r0), lim1 = limit_of(r1);
 
-  uint32_t qa[8][4];  // f16 fragments (8 k-steps of 16), or e4m3 ones (QF8: 4 k-steps of 32)
+  uint32_t qa[D / 16][4];  // f16 fragments (D/16 k-steps of 16), or e4m3 ones (QF8: D/32 k-steps of 32)
   {
     const __nv_bfloat16* q0 = nullptr;
     const __nv_bfloat16* q1 = nullptr;
@@ -1145,7 +1179,7 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
         return a | (b << 16);
       };
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
+      for (int ks = 0; ks < D / 32; ++ks) {
         const int d0 = 16 * (4 * (ks >> 1) + t) + 8 * (ks & 1);
         const uint4 v0 = q0 ? __ldg(reinterpret_cast<const uint4*>(q0 + d0)) : make_uint4(0, 0, 0, 0);
         const uint4 v1 = q1 ? __ldg(reinterpret_cast<const uint4*>(q1 + d0)) : make_uint4(0, 0, 0, 0);
@@ -1156,7 +1190,7 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
       }
     } else {
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
+      for (int ks = 0; ks < D / 16; ++ks) {
         const int d0 = 64 * (ks >> 2) + 16 * t + 4 * (ks & 3);
         qa[ks][0] = q0 ? bf16x2_to_f16x2(ld_u32(q0 + d0)) : 0u;
         qa[ks][1] = q1 ? bf16x2_to_f16x2(ld_u32(q1 + d0)) : 0u;
@@ -1166,9 +1200,9 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
     }
   }
 
-  float o[16][4];
+  float o[NO][4];
 #pragma unroll
-  for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  for (int n = 0; n < NO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   int merge_stage = -1;
   // A failed (timed-out or aborted) wait ends this warp's tiles, but the warp
@@ -1189,8 +1223,8 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
     for (int nt = 0; nt < NT; ++nt) {
       const int key = kw0 + nt * 8 + g;
 #pragma unroll
-      for (int G = 0; G < 2; ++G) {
-        const uint4 kv = lds_u128(kraw + key * 128 + ((((4 * G + t) ^ (key & 7))) << 4));
+      for (int G = 0; G < D / 64; ++G) {
+        const uint4 kv = lds_u128(kraw + raw_off<RB>(key, 4 * G + t));
         const uint32_t wd[4] = {kv.x, kv.y, kv.z, kv.w};
         if constexpr (QF8) {
           mma_e4m3(s[nt], qa[2 * G][0], qa[2 * G][1], qa[2 * G][2], qa[2 * G][3], wd[0], wd[1]);
@@ -1244,7 +1278,7 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
     l0 = l0 * al0 + ls0;
     l1 = l1 * al1 + ls1;
 #pragma unroll
-    for (int n = 0; n < 16; ++n) {
+    for (int n = 0; n < NO; ++n) {
       o[n][0] *= al0;
       o[n][1] *= al0;
       o[n][2] *= al1;
@@ -1269,10 +1303,10 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
       const int mi = lane >> 3;
       const int key = kw0 + kk * 16 + (mi & 1) * 8 + (lane & 7);
 #pragma unroll
-      for (int db = 0; db < 4; ++db) {
+      for (int db = 0; db < D / 32; ++db) {
         const int chunk = 2 * db + (mi >> 1);
         uint32_t v0, v1, v2, v3;
-        ldsm_x4_t(vraw + key * 128 + ((chunk ^ (key & 7)) << 4), v0, v1, v2, v3);
+        ldsm_x4_t(vraw + raw_off<RB>(key, chunk), v0, v1, v2, v3);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const uint32_t va = h ? v2 : v0, vb = h ? v3 : v1;
@@ -1322,11 +1356,12 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
     }
     return true;
   }
-  // Merge of the four warps' partial results in the borrowed 16 KB V stage:
-  // fragments are added in fragment order (all warps share the layout),
-  // warps 2,3 into 0,1, then warp 1 into warp 0, which writes the rows.
+  // Merge of the four warps' partial results in the borrowed V stage (D x
+  // 128 bytes): fragments are added in fragment order (all warps share the
+  // layout), warps 2,3 into 0,1, then warp 1 into warp 0, which writes the rows.
+  static_assert(2 * NO * 32 * 16 <= L::kTileBytes, "merge buffer fits one V stage");
   float* ml = reinterpret_cast<float*>(smem + L::kMlOff);
-  float4* buf = reinterpret_cast<float4*>(smem + L::kVOff + merge_stage * L::kTileBytes);  // [2][16][32] float4
+  float4* buf = reinterpret_cast<float4*>(smem + L::kVOff + merge_stage * L::kTileBytes);  // [2][NO][32] float4
   int* bad = reinterpret_cast<int*>(ml + kConsumerWarps * kDecodeRows * 2);  // [warp]: its waits failed
   if (t == 0) {
     ml[(cw * 16 + g) * 2 + 0] = m0;
@@ -1352,7 +1387,7 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
   }
   const float f0 = ex2(m0 - Mu0), f1 = ex2(m1 - Mu1);
 #pragma unroll
-  for (int n = 0; n < 16; ++n) {
+  for (int n = 0; n < NO; ++n) {
     o[n][0] *= f0;
     o[n][1] *= f0;
     o[n][2] *= f1;
@@ -1360,12 +1395,12 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
   }
   auto put = [&](int slot) {
 #pragma unroll
-    for (int n = 0; n < 16; ++n) buf[(slot * 16 + n) * 32 + lane] = make_float4(o[n][0], o[n][1], o[n][2], o[n][3]);
+    for (int n = 0; n < NO; ++n) buf[(slot * NO + n) * 32 + lane] = make_float4(o[n][0], o[n][1], o[n][2], o[n][3]);
   };
   auto add = [&](int slot) {
 #pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      const float4 v = buf[(slot * 16 + n) * 32 + lane];
+    for (int n = 0; n < NO; ++n) {
+      const float4 v = buf[(slot * NO + n) * 32 + lane];
       o[n][0] += v.x;
       o[n][1] += v.y;
       o[n][2] += v.z;
@@ -1392,7 +1427,7 @@ __device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* sm
       const int tok = w.q_row0 + row / p.G;
       const int head = w.hk * p.G + row % p.G;
 #pragma unroll
-      for (int db = 0; db < 4; ++db)
+      for (int db = 0; db < D / 32; ++db)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const float* e = o[4 * db + 2 * h];
@@ -1457,8 +1492,8 @@ __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
     if (w.kind == kDecode) {
       if (mma_consumer) {
         if constexpr (FP8)
-          ok = run_item_fp8<PF, kKvTile / kConsumerWarps, QF8>(p, w, smem, B, abort_flag, rk, rv, QF8 ? sl2q : sl2,
-                                                                vscale);
+          ok = run_item_fp8<D, PF, kKvTile / kConsumerWarps, QF8>(p, w, smem, B, abort_flag, rk, rv,
+                                                                   QF8 ? sl2q : sl2, vscale);
         else
           ok = run_item<D, FP8, PF, kKvTile / kConsumerWarps>(p, w, smem, B, abort_flag, rk, rv, sl2, vscale);
       } else {
@@ -1646,11 +1681,16 @@ cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tm_k, const
                              bool overlap_prev, cudaStream_t stream) {
   if (num_ctas == 0) return cudaSuccess;
   const bool o = overlap_prev;
-  if (fp8)
+  if (fp8 && head_dim == 128)
     return has_prefill  ? (p.q_scale ? launch_t<128, true, true, true>(p, tm_k, tm_v, tm_q, num_ctas, o, stream)
                                      : launch_t<128, true, true>(p, tm_k, tm_v, tm_q, num_ctas, o, stream))
            : p.q_scale ? launch_t<128, true, false, true>(p, tm_k, tm_v, tm_q, num_ctas, o, stream)
                        : launch_t<128, true, false>(p, tm_k, tm_v, tm_q, num_ctas, o, stream);
+  if (fp8)
+    return has_prefill  ? (p.q_scale ? launch_t<64, true, true, true>(p, tm_k, tm_v, tm_q, num_ctas, o, stream)
+                                     : launch_t<64, true, true>(p, tm_k, tm_v, tm_q, num_ctas, o, stream))
+           : p.q_scale ? launch_t<64, true, false, true>(p, tm_k, tm_v, tm_q, num_ctas, o, stream)
+                       : launch_t<64, true, false>(p, tm_k, tm_v, tm_q, num_ctas, o, stream);
   if (head_dim == 128)
     return has_prefill ? launch_t<128, false, true>(p, tm_k, tm_v, tm_q, num_ctas, o, stream)
                        : launch_t<128, false, false>(p, tm_k, tm_v, tm_q, num_ctas, o, stream);

@@ -51,8 +51,6 @@ pkv_status validate_problem(const pkv_problem* p) {
     return fail(PKV_ERR_INVALID_ARG, "cache_dtype %d unknown", p->cache_dtype);
   if (p->head_dim != 64 && p->head_dim != 128)
     return fail(PKV_ERR_UNSUPPORTED, "head_dim %d not in {64, 128}", p->head_dim);
-  if (p->cache_dtype == PKV_FP8_E4M3 && p->head_dim != 128)
-    return fail(PKV_ERR_UNSUPPORTED, "fp8 cache needs head_dim 128");
   if (p->page_size < 0 || p->page_size > 256 ||
       (p->page_size >= kBoxRows && p->page_size % kBoxRows != 0) ||
       (p->page_size > 0 && p->page_size < kBoxRows && (p->page_size & (p->page_size - 1)) != 0))

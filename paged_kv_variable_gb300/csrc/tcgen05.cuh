@@ -86,6 +86,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// The same for K-major operands with 64-byte rows and the 64-byte swizzle
+// (layout code 4): 8-row groups of 512 bytes, `sbo` apart.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version of the sm_100 family
+  d |= (uint64_t)4 << 61;  // 64-byte swizzle
+  return d;
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulator, A/B type (0 f16, 1 bf16),
 // K-major A, B K-major (b_mn = 0) or MN-major (b_mn = 1), M x N tile.
 __host__ __device__ constexpr uint32_t idesc_f16(int ab_type, int b_mn, int m, int n) {

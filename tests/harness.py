@@ -138,9 +138,10 @@ def compare_lse(got_t, want: np.ndarray, tol=LSE_TOL):
 
 def gpu_random_case(seed: int, *, cache_dtype="bf16", d=None, page_size=None, causal=None, max_cache=700,
                     max_new=80, sentinel="finite", with_new=True, q_equals_new=True, g=None, hkv=None):
-    """Random case inside the library's supported set (D in {64,128}; P drawn from 0, 16, 32, 64, 256)."""
+    """Random case inside the library's supported set (D in {64,128}, either cache dtype; P drawn from 0, 16,
+    32, 64, 256)."""
     rng = np.random.default_rng(seed)
-    d = d or (128 if cache_dtype == "fp8" else int(rng.choice([64, 128])))
+    d = d or int(rng.choice([64, 128]))
     P = int(rng.choice([0, 16, 32, 64, 256])) if page_size is None else page_size
     hkv = hkv or int(rng.choice([1, 2, 4]))
     g = g or int(rng.choice([1, 2, 4, 8]))

@@ -51,7 +51,6 @@ def _problem(pkv, **kw):
     (dict(page_size=3), 2),
     (dict(page_size=12), 2),
     (dict(page_size=512), 2),
-    (dict(cache_dtype="fp8", head_dim=64), 2),
     (dict(cache_capacity=0), 1),
     (dict(cache_capacity=40), 1),   # not a multiple of the page size
     (dict(softmax_scale=0.0), 1),

@@ -57,6 +57,26 @@ def test_random_fp8(seed):
     run_full(H.gpu_random_case(100 + seed, cache_dtype="fp8", sentinel="nan" if seed % 2 else "finite"))
 
 
+@pytest.mark.parametrize("P,q8", [(16, False), (0, False), (1, False), (4, False), (8, False), (64, False),
+                                  (16, True), (0, True)])
+def test_fp8_head_dim_64(P, q8):
+    """fp8 cache at D = 64 (64-byte e4m3 rows, 64-byte TMA swizzle): a mixed
+    batch of decode steps (one split along the keys), short query runs and
+    prefills on cached prefixes; with q_scale, Q.K^T on e4m3 MMAs (warp MMAs
+    on decode tiles, tcgen05 kind::f8f6f4 on 64-byte-swizzled tiles)."""
+    import dataclasses
+    spec = synth.Spec(batch=5, hq=16, hkv=4, d=64, page_size=P, causal=True,
+                      softmax_scale=float(np.float32(1.0 / np.sqrt(64))), cache_dtype="fp8",
+                      q_lens=np.array([1, 300, 1, 6, 140], np.int32), cache_lens=np.array([3000, 100, 0, 900, 37], np.int32),
+                      new_lens=np.array([1, 300, 1, 6, 140], np.int32), capacity=3008, name="fp8-d64")
+    case = synth.make_case(spec, np.random.default_rng(900 + P))
+    if q8:
+        amax = float(np.abs(synth.bf16_bits_to_f32(case.q)).max())
+        case = dataclasses.replace(case, q_scale=float(np.float32(amax / 448.0)))
+    g, _ = run_full(case, num_sms=16)
+    assert g.plan.stats()["num_split_units"] > 0
+
+
 @pytest.mark.parametrize("layout", ["head_pad", "base_offset"])
 @pytest.mark.parametrize("cache_dtype", ["bf16", "fp8"])
 def test_output_rows_not_32_byte_aligned(layout, cache_dtype):
