@@ -339,6 +339,10 @@ WORKLOAD_NAMES = {
     "prefill": "prefill: B=8, 512 new tokens on a 1536-token cached prefix, Hq=32, Hkv=8, D=128, bf16 "
                "contiguous cache, causal (profiler captures)",
     "fp8-decode": "decode at kv length 2048 on the fp8 cache of the B=64 fp8 prefill (profiler captures)",
+    "fp8-prefill-small": "fp8 cache: causal prefill of 2048 tokens into an empty cache, B=4, Hq=32, Hkv=8, D=128, "
+                         "page 16 (profiler captures)",
+    "mixed": "mixed: 60 decode requests (cache U[1024,8192]) + 4 prefill requests (2048 tokens on U[0,2048]), "
+             "Hq=32, Hkv=8, D=128, bf16 paged cache page 16, one launch (profiler captures)",
 }
 
 
@@ -519,7 +523,7 @@ def gpu_arm(args):
     peaks = _peaks()
 
     decode_case = synth.config2()
-    cpu_base = cpu_oracle_leg(12.0 if args.cpu_leg else 1.5) if rank == 0 else None
+    cpu_base = cpu_oracle_leg(12.0 if args.cpu_leg else 1.5) if rank == 0 and not args.quick else None
 
     from paged_kv_variable_gb300 import build
     build.build()
@@ -542,6 +546,12 @@ def gpu_arm(args):
         main.g.k_cache.copy_(pre.g.k_cache)
         main.g.v_cache.copy_(pre.g.v_cache)
         del pre
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()   # only the decode step's buffers stay on the device
+    elif args.workload == "fp8-prefill-small":
+        main = Workload("fp8-prefill-small", synth.config5(batch=4)[0], device)
+    elif args.workload == "mixed":
+        main = Workload("mixed", synth.config4(), device)
     else:
         main = Workload("decode", decode_case, device)
     with ClockSampler(local) as clk:
@@ -557,6 +567,12 @@ def gpu_arm(args):
             dist.barrier()
         t_wall = time.perf_counter() - t_wall
     clocks = clk.summary()
+    if args.quick:
+        # profiler runs: the timed graph replays only
+        if rank == 0:
+            print(json.dumps({"workload": args.workload, "ms_per_step": round(statistics.median(step_ms), 5),
+                              "attn_kernel_ms": round(statistics.median(kern_ms), 5), "quick": True}))
+        return
     eager_ms, eager_kern_ms = time_workload(main, max(10, args.steps // 4), 3, flush, stream, graph=False)
     t_step, job_bytes_per_s = aggregate_over_ranks(statistics.median(step_ms), main.work["bytes"], world, device)
     t_kern = statistics.median(kern_ms)
@@ -702,7 +718,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-secondary", dest="secondary", action="store_false")
-    ap.add_argument("--workload", default="decode", choices=["decode", "decode-small", "prefill", "fp8-decode"])
+    ap.add_argument("--workload", default="decode", choices=sorted(WORKLOAD_NAMES))
+    ap.add_argument("--quick", action="store_true",
+                    help="profiler runs: time the graph replays of the workload only (no CPU, eager, e2e or "
+                         "secondary legs)")
     ap.add_argument("--no-cpu-leg", dest="cpu_leg", action="store_false")
     ap.add_argument("--oracle-leg-child", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--oracle-threads", type=int, default=1, help=argparse.SUPPRESS)
