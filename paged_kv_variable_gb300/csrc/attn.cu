@@ -58,17 +58,26 @@ constexpr uint32_t kTmemO = 384;
 
 template <int D, bool FP8, bool PF>
 struct Layout {
-  // Warp roles: 0 K/Q producer, 1 S = Q K^T issuer, 2..5 consumers (softmax
-  // of prefill tiles, warp-MMA decode tiles), 6 V producer, for an fp8 cache
-  // 7..10 converters (e4m3 K/V tiles and the bf16 Q tile to f16 MMA
-  // operands), and with prefill tiles a last warp issuing O += P V.
+  // Warp roles with prefill tiles (tcgen05): 0 K/Q producer, 1 S = Q K^T
+  // issuer, 2..5 consumers (softmax of prefill tiles, warp-MMA decode tiles),
+  // 6 V producer, for an fp8 cache 7..10 converters (e4m3 K/V tiles and the
+  // bf16 Q tile to f16 MMA operands), and a last warp issuing O += P V.
+  // Decode-only plans: 0 K producer, 1 V producer, 2.. decode consumers.
   static constexpr bool kTc = PF;                           // prefill tiles (on tcgen05) in the plan
   static constexpr int kSoftmaxWarps = kConsumerWarps;      // one per TMEM lane quarter
-  static constexpr int kVProducerWarp = 2 + kSoftmaxWarps;
-  static constexpr int kConvWarp0 = kVProducerWarp + 1;
+  // Decode-only plans over an fp8 cache, whose tiles carry half the bytes of a
+  // bf16 tile for the same arithmetic: each consumer warp copies its share of
+  // a K and a V tile into registers and releases both stages at once (a stage
+  // is held for a few shared-memory loads, not the tile's arithmetic).  One
+  // group of consumer warps: two groups taking alternate tiles measured slower.
+  static constexpr bool kStageRegs = FP8 && !PF;
+  static constexpr int kDecGroups = 1;
+  static constexpr int kDecWarps = kConsumerWarps * kDecGroups;  // decode consumer warps
+  static constexpr int kVProducerWarp = PF ? 2 + kSoftmaxWarps : 1;
+  static constexpr int kConvWarp0 = 2 + kSoftmaxWarps + 1;
   static constexpr int kConvWarps = (FP8 && PF) ? 4 : 0;
   static constexpr int kPvWarp = kConvWarp0 + kConvWarps;
-  static constexpr int kThreads = 32 * (3 + kSoftmaxWarps + kConvWarps + (PF ? 1 : 0));
+  static constexpr int kThreads = PF ? 32 * (3 + kSoftmaxWarps + kConvWarps + 1) : 32 * (2 + kDecWarps);
   static constexpr int kEsize = FP8 ? 1 : 2;
   // decode-only plans give all shared memory to the rings
   static constexpr int kStagesK = PF ? (FP8 ? 2 : (D == 128 ? 3 : 4)) : (FP8 || D == 64 ? 6 : 4);
@@ -85,9 +94,15 @@ struct Layout {
   static constexpr int kConvTile = kKvTile * D * 2;           // one converted (f16) K or V tile
   static constexpr int kKcOff = kQOff + (PF ? kKvTile * D * 2 : 0);  // fp8: converted K tiles [2]
   static constexpr int kVcOff = kKcOff + (kConvWarps ? 2 * kConvTile : 0);  // fp8: converted V tiles [2]
-  // decode merge scratch: the item's last V stage, borrowed before it is released
-  static constexpr int kMlOff = kVcOff + (kConvWarps ? 2 * kConvTile : 0);  // float[4][16][2] (m, l), int[4]
-  static constexpr int kBarOff = kMlOff + kConsumerWarps * kDecodeRows * 2 * 4 + 16;  // + failed-wait flags
+  // decode merge scratch: the item's last V stage, borrowed before it is
+  // released, or (tiles staged in registers, every stage released at once)
+  // its own area
+  static constexpr int kMergeOff = kVcOff + (kConvWarps ? 2 * kConvTile : 0);
+  // (tiles staged in registers: every warp's O^T of one 8-column tile, or the
+  // tree's slots of two column tiles)
+  static constexpr int kMergeBytes = kStageRegs ? kDecWarps * (D / 16) * 32 * 16 : 0;
+  static constexpr int kMlOff = kMergeOff + kMergeBytes;     // float[kDecWarps][16][2] (m, l), int[kDecWarps]
+  static constexpr int kBarOff = kMlOff + kDecWarps * kDecodeRows * 2 * 4 + kDecWarps * 4;  // + failed-wait flags
   static constexpr int kNumBars = 2 * kStagesK + 2 * kStagesV + 3 + 3 * kSBufs + 9 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;     // tmem base, abort flag
   static constexpr int kBytes = kMiscOff + 16;
@@ -870,55 +885,117 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
   return true;
 }
 
-// ------------------------------------------------------------------ warp-MMA tiles of a bf16 cache (decode)
-// KPW = keys of each 128-key tile handled by one warp (the four warps split a tile).
-template <int D, bool FP8, bool PF, int KPW>
-__device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, const Bars& B,
-                         volatile int* abort_flag, Ring& rk, Ring& rv, float sl2, float vscale) {
+// ------------------------------------------------------------------ decode tiles (warp MMAs)
+// A decode unit has R = n_q * G <= 16 query rows.  The four consumer warps
+// split each 128-key tile (32 keys each) and compute it transposed: keys and
+// head dims fill the 16-row M side of m16n8k16 MMAs and the unit's query rows
+// the 8-column N side (NQ column tiles of 8), S^T = K Q^T, then O^T += V^T P^T,
+// P^T handed from the S^T accumulators to the B operand by 8x8 transposes
+// (movmatrix).  With G = 4 query rows this takes half the MMAs of the
+// untransposed form, whose 16-row M was three quarters padding; the legacy
+// warp-MMA path is what bounded these tiles.
+//
+// fp8 cache: e4m3 K and V become f16 in registers (exact).  A dot product does
+// not depend on the order of d, so the k slots of k-step 4c+u of a thread with
+// column index t map to d = 64c + 16t + 4u + {0,1 | 2,3} for both K and Q: one
+// 16-byte read of a key row serves four k-steps.  For V an ldmatrix.trans on
+// byte pairs gives a thread keys (2t, 2t+1) x d (2g, 2g+1) of a 16-byte chunk;
+// a byte permute splits that into the A rows g (d = 2g) and g+8 (d = 2g+1), so
+// the O^T rows of chunk c are d = 16c + 2g and 16c + 2g + 1.  With q_scale
+// (QF8) S^T runs as m16n8k32 e4m3 MMAs on the raw K bytes (k-step 2c+h: words
+// 2h, 2h+1 of chunk 4c+t).
+//
+// Decode-only plans over an fp8 cache (kStageRegs) copy each warp's share of
+// the K and V tiles into registers and release both stages before any
+// arithmetic; otherwise K is released after S and V after P V, the item's
+// last V stage serving as the merge scratch.
+template <int D, bool FP8, bool PF, bool QF8, int NQ>
+__device__ bool run_decode(const AttnParams& p, const WorkItem& w, uint8_t* smem, const Bars& B,
+                           volatile int* abort_flag, Ring& rk, Ring& rv, float sl2, float vscale, uint32_t& dtc) {
   using L = Layout<D, FP8, PF>;
-  constexpr int NT = KPW / 8;       // S column tiles per warp
-  constexpr int KS = D / 16;        // k-steps of Q K^T
-  constexpr int NO = D / 8;         // O column tiles
+  constexpr bool kArea = L::kStageRegs;          // the merge area exists (else: the borrowed V stage)
+  constexpr bool kRegs = L::kStageRegs && NQ == 1;  // tiles staged in registers (no room at NQ = 2)
+  constexpr int W = L::kDecWarps;                // consumer warps merged at the end of the item
+  constexpr int kThreadsW = 32 * W;
+  constexpr int KPW = kKvTile / kConsumerWarps;  // keys of each tile per warp
+  constexpr int MT = KPW / 16;                   // key m-tiles per warp
+  constexpr int DT = D / 16;                     // head-dim m-tiles of O^T
+  constexpr int KS = QF8 ? D / 32 : D / 16;      // k-steps of S^T
+  constexpr int RB = L::kRowBytes;
+  constexpr int kFin = D + 4;                    // row stride (floats) of the merged O in shared memory
   const int lane = threadIdx.x & 31;
-  const int cw = (threadIdx.x >> 5) - 2;  // consumer warp 0..3
+  const int cw = (threadIdx.x >> 5) - 2;         // 0 .. W-1
+  const int gi = cw / kConsumerWarps;            // consumer group: it runs the tiles with dtc % groups == gi
   const int ctid = threadIdx.x - 64;
   const int g = lane >> 2, t = lane & 3;
-  const int row_blk = 0;    // a decode unit is at most 16 rows: one MMA row block
-  const int kw0 = cw * KPW;  // this warp's keys of each tile
+  const int mi = lane >> 3;                      // ldmatrix: the 8x8 matrix this lane addresses
+  const int kw0 = (cw % kConsumerWarps) * KPW;   // this warp's keys of each of its group's tiles
   const int R = w.n_q * p.G;
-  const int r0 = row_blk * 16 + g, r1 = r0 + 8;
 
-  auto limit_of = [&](int r) {
-    if (r >= R) return w.kv_begin;
-    int lim = w.kv_end;
-    if (p.causal) lim = min(lim, w.q_i0 + r / p.G + w.lk - w.lq + 1);
-    return lim;
-  };
-  const int lim0 = limit_of(r0), lim1 = limit_of(r1);
-
-  // Q fragments (A operand of m16n8k16), rows r0 / r1
-  uint32_t qa[KS][4];
-  {
-    const __nv_bfloat16* q0 = nullptr;
-    const __nv_bfloat16* q1 = nullptr;
-    if (r0 < R)
-      q0 = p.q + (int64_t)(w.q_row0 + r0 / p.G) * p.q_stride_tok + (int64_t)(w.hk * p.G + r0 % p.G) * p.q_stride_head;
-    if (r1 < R)
-      q1 = p.q + (int64_t)(w.q_row0 + r1 / p.G) * p.q_stride_tok + (int64_t)(w.hk * p.G + r1 % p.G) * p.q_stride_head;
+  // this thread's query rows (N columns of S^T and O^T): 8j + 2t + e
+  int lim[NQ][2];
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      const int c = ks * 16 + 2 * t;
-      qa[ks][0] = q0 ? ld_u32(q0 + c) : 0u;
-      qa[ks][1] = q1 ? ld_u32(q1 + c) : 0u;
-      qa[ks][2] = q0 ? ld_u32(q0 + c + 8) : 0u;
-      qa[ks][3] = q1 ? ld_u32(q1 + c + 8) : 0u;
+  for (int j = 0; j < NQ; ++j)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int r = 8 * j + 2 * t + e;
+      int l = w.kv_begin;
+      if (r < R) {
+        l = w.kv_end;
+        if (p.causal) l = min(l, w.q_i0 + r / p.G + w.lk - w.lq + 1);
+      }
+      lim[j][e] = l;
+    }
+
+  // Q^T (B operand): query row 8j + g of the tile
+  uint32_t qb[NQ][KS][2];
+#pragma unroll
+  for (int j = 0; j < NQ; ++j) {
+    const int r = 8 * j + g;
+    const __nv_bfloat16* qr =
+        r < R ? p.q + (int64_t)(w.q_row0 + r / p.G) * p.q_stride_tok + (int64_t)(w.hk * p.G + r % p.G) * p.q_stride_head
+              : nullptr;
+    if constexpr (QF8) {
+      // the cache's encode: one IEEE reciprocal, an RN multiply per value, RN satfinite to e4m3
+      const float inv_q = __frcp_rn(__ldg(p.q_scale));
+      auto quant4 = [&](uint32_t w0, uint32_t w1) -> uint32_t {
+        auto lo = [](uint32_t v) { return __uint_as_float(v << 16); };
+        auto hi = [](uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); };
+        const uint32_t a = f32x2_to_e4m3x2(__fmul_rn(lo(w0), inv_q), __fmul_rn(hi(w0), inv_q));
+        const uint32_t b = f32x2_to_e4m3x2(__fmul_rn(lo(w1), inv_q), __fmul_rn(hi(w1), inv_q));
+        return a | (b << 16);
+      };
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const int d0 = 16 * (4 * (ks >> 1) + t) + 8 * (ks & 1);
+        const uint4 v = qr ? __ldg(reinterpret_cast<const uint4*>(qr + d0)) : make_uint4(0, 0, 0, 0);
+        qb[j][ks][0] = quant4(v.x, v.y);
+        qb[j][ks][1] = quant4(v.z, v.w);
+      }
+    } else if constexpr (FP8) {
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const int d0 = 64 * (ks >> 2) + 16 * t + 4 * (ks & 3);
+        qb[j][ks][0] = qr ? bf16x2_to_f16x2(ld_u32(qr + d0)) : 0u;
+        qb[j][ks][1] = qr ? bf16x2_to_f16x2(ld_u32(qr + d0 + 2)) : 0u;
+      }
+    } else {
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        qb[j][ks][0] = qr ? ld_u32(qr + 16 * ks + 2 * t) : 0u;
+        qb[j][ks][1] = qr ? ld_u32(qr + 16 * ks + 8 + 2 * t) : 0u;
+      }
     }
   }
 
-  float o[NO][4];
+  float o[NQ][DT][4];
 #pragma unroll
-  for (int n = 0; n < NO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  for (int j = 0; j < NQ; ++j)
+#pragma unroll
+    for (int dt = 0; dt < DT; ++dt) o[j][dt][0] = o[j][dt][1] = o[j][dt][2] = o[j][dt][3] = 0.f;
+  float m[NQ][2], l[NQ][2];
+#pragma unroll
+  for (int j = 0; j < NQ; ++j) m[j][0] = m[j][1] = -INFINITY, l[j][0] = l[j][1] = 0.f;
   int merge_stage = -1;
   // A failed (timed-out or aborted) wait ends this warp's tiles, but the warp
   // still passes every barrier of the merge below, so that no other consumer
@@ -926,130 +1003,230 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
   bool failed = false;
 
   for (int t0 = w.kv_begin; t0 < w.kv_end; t0 += kKvTile) {
+    const bool mine = L::kDecGroups == 1 || (int)(dtc % L::kDecGroups) == gi;
+    ++dtc;
+    if (!mine) {  // the other group's tile: every warp advances the rings over all tiles
+      rk.advance<L::kStagesK>();
+      rv.advance<L::kStagesV>();
+      continue;
+    }
     if (!warp_wait(&B.full_k[rk.stage], rk.phase, abort_flag)) {
       failed = true;
       break;
     }
-    uint8_t* stage_k = smem + L::kKOff + rk.stage * L::kTileBytes;
-    uint8_t* stage_v = smem + L::kVOff + rv.stage * L::kTileBytes;
-    const uint32_t kb = smem_u32(stage_k);
-    const uint32_t vb = smem_u32(stage_v);
-
-    // S = Q K^T over this warp's keys
-    float s[NT][4];
+    const uint32_t kb = smem_u32(smem + L::kKOff + rk.stage * L::kTileBytes);
+    const uint32_t vb = smem_u32(smem + L::kVOff + rv.stage * L::kTileBytes);
+    // fp8: this warp's K rows (16 bytes of each per lane) and, staged, its V fragments
+    uint4 kreg[kRegs ? MT : 1][2][kRegs ? D / 64 : 1];
+    uint32_t vreg[kRegs ? MT : 1][kRegs ? D / 32 : 1][4];
+    if constexpr (kRegs) {
 #pragma unroll
-    for (int n = 0; n < NT; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+      for (int i = 0; i < MT; ++i)
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
-      for (int np = 0; np < NT / 2; ++np) {
-        const int r = kw0 + np * 16 + (lane >> 4) * 8 + (lane & 7);
-        const int c = 2 * ks + ((lane >> 3) & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kb + tile_off(r, c), b0, b1, b2, b3);
-        mma_bf16(s[2 * np], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-        mma_bf16(s[2 * np + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+          for (int c = 0; c < D / 64; ++c) kreg[i][h][c] = lds_u128(kb + raw_off<RB>(kw0 + 16 * i + 8 * h + g, 4 * c + t));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B.empty_k[rk.stage]);
+      if (!warp_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) {
+        failed = true;
+        break;
       }
+#pragma unroll
+      for (int i = 0; i < MT; ++i)
+#pragma unroll
+        for (int cp = 0; cp < D / 32; ++cp)
+          ldsm_x4_t(vb + raw_off<RB>(kw0 + 16 * i + (mi & 1) * 8 + (lane & 7), 2 * cp + (mi >> 1)), vreg[i][cp][0],
+                    vreg[i][cp][1], vreg[i][cp][2], vreg[i][cp][3]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B.empty_v[rv.stage]);
     }
 
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&B.empty_k[rk.stage]);
-
-    // mask (select, never add) + online softmax in the log2 domain
-    const int jb = t0 + kw0 + 2 * t;
-    float mx0 = -INFINITY, mx1 = -INFINITY;
+    // S^T = K Q^T: key m-tile i, query column tile j
+    float s[NQ][MT][4];
 #pragma unroll
-    for (int n = 0; n < NT; ++n) {
+    for (int j = 0; j < NQ; ++j)
+#pragma unroll
+      for (int i = 0; i < MT; ++i) s[j][i][0] = s[j][i][1] = s[j][i][2] = s[j][i][3] = 0.f;
+#pragma unroll
+    for (int i = 0; i < MT; ++i) {
+      if constexpr (FP8) {
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          uint4 ka, kc;
+          if constexpr (kRegs) {
+            ka = kreg[i][0][c];
+            kc = kreg[i][1][c];
+          } else {
+            ka = lds_u128(kb + raw_off<RB>(kw0 + 16 * i + g, 4 * c + t));
+            kc = lds_u128(kb + raw_off<RB>(kw0 + 16 * i + 8 + g, 4 * c + t));
+          }
+          const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w}, wc[4] = {kc.x, kc.y, kc.z, kc.w};
+          if constexpr (QF8) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int j = 0; j < NQ; ++j)
+                mma_e4m3(s[j][i], wa[2 * h], wc[2 * h], wa[2 * h + 1], wc[2 * h + 1], qb[j][2 * c + h][0],
+                         qb[j][2 * c + h][1]);
+          } else {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const uint32_t a0 = e4m3x2_to_f16x2(wa[u]), a1 = e4m3x2_to_f16x2(wc[u]);
+              const uint32_t a2 = e4m3x2_to_f16x2(wa[u] >> 16), a3 = e4m3x2_to_f16x2(wc[u] >> 16);
+#pragma unroll
+              for (int j = 0; j < NQ; ++j) mma_f16(s[j][i], a0, a1, a2, a3, qb[j][4 * c + u][0], qb[j][4 * c + u][1]);
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(kb + tile_off(kw0 + 16 * i + (mi & 1) * 8 + (lane & 7), 2 * ks + (mi >> 1)), a0, a1, a2, a3);
+#pragma unroll
+          for (int j = 0; j < NQ; ++j) mma_bf16(s[j][i], a0, a1, a2, a3, qb[j][ks][0], qb[j][ks][1]);
+        }
+      }
+    }
+    if constexpr (!kRegs) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B.empty_k[rk.stage]);
+    }
+
+    // mask (select, never add) and online softmax in the log2 domain; a
+    // query row's keys are spread over the 8 lanes of its column (g)
+    float al[NQ][2];
+#pragma unroll
+    for (int j = 0; j < NQ; ++j) {
+      float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int i = 0; i < MT; ++i) {
+        const int ka = t0 + kw0 + 16 * i + g, kc = ka + 8;
+        s[j][i][0] = ka < lim[j][0] ? s[j][i][0] * sl2 : -INFINITY;
+        s[j][i][1] = ka < lim[j][1] ? s[j][i][1] * sl2 : -INFINITY;
+        s[j][i][2] = kc < lim[j][0] ? s[j][i][2] * sl2 : -INFINITY;
+        s[j][i][3] = kc < lim[j][1] ? s[j][i][3] * sl2 : -INFINITY;
+        mx[0] = fmax3(mx[0], s[j][i][0], s[j][i][2]);
+        mx[1] = fmax3(mx[1], s[j][i][1], s[j][i][3]);
+      }
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int j = jb + n * 8 + e;
-        s[n][e] = j < lim0 ? s[n][e] * sl2 : -INFINITY;
-        s[n][2 + e] = j < lim1 ? s[n][2 + e] * sl2 : -INFINITY;
-        mx0 = fmaxf(mx0, s[n][e]);
-        mx1 = fmaxf(mx1, s[n][2 + e]);
+        mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 4));
+        mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 8));
+        mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 16));
+        const float mn = fmaxf(m[j][e], mx[e]);
+        const float mu = mn == -INFINITY ? 0.f : mn;
+        al[j][e] = ex2(m[j][e] - mu);
+        m[j][e] = mn;
+        mx[e] = mu;
+      }
+      float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < MT; ++i) {
+        s[j][i][0] = ex2(s[j][i][0] - mx[0]);
+        s[j][i][1] = ex2(s[j][i][1] - mx[1]);
+        s[j][i][2] = ex2(s[j][i][2] - mx[0]);
+        s[j][i][3] = ex2(s[j][i][3] - mx[1]);
+        ls0 += s[j][i][0] + s[j][i][2];
+        ls1 += s[j][i][1] + s[j][i][3];
+      }
+      l[j][0] = l[j][0] * al[j][0] + ls0;
+      l[j][1] = l[j][1] * al[j][1] + ls1;
+#pragma unroll
+      for (int dt = 0; dt < DT; ++dt) {
+        o[j][dt][0] *= al[j][0];
+        o[j][dt][1] *= al[j][1];
+        o[j][dt][2] *= al[j][0];
+        o[j][dt][3] *= al[j][1];
       }
     }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
-    const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float al0 = ex2(m0 - mu0), al1 = ex2(m1 - mu1);
-    m0 = mn0;
-    m1 = mn1;
-    float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      s[n][0] = ex2(s[n][0] - mu0);
-      s[n][1] = ex2(s[n][1] - mu0);
-      s[n][2] = ex2(s[n][2] - mu1);
-      s[n][3] = ex2(s[n][3] - mu1);
-      ls0 += s[n][0] + s[n][1];
-      ls1 += s[n][2] + s[n][3];
-    }
-    l0 = l0 * al0 + ls0;
-    l1 = l1 * al1 + ls1;
-#pragma unroll
-    for (int n = 0; n < NO; ++n) {
-      o[n][0] *= al0;
-      o[n][1] *= al0;
-      o[n][2] *= al1;
-      o[n][3] *= al1;
-    }
 
-    // O += P V
-    if (!warp_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) {
+    if (!kRegs && !warp_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) {
       failed = true;
       break;
     }
+    // O^T += V^T P^T, one key m-tile of P^T (16 keys) per k-step
     const bool vmask = t0 + kKvTile > w.lk;  // rows past the sequence may hold anything: zero them
 #pragma unroll
-    for (int kk = 0; kk < KPW / 16; ++kk) {
-      const uint32_t a0 = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
-      const uint32_t a1 = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
-      const uint32_t a2 = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-      const uint32_t a3 = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-      const int kbase = t0 + kw0 + kk * 16 + 2 * t;
-      const uint32_t mlo0 = (kbase < w.lk ? 0x0000FFFFu : 0u) | (kbase + 1 < w.lk ? 0xFFFF0000u : 0u);
-      const uint32_t mlo1 = (kbase + 8 < w.lk ? 0x0000FFFFu : 0u) | (kbase + 9 < w.lk ? 0xFFFF0000u : 0u);
+    for (int i = 0; i < MT; ++i) {
+      uint32_t pb[NQ][2];
 #pragma unroll
-      for (int dp = 0; dp < D / 16; ++dp) {
-        const int r = kw0 + kk * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-        const int c = 2 * dp + (lane >> 4);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vb + tile_off(r, c), b0, b1, b2, b3);
-        if (vmask) {
-          b0 &= mlo0;
-          b2 &= mlo0;
-          b1 &= mlo1;
-          b3 &= mlo1;
+      for (int j = 0; j < NQ; ++j) {
+        pb[j][0] = movm_t(FP8 ? pack_f16(s[j][i][0], s[j][i][1]) : pack_bf16(s[j][i][0], s[j][i][1]));
+        pb[j][1] = movm_t(FP8 ? pack_f16(s[j][i][2], s[j][i][3]) : pack_bf16(s[j][i][2], s[j][i][3]));
+      }
+      const int k0 = t0 + kw0 + 16 * i + 2 * t;
+      const uint32_t mlo = (k0 < w.lk ? 0x0000FFFFu : 0u) | (k0 + 1 < w.lk ? 0xFFFF0000u : 0u);
+      const uint32_t mhi = (k0 + 8 < w.lk ? 0x0000FFFFu : 0u) | (k0 + 9 < w.lk ? 0xFFFF0000u : 0u);
+      if constexpr (FP8) {
+#pragma unroll
+        for (int cp = 0; cp < D / 32; ++cp) {
+          uint32_t v[4];
+          if constexpr (kRegs) {
+            v[0] = vreg[i][cp][0], v[1] = vreg[i][cp][1], v[2] = vreg[i][cp][2], v[3] = vreg[i][cp][3];
+          } else {
+            ldsm_x4_t(vb + raw_off<RB>(kw0 + 16 * i + (mi & 1) * 8 + (lane & 7), 2 * cp + (mi >> 1)), v[0], v[1],
+                      v[2], v[3]);
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {  // chunk 2cp + h: O^T m-tile 2cp + h
+            uint32_t a0 = e4m3x2_to_f16x2(prmt(v[2 * h], 0u, 0x0020u));
+            uint32_t a1 = e4m3x2_to_f16x2(prmt(v[2 * h], 0u, 0x0031u));
+            uint32_t a2 = e4m3x2_to_f16x2(prmt(v[2 * h + 1], 0u, 0x0020u));
+            uint32_t a3 = e4m3x2_to_f16x2(prmt(v[2 * h + 1], 0u, 0x0031u));
+            if (vmask) {
+              a0 &= mlo;
+              a1 &= mlo;
+              a2 &= mhi;
+              a3 &= mhi;
+            }
+#pragma unroll
+            for (int j = 0; j < NQ; ++j) mma_f16(o[j][2 * cp + h], a0, a1, a2, a3, pb[j][0], pb[j][1]);
+          }
         }
-        mma_bf16(o[2 * dp], a0, a1, a2, a3, b0, b1);
-        mma_bf16(o[2 * dp + 1], a0, a1, a2, a3, b2, b3);
+      } else {
+#pragma unroll
+        for (int dt = 0; dt < DT; ++dt) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_t(vb + tile_off(kw0 + 16 * i + (mi >> 1) * 8 + (lane & 7), 2 * dt + (mi & 1)), a0, a1, a2, a3);
+          if (vmask) {
+            a0 &= mlo;
+            a1 &= mlo;
+            a2 &= mhi;
+            a3 &= mhi;
+          }
+#pragma unroll
+          for (int j = 0; j < NQ; ++j) mma_bf16(o[j][dt], a0, a1, a2, a3, pb[j][0], pb[j][1]);
+        }
       }
     }
-    if (t0 + kKvTile >= w.kv_end) {
-      merge_stage = rv.stage;  // released after the merge below, which uses it as scratch
-    } else {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&B.empty_v[rv.stage]);
+    if constexpr (!kRegs) {
+      if (!kArea && t0 + kKvTile >= w.kv_end) {
+        merge_stage = rv.stage;  // released after the merge below, which uses it as scratch
+      } else {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.empty_v[rv.stage]);
+      }
     }
     rk.advance<L::kStagesK>();
     rv.advance<L::kStagesV>();
   }
 
   // ---------------------------------------------------------------- epilogue
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-
+  // the row sums were accumulated per lane over its own keys
+#pragma unroll
+  for (int j = 0; j < NQ; ++j)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      l[j][e] += __shfl_xor_sync(0xffffffffu, l[j][e], 4);
+      l[j][e] += __shfl_xor_sync(0xffffffffu, l[j][e], 8);
+      l[j][e] += __shfl_xor_sync(0xffffffffu, l[j][e], 16);
+    }
   if (num_tiles(w) == 0) {
     // no key at all: every row is 0 with LSE -inf (a split-KV chunk that a
     // dynamic plan's current length left empty gives such a partial)
-    for (int idx = ctid; idx < R * D; idx += kConsumerThreads) {
+    for (int idx = ctid; idx < R * D; idx += kThreadsW) {
       const int row = idx / D, d = idx % D;
       if (w.partial >= 0) {
         p.partial_o[((int64_t)w.partial * kDecodeRows + row) * D + d] = 0.f;
@@ -1063,401 +1240,177 @@ __device__ bool run_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, 
     }
     return true;
   }
+  // Merge of the W warps' partial results.  The warps write their (m, l) per
+  // row; then either (one column tile, merge area) every warp writes its O^T
+  // fragments and every consumer thread sums the W warps' values of the
+  // output columns it writes, or the fragments are added in fragment order in
+  // a tree (the upper half of the remaining warps putting, the lower half
+  // adding) until warp 0 holds the sum and stores O / l as a [16][D] matrix
+  // over the slots it has read, and every consumer thread writes whole output
+  // rows from it.  Scratch: the borrowed V stage or the merge area.
+  constexpr bool kFlat = kArea && NQ == 1;
+  constexpr int kSlot = NQ * DT * 32;  // float4 per slot
+  constexpr int kScratch = kArea ? L::kMergeBytes : L::kTileBytes;
+  static_assert((kFlat ? W : W / 2) * kSlot * 16 <= kScratch, "merge slots fit the scratch");
+  static_assert(kFlat || kDecodeRows * kFin * 4 <= kScratch, "merged rows fit the scratch");
   float* ml = reinterpret_cast<float*>(smem + L::kMlOff);
-  float* mo = reinterpret_cast<float*>(smem + L::kVOff + merge_stage * L::kTileBytes);
-  int* bad = reinterpret_cast<int*>(ml + kConsumerWarps * kDecodeRows * 2);  // [warp]: its waits failed
-  if (t == 0) {
-    ml[(cw * 16 + g) * 2 + 0] = m0;
-    ml[(cw * 16 + g) * 2 + 1] = l0;
-    ml[(cw * 16 + g + 8) * 2 + 0] = m1;
-    ml[(cw * 16 + g + 8) * 2 + 1] = l1;
-  }
-  if (lane == 0) bad[cw] = failed ? 1 : 0;
-  if (failed && lane == 0) *abort_flag = 1;
-  named_bar_sync(1, kConsumerThreads);
-  const bool any_bad = (bad[0] | bad[1] | bad[2] | bad[3]) != 0;
-  float M0 = -INFINITY, M1 = -INFINITY;
+  uint8_t* scratch = smem + (kArea ? L::kMergeOff : L::kVOff + merge_stage * L::kTileBytes);
+  float4* buf = reinterpret_cast<float4*>(scratch);  // [slots][NQ][DT][32] float4
+  float* fin = reinterpret_cast<float*>(scratch);    // [16][kFin], after the tree
+  int* bad = reinterpret_cast<int*>(ml + W * kDecodeRows * 2);  // [warp]: its waits failed
+  if (g == 0) {
 #pragma unroll
-  for (int ww = 0; ww < kConsumerWarps; ++ww) {
-    M0 = fmaxf(M0, ml[(ww * 16 + g) * 2]);
-    M1 = fmaxf(M1, ml[(ww * 16 + g + 8) * 2]);
-  }
-  const float f0 = ex2(m0 - (M0 == -INFINITY ? 0.f : M0));
-  const float f1 = ex2(m1 - (M1 == -INFINITY ? 0.f : M1));
-#pragma unroll
-  for (int n = 0; n < NO && !any_bad; ++n) {
-    *reinterpret_cast<float2*>(mo + (cw * 16 + g) * D + n * 8 + 2 * t) = make_float2(o[n][0] * f0, o[n][1] * f0);
-    *reinterpret_cast<float2*>(mo + (cw * 16 + g + 8) * D + n * 8 + 2 * t) =
-        make_float2(o[n][2] * f1, o[n][3] * f1);
-  }
-  named_bar_sync(1, kConsumerThreads);
-  for (int idx = ctid; idx < R * D && !any_bad; idx += kConsumerThreads) {
-    const int row = idx / D, d = idx % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int ww = 0; ww < kConsumerWarps; ++ww) M = fmaxf(M, ml[(ww * 16 + row) * 2]);
-    const float Mu = M == -INFINITY ? 0.f : M;
-    float Lsum = 0.f, acc = 0.f;
-#pragma unroll
-    for (int ww = 0; ww < kConsumerWarps; ++ww) {
-      Lsum += ml[(ww * 16 + row) * 2 + 1] * ex2(ml[(ww * 16 + row) * 2] - Mu);
-      acc += mo[(ww * 16 + row) * D + d];
-    }
-    const float val = Lsum > 0.f ? acc / Lsum * vscale : 0.f;
-    const float lse2 = Lsum > 0.f ? Mu + __log2f(Lsum) : -INFINITY;
-    if (w.partial >= 0) {
-      p.partial_o[((int64_t)w.partial * kDecodeRows + row) * D + d] = val;
-      if (d == 0) p.partial_lse[w.partial * kDecodeRows + row] = lse2;
-    } else {
-      const int tok = w.q_row0 + row / p.G;
-      const int head = w.hk * p.G + row % p.G;
-      p.out[(int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head + d] = __float2bfloat16_rn(val);
-      if (d == 0 && p.lse != nullptr) p.lse[(int64_t)head * p.total_q + tok] = lse2 * kLn2;
-    }
-  }
-  named_bar_sync(1, kConsumerThreads);
-  // the borrowed V stage goes back to the producer (generic writes before the next async copy)
-  fence_proxy_async_smem();
-  __syncwarp();
-  if (lane == 0 && merge_stage >= 0) mbar_arrive(&B.empty_v[merge_stage]);
-  return !any_bad;
-}
-
-// ------------------------------------------------------------------ fp8-cache tiles (warp MMA, f16)
-// e4m3 K and V are converted to f16 straight into MMA fragments (exact).
-// K: a dot product over d does not depend on the order of d, so the k slots
-// of k-step ks = 4*G + u map to d = 64G + 16t + 4u + {0,1 | 2,3} for both Q and
-// K, and each thread reads its 16 bytes of a key row with one 128-bit load.
-// V: ldmatrix.trans on byte pairs gives a thread (key 2t, 2t+1) x (d 2g, 2g+1);
-// a byte permute splits that into the fragment of column d = 2g (even O tile)
-// and of d = 2g+1 (odd O tile); the epilogue puts O columns back in order.
-//
-// QF8 (q_scale given): Q is quantised to e4m3 and S = Q K^T runs as
-// m16n8k32 e4m3 MMAs straight on the cached K bytes (no K conversion).  The
-// same d permutation serves both operands: for k-step ks = 2G+h, thread t's
-// k slots 4t..4t+3 and 16+4t..16+4t+3 are dims 16(4G+t) + 8h + {0..3 | 4..7},
-// i.e. words 2h and 2h+1 of the 16-byte chunk 4G+t of a key row.
-template <int D, bool PF, int KPW, bool QF8>
-__device__ bool run_item_fp8(const AttnParams& p, const WorkItem& w, uint8_t* smem, const Bars& B,
-                             volatile int* abort_flag, Ring& rk, Ring& rv, float sl2, float vscale) {
-  using L = Layout<D, true, PF>;
-  constexpr int NT = KPW / 8;
-  constexpr int NO = D / 8;        // O column tiles
-  constexpr int RB = L::kRowBytes; // raw e4m3 row: D bytes (64-byte swizzle at D = 64)
-  const int lane = threadIdx.x & 31;
-  const int cw = (threadIdx.x >> 5) - 2;
-  const int ctid = threadIdx.x - 64;
-  const int g = lane >> 2, t = lane & 3;
-  const int row_blk = 0;    // a decode unit is at most 16 rows: one MMA row block
-  const int kw0 = cw * KPW;  // this warp's keys of each tile
-  const int R = w.n_q * p.G;
-  const int r0 = row_blk * 16 + g, r1 = r0 + 8;
-  auto limit_of = [&](int r) {
-    if (r >= R) return w.kv_begin;
-    int lim = w.kv_end;
-    if (p.causal) lim = min(lim, w.q_i0 + r / p.G + w.lk - w.lq + 1);
-    return lim;
-  };
-  const int lim0 = limit_of(r0), lim1 = limit_of(r1);
-
-  uint32_t qa[D / 16][4];  // f16 fragments (D/16 k-steps of 16), or e4m3 ones (QF8: D/32 k-steps of 32)
-  {
-    const __nv_bfloat16* q0 = nullptr;
-    const __nv_bfloat16* q1 = nullptr;
-    if (r0 < R)
-      q0 = p.q + (int64_t)(w.q_row0 + r0 / p.G) * p.q_stride_tok + (int64_t)(w.hk * p.G + r0 % p.G) * p.q_stride_head;
-    if (r1 < R)
-      q1 = p.q + (int64_t)(w.q_row0 + r1 / p.G) * p.q_stride_tok + (int64_t)(w.hk * p.G + r1 % p.G) * p.q_stride_head;
-    if constexpr (QF8) {
-      // the cache's encode: one IEEE reciprocal, an RN multiply per value, RN satfinite to e4m3
-      const float inv_q = __frcp_rn(__ldg(p.q_scale));
-      auto quant4 = [&](uint32_t w0, uint32_t w1) -> uint32_t {
-        auto lo = [](uint32_t v) { return __uint_as_float(v << 16); };
-        auto hi = [](uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); };
-        const uint32_t a = f32x2_to_e4m3x2(__fmul_rn(lo(w0), inv_q), __fmul_rn(hi(w0), inv_q));
-        const uint32_t b = f32x2_to_e4m3x2(__fmul_rn(lo(w1), inv_q), __fmul_rn(hi(w1), inv_q));
-        return a | (b << 16);
-      };
-#pragma unroll
-      for (int ks = 0; ks < D / 32; ++ks) {
-        const int d0 = 16 * (4 * (ks >> 1) + t) + 8 * (ks & 1);
-        const uint4 v0 = q0 ? __ldg(reinterpret_cast<const uint4*>(q0 + d0)) : make_uint4(0, 0, 0, 0);
-        const uint4 v1 = q1 ? __ldg(reinterpret_cast<const uint4*>(q1 + d0)) : make_uint4(0, 0, 0, 0);
-        qa[ks][0] = quant4(v0.x, v0.y);
-        qa[ks][1] = quant4(v1.x, v1.y);
-        qa[ks][2] = quant4(v0.z, v0.w);
-        qa[ks][3] = quant4(v1.z, v1.w);
-      }
-    } else {
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const int d0 = 64 * (ks >> 2) + 16 * t + 4 * (ks & 3);
-        qa[ks][0] = q0 ? bf16x2_to_f16x2(ld_u32(q0 + d0)) : 0u;
-        qa[ks][1] = q1 ? bf16x2_to_f16x2(ld_u32(q1 + d0)) : 0u;
-        qa[ks][2] = q0 ? bf16x2_to_f16x2(ld_u32(q0 + d0 + 2)) : 0u;
-        qa[ks][3] = q1 ? bf16x2_to_f16x2(ld_u32(q1 + d0 + 2)) : 0u;
-      }
-    }
-  }
-
-  float o[NO][4];
-#pragma unroll
-  for (int n = 0; n < NO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  int merge_stage = -1;
-  // A failed (timed-out or aborted) wait ends this warp's tiles, but the warp
-  // still passes every barrier of the merge below, so that no other consumer
-  // warp can be left waiting there.
-  bool failed = false;
-
-  for (int t0 = w.kv_begin; t0 < w.kv_end; t0 += kKvTile) {
-    if (!warp_wait(&B.full_k[rk.stage], rk.phase, abort_flag)) {
-      failed = true;
-      break;
-    }
-    const uint32_t kraw = smem_u32(smem + L::kKOff + rk.stage * L::kTileBytes);
-    float s[NT][4];
-#pragma unroll
-    for (int n = 0; n < NT; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int key = kw0 + nt * 8 + g;
-#pragma unroll
-      for (int G = 0; G < D / 64; ++G) {
-        const uint4 kv = lds_u128(kraw + raw_off<RB>(key, 4 * G + t));
-        const uint32_t wd[4] = {kv.x, kv.y, kv.z, kv.w};
-        if constexpr (QF8) {
-          mma_e4m3(s[nt], qa[2 * G][0], qa[2 * G][1], qa[2 * G][2], qa[2 * G][3], wd[0], wd[1]);
-          mma_e4m3(s[nt], qa[2 * G + 1][0], qa[2 * G + 1][1], qa[2 * G + 1][2], qa[2 * G + 1][3], wd[2], wd[3]);
-        } else {
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int ks = 4 * G + u;
-            mma_f16(s[nt], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], e4m3x2_to_f16x2(wd[u]),
-                    e4m3x2_to_f16x2(wd[u] >> 16));
-          }
-        }
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&B.empty_k[rk.stage]);
-
-    const int jb = t0 + kw0 + 2 * t;
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-    for (int n = 0; n < NT; ++n) {
+    for (int j = 0; j < NQ; ++j)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int j = jb + n * 8 + e;
-        s[n][e] = j < lim0 ? s[n][e] * sl2 : -INFINITY;
-        s[n][2 + e] = j < lim1 ? s[n][2 + e] * sl2 : -INFINITY;
-        mx0 = fmaxf(mx0, s[n][e]);
-        mx1 = fmaxf(mx1, s[n][2 + e]);
+        const int row = 8 * j + 2 * t + e;
+        ml[(cw * 16 + row) * 2 + 0] = m[j][e];
+        ml[(cw * 16 + row) * 2 + 1] = l[j][e];
       }
-    }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
-    const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float al0 = ex2(m0 - mu0), al1 = ex2(m1 - mu1);
-    m0 = mn0;
-    m1 = mn1;
-    float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      s[n][0] = ex2(s[n][0] - mu0);
-      s[n][1] = ex2(s[n][1] - mu0);
-      s[n][2] = ex2(s[n][2] - mu1);
-      s[n][3] = ex2(s[n][3] - mu1);
-      ls0 += s[n][0] + s[n][1];
-      ls1 += s[n][2] + s[n][3];
-    }
-    l0 = l0 * al0 + ls0;
-    l1 = l1 * al1 + ls1;
-#pragma unroll
-    for (int n = 0; n < NO; ++n) {
-      o[n][0] *= al0;
-      o[n][1] *= al0;
-      o[n][2] *= al1;
-      o[n][3] *= al1;
-    }
-
-    if (!warp_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) {
-      failed = true;
-      break;
-    }
-    const uint32_t vraw = smem_u32(smem + L::kVOff + rv.stage * L::kTileBytes);
-    const bool vmask = t0 + kKvTile > w.lk;  // rows past the sequence may hold anything: zero them
-#pragma unroll
-    for (int kk = 0; kk < KPW / 16; ++kk) {
-      const uint32_t a0 = pack_f16(s[2 * kk][0], s[2 * kk][1]);
-      const uint32_t a1 = pack_f16(s[2 * kk][2], s[2 * kk][3]);
-      const uint32_t a2 = pack_f16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-      const uint32_t a3 = pack_f16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-      const int kbase = t0 + kw0 + kk * 16 + 2 * t;
-      const uint32_t mlo0 = (kbase < w.lk ? 0x0000FFFFu : 0u) | (kbase + 1 < w.lk ? 0xFFFF0000u : 0u);
-      const uint32_t mlo1 = (kbase + 8 < w.lk ? 0x0000FFFFu : 0u) | (kbase + 9 < w.lk ? 0xFFFF0000u : 0u);
-      const int mi = lane >> 3;
-      const int key = kw0 + kk * 16 + (mi & 1) * 8 + (lane & 7);
-#pragma unroll
-      for (int db = 0; db < D / 32; ++db) {
-        const int chunk = 2 * db + (mi >> 1);
-        uint32_t v0, v1, v2, v3;
-        ldsm_x4_t(vraw + raw_off<RB>(key, chunk), v0, v1, v2, v3);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t va = h ? v2 : v0, vb = h ? v3 : v1;
-          uint32_t e0 = e4m3x2_to_f16x2(prmt(va, 0u, 0x0020u)), e1 = e4m3x2_to_f16x2(prmt(vb, 0u, 0x0020u));
-          uint32_t d0 = e4m3x2_to_f16x2(prmt(va, 0u, 0x0031u)), d1 = e4m3x2_to_f16x2(prmt(vb, 0u, 0x0031u));
-          if (vmask) {
-            e0 &= mlo0;
-            d0 &= mlo0;
-            e1 &= mlo1;
-            d1 &= mlo1;
-          }
-          mma_f16(o[4 * db + 2 * h], a0, a1, a2, a3, e0, e1);
-          mma_f16(o[4 * db + 2 * h + 1], a0, a1, a2, a3, d0, d1);
-        }
-      }
-    }
-    if (t0 + kKvTile >= w.kv_end) {
-      merge_stage = rv.stage;  // released after the merge below, which uses it as scratch
-    } else {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&B.empty_v[rv.stage]);
-    }
-    rk.advance<L::kStagesK>();
-    rv.advance<L::kStagesV>();
-  }
-
-  // epilogue.  O tile 4db+2h+par, column c holds d = 32db + 16h + 2c + par, so a
-  // thread's (even, odd) tile pair covers d = 32db + 16h + 4t + {0,1,2,3}.
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  if (num_tiles(w) == 0) {
-    // no key at all: every row is 0 with LSE -inf (a split-KV chunk that a
-    // dynamic plan's current length left empty gives such a partial)
-    for (int idx = ctid; idx < R * D; idx += kConsumerThreads) {
-      const int row = idx / D, dd = idx % D;
-      if (w.partial >= 0) {
-        p.partial_o[((int64_t)w.partial * kDecodeRows + row) * D + dd] = 0.f;
-        if (dd == 0) p.partial_lse[w.partial * kDecodeRows + row] = -INFINITY;
-        continue;
-      }
-      const int tok = w.q_row0 + row / p.G;
-      const int head = w.hk * p.G + row % p.G;
-      p.out[(int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head + dd] = __float2bfloat16_rn(0.f);
-      if (dd == 0 && p.lse != nullptr) p.lse[(int64_t)head * p.total_q + tok] = -INFINITY;
-    }
-    return true;
-  }
-  // Merge of the four warps' partial results in the borrowed V stage (D x
-  // 128 bytes): fragments are added in fragment order (all warps share the
-  // layout), warps 2,3 into 0,1, then warp 1 into warp 0, which writes the rows.
-  static_assert(2 * NO * 32 * 16 <= L::kTileBytes, "merge buffer fits one V stage");
-  float* ml = reinterpret_cast<float*>(smem + L::kMlOff);
-  float4* buf = reinterpret_cast<float4*>(smem + L::kVOff + merge_stage * L::kTileBytes);  // [2][NO][32] float4
-  int* bad = reinterpret_cast<int*>(ml + kConsumerWarps * kDecodeRows * 2);  // [warp]: its waits failed
-  if (t == 0) {
-    ml[(cw * 16 + g) * 2 + 0] = m0;
-    ml[(cw * 16 + g) * 2 + 1] = l0;
-    ml[(cw * 16 + g + 8) * 2 + 0] = m1;
-    ml[(cw * 16 + g + 8) * 2 + 1] = l1;
   }
   if (lane == 0) bad[cw] = failed ? 1 : 0;
   if (failed && lane == 0) *abort_flag = 1;
-  named_bar_sync(1, kConsumerThreads);
-  const bool any_bad = (bad[0] | bad[1] | bad[2] | bad[3]) != 0;
-  float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
-#pragma unroll
-  for (int ww = 0; ww < kConsumerWarps; ++ww) {
-    M0 = fmaxf(M0, ml[(ww * 16 + g) * 2]);
-    M1 = fmaxf(M1, ml[(ww * 16 + g + 8) * 2]);
-  }
-  const float Mu0 = M0 == -INFINITY ? 0.f : M0, Mu1 = M1 == -INFINITY ? 0.f : M1;
-#pragma unroll
-  for (int ww = 0; ww < kConsumerWarps; ++ww) {
-    L0 += ml[(ww * 16 + g) * 2 + 1] * ex2(ml[(ww * 16 + g) * 2] - Mu0);
-    L1 += ml[(ww * 16 + g + 8) * 2 + 1] * ex2(ml[(ww * 16 + g + 8) * 2] - Mu1);
-  }
-  const float f0 = ex2(m0 - Mu0), f1 = ex2(m1 - Mu1);
-#pragma unroll
-  for (int n = 0; n < NO; ++n) {
-    o[n][0] *= f0;
-    o[n][1] *= f0;
-    o[n][2] *= f1;
-    o[n][3] *= f1;
-  }
   auto put = [&](int slot) {
 #pragma unroll
-    for (int n = 0; n < NO; ++n) buf[(slot * NO + n) * 32 + lane] = make_float4(o[n][0], o[n][1], o[n][2], o[n][3]);
-  };
-  auto add = [&](int slot) {
+    for (int j = 0; j < NQ; ++j)
 #pragma unroll
-    for (int n = 0; n < NO; ++n) {
-      const float4 v = buf[(slot * NO + n) * 32 + lane];
-      o[n][0] += v.x;
-      o[n][1] += v.y;
-      o[n][2] += v.z;
-      o[n][3] += v.w;
-    }
+      for (int dt = 0; dt < DT; ++dt)
+        buf[(slot * NQ * DT + j * DT + dt) * 32 + lane] = make_float4(o[j][dt][0], o[j][dt][1], o[j][dt][2], o[j][dt][3]);
   };
-  if (!any_bad && cw >= 2) put(cw - 2);
-  named_bar_sync(1, kConsumerThreads);
-  if (!any_bad && cw < 2) add(cw);
-  named_bar_sync(1, kConsumerThreads);
-  if (!any_bad && cw == 1) put(0);
-  named_bar_sync(1, kConsumerThreads);
-  if (!any_bad && cw == 0) {
-    add(0);
-    // O tile 4db+2h+par, column c holds d = 32db + 16h + 2c + par: a thread's
-    // (even, odd) tile pair covers d = 32db + 16h + 4t + {0,1,2,3}
+  if constexpr (kFlat) {
+    if (!failed) put(cw);
+  }
+  named_bar_sync(1, kThreadsW);
+  bool any_bad = false;
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int row = half ? r1 : r0;
-      if (row >= R) continue;
-      const float Ls = half ? L1 : L0;
-      const float inv = Ls > 0.f ? vscale / Ls : 0.f;
-      const float lse2 = Ls > 0.f ? (half ? Mu1 : Mu0) + __log2f(Ls) : -INFINITY;
+  for (int ww = 0; ww < W; ++ww) any_bad |= bad[ww] != 0;
+  // row statistics over the W warps: the common max, the sum, and the log2 LSE
+  auto row_stats = [&](int row, float& mu, float& Lsum) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int ww = 0; ww < W; ++ww) M = fmaxf(M, ml[(ww * 16 + row) * 2]);
+    mu = M == -INFINITY ? 0.f : M;
+    Lsum = 0.f;
+#pragma unroll
+    for (int ww = 0; ww < W; ++ww) Lsum += ml[(ww * 16 + row) * 2 + 1] * ex2(ml[(ww * 16 + row) * 2] - mu);
+  };
+  auto write_lse = [&](int row, float mu, float Lsum) {
+    const float lse2 = Lsum > 0.f ? mu + __log2f(Lsum) : -INFINITY;
+    if (w.partial >= 0) {
+      p.partial_lse[w.partial * kDecodeRows + row] = lse2;
+    } else if (p.lse != nullptr) {
       const int tok = w.q_row0 + row / p.G;
       const int head = w.hk * p.G + row % p.G;
+      p.lse[(int64_t)head * p.total_q + tok] = lse2 * kLn2;
+    }
+  };
+  auto write_row8 = [&](int row, int d, const float* v) {
+    if (w.partial >= 0) {
+      float* dst = p.partial_o + ((int64_t)w.partial * kDecodeRows + row) * D + d;
+      *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+      *reinterpret_cast<float4*>(dst + 4) = make_float4(v[4], v[5], v[6], v[7]);
+    } else {
+      const int tok = w.q_row0 + row / p.G;
+      const int head = w.hk * p.G + row % p.G;
+      *reinterpret_cast<uint4*>(p.out + (int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head + d) =
+          make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
+    }
+  };
+  if constexpr (kFlat) {
+    // thread: row r, columns d .. d+7.  Row r = 2t + e of the fragments; column
+    // d of m-tile dt sits at (g, component) = bf16 V: (d % 8, e + 2 * (d % 16 >= 8)),
+    // fp8 V: ((d % 16) / 2, e + 2 * (d % 2))
+    for (int idx = ctid; idx < R * (D / 8) && !any_bad; idx += kThreadsW) {
+      const int row = idx / (D / 8), d0 = (idx % (D / 8)) * 8;
+      const int rt = row >> 1, re = row & 1, dt = d0 >> 4;
+      float mu, Lsum;
+      row_stats(row, mu, Lsum);
+      const float inv = Lsum > 0.f ? vscale / Lsum : 0.f;
+      float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int db = 0; db < D / 32; ++db)
+      for (int ww = 0; ww < W; ++ww) {
+        const float f = ex2(ml[(ww * 16 + row) * 2] - mu) * inv;
+        const float* sl = reinterpret_cast<const float*>(buf + (ww * DT + dt) * 32);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const float* e = o[4 * db + 2 * h];
-          const float* d = o[4 * db + 2 * h + 1];
-          const int col = 32 * db + 16 * h + 4 * t;
-          const float4 v = make_float4(e[2 * half] * inv, d[2 * half] * inv, e[2 * half + 1] * inv,
-                                       d[2 * half + 1] * inv);
-          if (w.partial >= 0) {
-            *reinterpret_cast<float4*>(p.partial_o + ((int64_t)w.partial * kDecodeRows + row) * D + col) = v;
-          } else {
-            uint2 pk2;
-            pk2.x = pack_bf16(v.x, v.y);
-            pk2.y = pack_bf16(v.z, v.w);
-            *reinterpret_cast<uint2*>(p.out + (int64_t)tok * p.o_stride_tok + (int64_t)head * p.o_stride_head + col) =
-                pk2;
-          }
+        for (int k = 0; k < 8; ++k) {
+          const int dd = (d0 & 15) + k;
+          const int gg = FP8 ? dd >> 1 : dd & 7;
+          const int cc = FP8 ? re + 2 * (dd & 1) : re + 2 * (dd >> 3);
+          v[k] += f * sl[(4 * gg + rt) * 4 + cc];
         }
-      if (t == 0) {
-        if (w.partial >= 0)
-          p.partial_lse[w.partial * kDecodeRows + row] = lse2;
-        else if (p.lse != nullptr)
-          p.lse[(int64_t)head * p.total_q + tok] = lse2 * kLn2;
       }
+      write_row8(row, d0, v);
+      if (d0 == 0) write_lse(row, mu, Lsum);
+    }
+  } else {
+    float Mu[NQ][2], Ls[NQ][2];
+#pragma unroll
+    for (int j = 0; j < NQ; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        row_stats(8 * j + 2 * t + e, Mu[j][e], Ls[j][e]);
+        const float f = ex2(m[j][e] - Mu[j][e]);
+#pragma unroll
+        for (int dt = 0; dt < DT; ++dt) {
+          o[j][dt][e] *= f;
+          o[j][dt][2 + e] *= f;
+        }
+      }
+    auto add = [&](int slot) {
+#pragma unroll
+      for (int j = 0; j < NQ; ++j)
+#pragma unroll
+        for (int dt = 0; dt < DT; ++dt) {
+          const float4 v = buf[(slot * NQ * DT + j * DT + dt) * 32 + lane];
+          o[j][dt][0] += v.x;
+          o[j][dt][1] += v.y;
+          o[j][dt][2] += v.z;
+          o[j][dt][3] += v.w;
+        }
+    };
+#pragma unroll
+    for (int half = W / 2; half >= 1; half >>= 1) {
+      if (!any_bad && cw >= half && cw < 2 * half) put(cw - half);
+      named_bar_sync(1, kThreadsW);
+      if (!any_bad && cw < half) add(cw);
+      if (half > 1) named_bar_sync(1, kThreadsW);
+    }
+    if (!any_bad && cw == 0) {
+      __syncwarp();  // every lane has read slot 0 before it is overwritten
+#pragma unroll
+      for (int j = 0; j < NQ; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int row = 8 * j + 2 * t + e;
+          const float inv = Ls[j][e] > 0.f ? vscale / Ls[j][e] : 0.f;
+#pragma unroll
+          for (int dt = 0; dt < DT; ++dt) {
+            // O^T rows g and g+8 of m-tile dt: d = 16dt + g, 16dt + 8 + g (bf16 V), or 16dt + 2g, 16dt + 2g + 1 (fp8 V)
+            const int da = FP8 ? 16 * dt + 2 * g : 16 * dt + g;
+            const int dc = FP8 ? da + 1 : da + 8;
+            fin[row * kFin + da] = o[j][dt][e] * inv;
+            fin[row * kFin + dc] = o[j][dt][2 + e] * inv;
+          }
+          if (g == 0 && row < R) write_lse(row, Mu[j][e], Ls[j][e]);
+        }
+    }
+    named_bar_sync(1, kThreadsW);
+    // every consumer thread writes 8 consecutive columns of a row at a time
+    for (int idx = ctid; idx < R * (D / 8) && !any_bad; idx += kThreadsW) {
+      const int row = idx / (D / 8), d = (idx % (D / 8)) * 8;
+      float v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = fin[row * kFin + d + k];
+      write_row8(row, d, v);
     }
   }
-  named_bar_sync(1, kConsumerThreads);
-  // the borrowed V stage goes back to the producer (generic writes before the next async copy)
-  fence_proxy_async_smem();
-  __syncwarp();
-  if (lane == 0 && merge_stage >= 0) mbar_arrive(&B.empty_v[merge_stage]);
+  named_bar_sync(1, kThreadsW);
+  if (merge_stage >= 0) {
+    // the borrowed V stage goes back to the producer (generic writes before the next async copy)
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&B.empty_v[merge_stage]);
+  }
   return !any_bad;
 }
 
@@ -1466,9 +1419,9 @@ __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
                          int it0, int it1) {
   using L = Layout<D, FP8, PF>;
   const int ctid = threadIdx.x - 64;
-  const bool mma_consumer = ctid < kConsumerThreads;  // warps 2..5
+  const bool mma_consumer = ctid < 32 * L::kDecWarps;  // the decode consumer warps
   if (blockIdx.x == 0 && mma_consumer) {
-    for (int b = ctid; b < p.batch; b += kConsumerThreads) {
+    for (int b = ctid; b < p.batch; b += 32 * L::kDecWarps) {
       const int lc = __ldg(p.cache_seqlens + b), planned = __ldg(p.plan_lc + b);
       if (p.dynamic ? (lc < 0 || lc > planned) : lc != planned) record_status(p.status, PKV_ERR_PLAN_MISMATCH, b, lc);
     }
@@ -1480,6 +1433,7 @@ __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
   const float sl2q = (FP8 && p.q_scale) ? sl2 * __ldg(p.q_scale) : sl2;
   Ring rk, rv;
   uint32_t pt = 0;
+  uint32_t dtc = 0;  // decode tiles seen (consumer groups take alternate ones)
   PendingEpi pend;
   for (int it = it0; it < it1; ++it) {
     const WorkItem w = load_item(p, it);
@@ -1491,11 +1445,11 @@ __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
     bool ok = true;
     if (w.kind == kDecode) {
       if (mma_consumer) {
-        if constexpr (FP8)
-          ok = run_item_fp8<D, PF, kKvTile / kConsumerWarps, QF8>(p, w, smem, B, abort_flag, rk, rv,
-                                                                   QF8 ? sl2q : sl2, vscale);
+        // one or two 8-column query tiles (decode units hold at most 16 rows)
+        if (w.n_q * p.G <= 8)
+          ok = run_decode<D, FP8, PF, QF8, 1>(p, w, smem, B, abort_flag, rk, rv, QF8 ? sl2q : sl2, vscale, dtc);
         else
-          ok = run_item<D, FP8, PF, kKvTile / kConsumerWarps>(p, w, smem, B, abort_flag, rk, rv, sl2, vscale);
+          ok = run_decode<D, FP8, PF, QF8, 2>(p, w, smem, B, abort_flag, rk, rv, QF8 ? sl2q : sl2, vscale, dtc);
       } else {
         rk.advance<L::kStagesK>(num_tiles(w));
         rv.advance<L::kStagesV>(num_tiles(w));
@@ -1619,7 +1573,7 @@ __global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
       return;
     }
   }
-  if (warp == 1 || (L::kTc && warp == L::kPvWarp)) {
+  if (L::kTc && (warp == 1 || warp == L::kPvWarp)) {
     if constexpr (L::kTc) {
       if (lane == 0) {
         const bool pv = warp == L::kPvWarp;
@@ -1638,11 +1592,13 @@ __global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
   } else {
     consumer<D, FP8, PF, QF8>(p, smem, B, abort_flag, tmem, it0, it1);
   }
-  // warps 1..5 and the P V warp: every tensor-memory access is done before warp 1 frees it
-  tc_fence_before();
-  named_bar_sync(2, 32 * (1 + L::kSoftmaxWarps + (L::kTc ? 1 : 0)));
-  tc_fence_after();
-  if (L::kTc && warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if constexpr (L::kTc) {
+    // warps 1..5 and the P V warp: every tensor-memory access is done before warp 1 frees it
+    tc_fence_before();
+    named_bar_sync(2, 32 * (2 + L::kSoftmaxWarps));
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  }
 }
 
 template <int D, bool FP8, bool PF, bool QF8 = false>
