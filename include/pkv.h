@@ -92,8 +92,16 @@ typedef struct {
   int64_t q_stride_tok, q_stride_head;
   void* out;                     /* (total_q, Hq, D) bf16, written                   */
   int64_t o_stride_tok, o_stride_head;
-  float* lse;                    /* nullable; (Hq, total_q) fp32 natural-log LSE     */
-  const int32_t* cu_seqlens_q;   /* [B+1] prefix sums of query lengths               */
+  float* lse;                    /* nullable; (Hq, q_rows) fp32 natural-log LSE      */
+  const int32_t* cu_seqlens_q;   /* [B+1] query row offsets: sequence b's Lq[b] query
+                                    (and output) rows start at row cu_seqlens_q[b],
+                                    Lq[b] being the plan's query length.  Packed rows
+                                    are the prefix sums of the lengths; any other
+                                    start offsets (gaps, any order: the non-contiguous
+                                    Q/O layout of the flashinfer PR "Uniform
+                                    PoDAttention API", Key Changes 1, q_indptr with
+                                    q_lenptr) are accepted, with q_rows giving the
+                                    rows of q / out / lse.  Read on the device.     */
   int32_t max_seqlen_q;          /* upper bound of the query lengths                 */
   const void* k_new;             /* nullable; (total_new, Hkv, D) bf16               */
   const void* v_new;             /* nullable iff k_new is                            */
@@ -123,6 +131,9 @@ typedef struct {
                                     Decode tiles use warp-level e4m3 MMAs, prefill
                                     tiles tcgen05 kind::f8f6f4 on the raw cache tile.
                                     A bf16 cache returns PKV_ERR_UNSUPPORTED.        */
+  int32_t q_rows;                /* rows of q, out and lse (>= every cu_seqlens_q[b] +
+                                    Lq[b]); 0: the plan's total query count (packed
+                                    rows).                                           */
 } pkv_fwd_args;
 
 typedef struct pkv_plan_s* pkv_plan_t;

@@ -52,7 +52,7 @@ class FwdArgs(ctypes.Structure):
                 ("kc_stride_tok", ctypes.c_int64), ("kc_stride_head", ctypes.c_int64),
                 ("cache_seqlens", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
                 ("block_table_stride", ctypes.c_int32), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
-                ("page_indptr", ctypes.c_void_p), ("q_scale", ctypes.c_void_p)]
+                ("page_indptr", ctypes.c_void_p), ("q_scale", ctypes.c_void_p), ("q_rows", ctypes.c_int32)]
 
 
 class WorkItemInfo(ctypes.Structure):
@@ -140,7 +140,7 @@ def make_problem(*, batch, num_heads_q, num_heads_kv, head_dim, page_size, cache
 
 def make_args(*, q, out, cu_seqlens_q, max_seqlen_q, k_cache, v_cache, cache_seqlens, lse=None, k_new=None,
               v_new=None, cu_seqlens_knew=None, block_table=None, k_scale=None, v_scale=None,
-              page_indptr=None, q_scale=None) -> FwdArgs:
+              page_indptr=None, q_scale=None, q_rows=0) -> FwdArgs:
     """Pointers and element strides of torch tensors laid out as in pkv.h."""
     a = FwdArgs()
     if q is not None:
@@ -163,6 +163,7 @@ def make_args(*, q, out, cu_seqlens_q, max_seqlen_q, k_cache, v_cache, cache_seq
     a.k_scale, a.v_scale = _ptr(k_scale), _ptr(v_scale)
     a.page_indptr = _ptr(page_indptr)
     a.q_scale = _ptr(q_scale)
+    a.q_rows = int(q_rows)
     return a
 
 

@@ -234,7 +234,10 @@ pkv_status validate_call(const pkv_problem* problem, const pkv_fwd_args* args, p
         (args->o_stride_head % 8) || (args->o_stride_tok % 8))
       return fail(PKV_ERR_INVALID_ARG, "q / out must be 16-byte aligned with strides multiple of 8 elements");
     if (args->max_seqlen_q < 0) return fail(PKV_ERR_INVALID_ARG, "max_seqlen_q < 0");
+    if (args->q_rows != 0 && args->q_rows < plan->total_q)
+      return fail(PKV_ERR_INVALID_ARG, "q_rows %d < the plan's %d query rows", args->q_rows, plan->total_q);
   }
+  if (args->q_rows < 0) return fail(PKV_ERR_INVALID_ARG, "q_rows < 0");
   const bool has_new = args->k_new != nullptr || args->v_new != nullptr;
   if (plan->total_new > 0 && !has_new)
     return fail(PKV_ERR_INVALID_ARG, "the plan appends %d tokens but k_new / v_new are NULL", plan->total_new);
@@ -279,7 +282,7 @@ extern "C" pkv_status pkv_attn_varlen_kvcache_fwd(const pkv_problem* problem, co
   if (st != PKV_OK) return st;
   memset(&tq, 0, sizeof(tq));
   if (plan->num_prefill_items > 0) {
-    st = make_q_map(&tq, pr, *args, plan->total_q);
+    st = make_q_map(&tq, pr, *args, args->q_rows ? args->q_rows : plan->total_q);
     if (st != PKV_OK) return st;
   }
 
@@ -293,7 +296,8 @@ extern "C" pkv_status pkv_attn_varlen_kvcache_fwd(const pkv_problem* problem, co
   p.out_v8 = (reinterpret_cast<uintptr_t>(args->out) % 32 == 0) && (args->o_stride_tok % 16 == 0) &&
              (args->o_stride_head % 16 == 0);
   p.lse = args->lse;
-  p.total_q = plan->total_q;
+  p.total_q = args->q_rows ? args->q_rows : plan->total_q;
+  p.cu_q = args->cu_seqlens_q;
   p.block_table = args->block_table;
   p.bt_stride = args->block_table_stride;
   p.page_indptr = args->page_indptr;
@@ -337,6 +341,7 @@ extern "C" pkv_status pkv_attn_varlen_kvcache_fwd(const pkv_problem* problem, co
   if (plan->num_combine > 0) {
     CombineParams cp{};
     cp.items = reinterpret_cast<const CombineItem*>(ws + plan->layout.combine);
+    cp.cu_q = p.cu_q;
     cp.partial_o = p.partial_o;
     cp.partial_lse = p.partial_lse;
     cp.out = p.out;

@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
       acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    const int tok = ci.q_row0 + row / ci.nh;
+    const int tok = __ldg(p.cu_q + ci.b) + row / ci.nh;
     const int head = ci.hk * p.G + ci.h0 + row % ci.nh;
     uint4 v;
     v.x = pack_bf16(acc[0] * inv, acc[1] * inv);

@@ -151,12 +151,15 @@ __device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16* p) {
   return __ldg(reinterpret_cast<const unsigned int*>(p));
 }
 
-// Work item `it` as this call runs it.  A dynamic plan was made for bounds on
+// Work item `it` as this call runs it.  Its query rows start at
+// cu_seqlens_q[b] + q_i0.  A dynamic plan was made for bounds on
 // the cache lengths: the sequence's current length (cache_seqlens, clamped to
 // its bound) cuts the item's key range.  Every role of the kernel reads items
 // through here, so they all see the same tiles.
 __device__ __forceinline__ WorkItem load_item(const AttnParams& p, int it) {
   WorkItem w = p.items[it];
+  // the sequence's query rows start where cu_seqlens_q says (packed or not)
+  w.q_row0 = __ldg(p.cu_q + w.b) + w.q_i0;
   if (p.dynamic) {
     const int bound = __ldg(p.plan_lc + w.b);
     const int lc = min(max(__ldg(p.cache_seqlens + w.b), 0), bound);

@@ -44,7 +44,8 @@ PKV_HOST_DEVICE inline int tc_group_heads(int G) { return G < kPrefillRowsTc ? G
 struct WorkItem {
   int32_t b;         // sequence
   int32_t hk;        // kv head
-  int32_t q_row0;    // packed-q index of the tile's first query token
+  int32_t q_row0;    // packed-q index of the tile's first query token (prefix sums of the plan's
+                     // lengths; the kernels use cu_seqlens_q[b] + q_i0, read on the device)
   int32_t q_i0;      // index of that token within its sequence
   int32_t n_q;       // query tokens in the tile
   int32_t lq;        // query length of the sequence
@@ -62,7 +63,7 @@ static_assert(sizeof(WorkItem) == 64, "WorkItem layout");
 // A unit split into KV chunks, merged by the combine kernel: chunk s wrote
 // rows [0, n_q * nh) starting at partial slot slot0 + s * slot_stride.
 struct CombineItem {
-  int32_t q_row0;
+  int32_t b;            // sequence (its query rows start at cu_seqlens_q[b]; split units hold all of them)
   int32_t n_q;
   int32_t hk;
   int32_t nsplit;

@@ -34,6 +34,7 @@ struct AppendParams {
 
 struct CombineParams {
   const CombineItem* items;
+  const int32_t* cu_q;     // query row offsets of the sequences
   const float* partial_o;
   const float* partial_lse;
   __nv_bfloat16* out;
@@ -50,7 +51,8 @@ struct AttnParams {
   int64_t o_stride_tok, o_stride_head;
   int32_t out_v8;      // every output row starts on 32 bytes: prefill rows are written 32 bytes per store
   float* lse;
-  int32_t total_q;
+  int32_t total_q;     // rows of q / out / lse
+  const int32_t* cu_q; // query row offsets of the sequences (read for every work item)
   const int32_t* block_table;
   int32_t bt_stride;
   const int32_t* page_indptr;  // nullable: ragged page list offsets

@@ -182,7 +182,7 @@ pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const 
           }
           if (nchunks > 1) {
             CombineItem ci{};
-            ci.q_row0 = (int32_t)q_row;
+            ci.b = b;
             ci.n_q = lq;
             ci.hk = hk;
             ci.nsplit = nchunks;

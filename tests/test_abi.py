@@ -228,6 +228,8 @@ def test_fwd_validation_before_any_launch(pkv):
     assert call(k_new=None, v_new=None, cu_seqlens_knew=None) == 1                  # plan expects new tokens
     assert call(q=_FakeTensor(1 << 20, (4, 4, 64), strides=[256, 66, 1])) == 1      # stride not 16 B multiple
     assert call(q_scale=i32) == 2      # quantised queries need an fp8 cache
+    assert call(q_rows=3) == 1         # fewer q / out rows than the plan's 4 query rows
+    assert call(q_rows=-1) == 1
     small = _FakeTensor(4096 * 256, (pl.workspace_bytes - 256,), esize=1)
     with pytest.raises(pkv.PkvError) as e:
         pkv.attn_varlen_kvcache_fwd(prob, pkv.make_args(**good), pl, small, stream=0)

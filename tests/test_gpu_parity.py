@@ -428,6 +428,67 @@ def test_ragged_page_list_equals_block_table():
     H.compare_lse(r.lse, ref["lse"])
 
 
+@pytest.mark.parametrize("hq,hkv,cache_dtype", [(16, 4, "bf16"), (32, 1, "bf16"), (16, 4, "fp8")])
+def test_non_contiguous_query_rows(hq, hkv, cache_dtype):
+    """Query / output rows placed anywhere (the non-contiguous Q/O layout:
+    row offsets per sequence in cu_seqlens_q, lengths from the plan, gaps and
+    any order) with a ragged page list holding spare pages (KV lengths from
+    cache_seqlens alone): decode units (split along the keys), a short query
+    run and prefill tiles match the oracle, and the rows in the gaps are never
+    written."""
+    import torch
+    spec = synth.Spec(batch=5, hq=hq, hkv=hkv, d=128, page_size=16, causal=True,
+                      softmax_scale=float(np.float32(1.0 / np.sqrt(128))), cache_dtype=cache_dtype,
+                      q_lens=np.array([1, 300, 1, 5, 140], np.int32), cache_lens=np.array([3000, 100, 700, 0, 33], np.int32),
+                      new_lens=np.array([1, 300, 1, 5, 140], np.int32), capacity=3008, name="gapped-q")
+    case = synth.make_case(spec, np.random.default_rng(800 + hq))
+    rng = np.random.default_rng(801)
+    order = rng.permutation(spec.batch)                 # sequences laid out in this order
+    gaps = rng.integers(1, 40, spec.batch)              # rows left free before each one
+    starts = np.zeros(spec.batch, np.int64)
+    row = 0
+    for b in order:
+        row += int(gaps[b])
+        starts[b] = row
+        row += int(spec.q_lens[b])
+    q_rows = row + 7
+    g = H.GpuCase(case, num_sms=24)
+    assert g.plan.stats()["num_split_units"] > 0
+    g.write_prefix()
+    cu = spec.cu_q
+    qbig = torch.full((q_rows, hq, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    for b in range(spec.batch):
+        qbig[starts[b]:starts[b] + spec.q_lens[b]] = g.q[cu[b]:cu[b + 1]]
+    obig = torch.full((q_rows, hq, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lbig = torch.full((hq, q_rows), float("nan"), dtype=torch.float32, device="cuda")
+    P = spec.page_size
+    width = case.block_table.shape[1]
+    counts = [min((int(n) + P - 1) // P + 1, width) for n in spec.kv_lens]   # a spare page where the row has one
+    flat = np.concatenate([case.block_table[b, :counts[b]] for b in range(spec.batch)])
+    indptr = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    assert flat.size == indptr[-1]
+    a = g.pkv.make_args(q=qbig, out=obig, lse=lbig, cu_seqlens_q=H.i32(np.append(starts, q_rows)),
+                        max_seqlen_q=int(spec.q_lens.max()), k_cache=g.k_cache, v_cache=g.v_cache,
+                        cache_seqlens=g.cache_lens, k_new=g.k_new, v_new=g.v_new, cu_seqlens_knew=g.cu_new,
+                        block_table=H.i32(flat), page_indptr=H.i32(indptr),
+                        k_scale=g.k_scale if cache_dtype == "fp8" else None,
+                        v_scale=g.v_scale if cache_dtype == "fp8" else None, q_rows=q_rows)
+    g.pkv.attn_varlen_kvcache_fwd(g.problem, a, g.plan, g.workspace)
+    assert g.status() == 0, g.pkv.last_error()
+    ref = oracle.forward(case)
+    used = np.zeros(q_rows, bool)
+    got = torch.empty_like(g.out)
+    got_lse = torch.empty((hq, spec.total_q), dtype=torch.float32, device="cuda")
+    for b in range(spec.batch):
+        used[starts[b]:starts[b] + spec.q_lens[b]] = True
+        got[cu[b]:cu[b + 1]] = obig[starts[b]:starts[b] + spec.q_lens[b]]
+        got_lse[:, cu[b]:cu[b + 1]] = lbig[:, starts[b]:starts[b] + spec.q_lens[b]]
+    H.compare_out(got, ref["out"], tol_for(case))
+    H.compare_lse(got_lse, ref["lse"])
+    free = torch.from_numpy(~used).cuda()
+    assert torch.isnan(obig[free].float()).all() and torch.isnan(lbig[:, free]).all(), "a gap row was written"
+
+
 @pytest.mark.parametrize("cache_dtype,P", [("bf16", 16), ("bf16", 1), ("fp8", 16), ("bf16", 64)])
 def test_ragged_page_list_prefill_against_oracle(cache_dtype, P):
     """Prefill-heavy batches (several 128-row query tiles per kv head, cached
