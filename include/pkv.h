@@ -75,7 +75,7 @@ typedef struct {
   int32_t batch;          /* number of sequences B                                   */
   int32_t num_heads_q;    /* Hq                                                      */
   int32_t num_heads_kv;   /* Hkv; Hq % Hkv == 0 (MQA: Hkv = 1)                       */
-  int32_t head_dim;       /* D: 64 or 128, either cache dtype                        */
+  int32_t head_dim;       /* D: 64, 128 or 256, either cache dtype                   */
   int32_t page_size;      /* 0 = contiguous cache; else 1, 2, 4 or a multiple of 8,
                              <= 256 (pages under 8 tokens are gathered row by row) */
   int32_t cache_capacity; /* tokens one sequence can hold: contiguous seqlen_cache,
@@ -95,13 +95,14 @@ typedef struct {
   float* lse;                    /* nullable; (Hq, q_rows) fp32 natural-log LSE      */
   const int32_t* cu_seqlens_q;   /* [B+1] query row offsets: sequence b's Lq[b] query
                                     (and output) rows start at row cu_seqlens_q[b],
-                                    Lq[b] being the plan's query length.  Packed rows
-                                    are the prefix sums of the lengths; any other
-                                    start offsets (gaps, any order: the non-contiguous
-                                    Q/O layout of the flashinfer PR "Uniform
-                                    PoDAttention API", Key Changes 1, q_indptr with
-                                    q_lenptr) are accepted, with q_rows giving the
-                                    rows of q / out / lse.  Read on the device.     */
+                                    Lq[b] being the plan's query length.  With q_rows
+                                    = 0 the rows are packed (the prefix sums of the
+                                    plan's lengths, which cu_seqlens_q must hold).
+                                    With q_rows > 0 any start offsets (gaps, any
+                                    order: the non-contiguous Q/O layout of the
+                                    flashinfer PR "Uniform PoDAttention API", Key
+                                    Changes 1, q_indptr with q_lenptr) are read on
+                                    the device.                                      */
   int32_t max_seqlen_q;          /* upper bound of the query lengths                 */
   const void* k_new;             /* nullable; (total_new, Hkv, D) bf16               */
   const void* v_new;             /* nullable iff k_new is                            */
@@ -131,9 +132,10 @@ typedef struct {
                                     Decode tiles use warp-level e4m3 MMAs, prefill
                                     tiles tcgen05 kind::f8f6f4 on the raw cache tile.
                                     A bf16 cache returns PKV_ERR_UNSUPPORTED.        */
-  int32_t q_rows;                /* rows of q, out and lse (>= every cu_seqlens_q[b] +
-                                    Lq[b]); 0: the plan's total query count (packed
-                                    rows).                                           */
+  int32_t q_rows;                /* 0: packed rows (the plan's total query count);
+                                    > 0: rows placed by cu_seqlens_q, and the row
+                                    count of q, out and lse (>= every cu_seqlens_q[b]
+                                    + Lq[b]).                                        */
 } pkv_fwd_args;
 
 typedef struct pkv_plan_s* pkv_plan_t;

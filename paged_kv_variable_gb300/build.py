@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libpkv.so")
-SOURCES = ["api.cu", "attn.cu", "append_combine.cu", "plan.cpp", "noalloc.cu"]
+SOURCES = ["api.cu", "attn.cu", "attn_d64.cu", "attn_d128.cu", "attn_d256.cu", "append_combine.cu", "plan.cpp", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

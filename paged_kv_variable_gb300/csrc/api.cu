@@ -77,7 +77,8 @@ pkv_status make_cache_map(CUtensorMap* map, const pkv_problem& pr, const pkv_fwd
   cuuint64_t dims[4] = {(cuuint64_t)pr.head_dim, (cuuint64_t)pr.num_heads_kv, rows, (cuuint64_t)pr.num_pages};
   cuuint64_t strides[3] = {(cuuint64_t)a.kc_stride_head * es, (cuuint64_t)a.kc_stride_tok * es,
                            (cuuint64_t)a.kc_stride_page * es};
-  cuuint32_t box[4] = {(cuuint32_t)(128 / es), 1, (cuuint32_t)cache_box_rows(pr.page_size, pr.cache_capacity), 1};
+  cuuint32_t box[4] = {(cuuint32_t)(128 / es), 1,
+                       (cuuint32_t)cache_box_rows(pr.page_size, pr.cache_capacity, kv_tile_keys(pr.head_dim)), 1};
   const bool narrow = pr.head_dim * es < 128;
   if (narrow) box[0] = (cuuint32_t)pr.head_dim;
   cuuint32_t estr[4] = {1, 1, 1, 1};
@@ -297,12 +298,13 @@ extern "C" pkv_status pkv_attn_varlen_kvcache_fwd(const pkv_problem* problem, co
              (args->o_stride_head % 16 == 0);
   p.lse = args->lse;
   p.total_q = args->q_rows ? args->q_rows : plan->total_q;
-  p.cu_q = args->cu_seqlens_q;
+  // rows placed by the caller (q_rows given): offsets read on the device
+  p.q_offsets = args->q_rows ? args->cu_seqlens_q : nullptr;
   p.block_table = args->block_table;
   p.bt_stride = args->block_table_stride;
   p.page_indptr = args->page_indptr;
   p.page_size = pr.page_size;
-  p.box_rows = cache_box_rows(pr.page_size, pr.cache_capacity);
+  p.box_rows = cache_box_rows(pr.page_size, pr.cache_capacity, kv_tile_keys(pr.head_dim));
   p.num_pages = pr.num_pages;
   p.G = pr.num_heads_q / pr.num_heads_kv;
   p.causal = pr.causal;
@@ -334,14 +336,15 @@ extern "C" pkv_status pkv_attn_varlen_kvcache_fwd(const pkv_problem* problem, co
   // across a profiling event, which must see the kernels in order.
   const bool overlap = plan->num_prefill_items == 0;
   e = launch_attention(p, tk, tv, tq, plan->num_ctas, pr.head_dim, pr.cache_dtype == PKV_FP8_E4M3,
-                       plan->num_prefill_items > 0, overlap && plan->total_new > 0 && !g_ev_start, s);
+                       plan->num_prefill_items > 0, plan->num_decode_items > 0,
+                       overlap && plan->total_new > 0 && !g_ev_start, s);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   if (g_ev_stop && (e = record_profile_event(g_ev_stop, s)) != cudaSuccess) return cuda_fail(e, "profile event");
 
   if (plan->num_combine > 0) {
     CombineParams cp{};
     cp.items = reinterpret_cast<const CombineItem*>(ws + plan->layout.combine);
-    cp.cu_q = p.cu_q;
+    cp.q_offsets = p.q_offsets;
     cp.partial_o = p.partial_o;
     cp.partial_lse = p.partial_lse;
     cp.out = p.out;

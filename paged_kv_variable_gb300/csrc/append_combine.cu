@@ -22,7 +22,7 @@ constexpr int kCombineThreads = 256;
 // One warp per (new token, kv head) row; lane l moves elements [l*E, l*E+E).
 template <int D, bool FP8>
 __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
-  constexpr int E = D / 32;  // elements per lane: 4 (D=128) or 2 (D=64)
+  constexpr int E = D / 32;  // elements per lane: 8 (D=256), 4 (D=128) or 2 (D=64)
   grid_dep_launch();         // the attention kernel may start; it waits before reading appended rows
   const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -62,7 +62,10 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
   if constexpr (!FP8) {
     __nv_bfloat16* kc = reinterpret_cast<__nv_bfloat16*>(p.k_cache) + dst;
     __nv_bfloat16* vc = reinterpret_cast<__nv_bfloat16*>(p.v_cache) + dst;
-    if constexpr (E == 4) {
+    if constexpr (E == 8) {
+      *reinterpret_cast<uint4*>(kc) = __ldg(reinterpret_cast<const uint4*>(kin));
+      *reinterpret_cast<uint4*>(vc) = __ldg(reinterpret_cast<const uint4*>(vin));
+    } else if constexpr (E == 4) {
       *reinterpret_cast<uint2*>(kc) = __ldg(reinterpret_cast<const uint2*>(kin));
       *reinterpret_cast<uint2*>(vc) = __ldg(reinterpret_cast<const uint2*>(vin));
     } else {
@@ -80,7 +83,14 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
     };
     uint8_t* kc = reinterpret_cast<uint8_t*>(p.k_cache) + dst;
     uint8_t* vc = reinterpret_cast<uint8_t*>(p.v_cache) + dst;
-    if constexpr (E == 4) {
+    if constexpr (E == 8) {
+      const uint4 kr = __ldg(reinterpret_cast<const uint4*>(kin));
+      const uint4 vr = __ldg(reinterpret_cast<const uint4*>(vin));
+      *reinterpret_cast<uint2*>(kc) = make_uint2(enc2(kr.x, inv_k) | (enc2(kr.y, inv_k) << 16),
+                                                 enc2(kr.z, inv_k) | (enc2(kr.w, inv_k) << 16));
+      *reinterpret_cast<uint2*>(vc) = make_uint2(enc2(vr.x, inv_v) | (enc2(vr.y, inv_v) << 16),
+                                                 enc2(vr.z, inv_v) | (enc2(vr.w, inv_v) << 16));
+    } else if constexpr (E == 4) {
       const uint2 kr = __ldg(reinterpret_cast<const uint2*>(kin));
       const uint2 vr = __ldg(reinterpret_cast<const uint2*>(vin));
       *reinterpret_cast<uint32_t*>(kc) = enc2(kr.x, inv_k) | (enc2(kr.y, inv_k) << 16);
@@ -124,7 +134,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
       acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    const int tok = __ldg(p.cu_q + ci.b) + row / ci.nh;
+    const int tok = (p.q_offsets != nullptr ? __ldg(p.q_offsets + ci.b) : ci.q_row0) + row / ci.nh;
     const int head = ci.hk * p.G + ci.h0 + row % ci.nh;
     uint4 v;
     v.x = pack_bf16(acc[0] * inv, acc[1] * inv);
@@ -143,10 +153,14 @@ cudaError_t launch_kv_append(const AppendParams& p, int head_dim, bool fp8, cuda
   const int threads = 256;
   const int64_t blocks = (rows * 32 + threads - 1) / threads;
   if (blocks > INT32_MAX) return cudaErrorInvalidValue;
-  if (fp8 && head_dim == 128) {
+  if (fp8 && head_dim == 256) {
+    kv_append_kernel<256, true><<<(unsigned)blocks, threads, 0, stream>>>(p);
+  } else if (fp8 && head_dim == 128) {
     kv_append_kernel<128, true><<<(unsigned)blocks, threads, 0, stream>>>(p);
   } else if (fp8) {
     kv_append_kernel<64, true><<<(unsigned)blocks, threads, 0, stream>>>(p);
+  } else if (head_dim == 256) {
+    kv_append_kernel<256, false><<<(unsigned)blocks, threads, 0, stream>>>(p);
   } else if (head_dim == 128) {
     kv_append_kernel<128, false><<<(unsigned)blocks, threads, 0, stream>>>(p);
   } else {
@@ -168,8 +182,9 @@ cudaError_t launch_combine(const CombineParams& p, int num_items, int head_dim, 
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = overlap_prev ? 1 : 0;
-  return head_dim == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<128>, p)
-                         : cudaLaunchKernelEx(&cfg, combine_kernel<64>, p);
+  return head_dim == 256   ? cudaLaunchKernelEx(&cfg, combine_kernel<256>, p)
+         : head_dim == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<128>, p)
+                           : cudaLaunchKernelEx(&cfg, combine_kernel<64>, p);
 }
 
 }  // namespace pkv

@@ -14,11 +14,17 @@ constexpr int kPrefillRowsTc = 128;  // rows of a prefill tile (tcgen05, one TME
 constexpr int kBoxRows = 8;         // smallest TMA box (cache rows, 1 KB at 128 B a row, so every box
                                     // starts on a 128-byte-swizzle atom); every page size is a multiple
 
+// Keys per K/V tile of the attention kernel: 128, or 64 at head_dim 256.
+inline int kv_tile_keys(int head_dim) { return head_dim == 256 ? 64 : kKvTile; }
+
+// Query rows a decode (warp-MMA) tile holds: 16, or 8 at head_dim 256.
+inline int decode_rows(int head_dim) { return head_dim == 256 ? 8 : kDecodeRows; }
+
 // Rows per TMA box for a cache: for a contiguous cache the largest power of
-// two (16..128) not above its capacity, else the largest power of two (16..128)
-// dividing the page size, so a box never crosses a page.
-inline int cache_box_rows(int page_size, int capacity) {
-  int r = 128;
+// two (8..tile) not above its capacity, else the largest power of two
+// (8..tile) dividing the page size, so a box never crosses a page or a tile.
+inline int cache_box_rows(int page_size, int capacity, int tile) {
+  int r = tile;
   if (page_size <= 0) {
     while (r > kBoxRows && r > capacity) r >>= 1;
   } else {
@@ -45,7 +51,7 @@ struct WorkItem {
   int32_t b;         // sequence
   int32_t hk;        // kv head
   int32_t q_row0;    // packed-q index of the tile's first query token (prefix sums of the plan's
-                     // lengths; the kernels use cu_seqlens_q[b] + q_i0, read on the device)
+                     // lengths; with rows placed by the caller, cu_seqlens_q[b] + q_i0 instead)
   int32_t q_i0;      // index of that token within its sequence
   int32_t n_q;       // query tokens in the tile
   int32_t lq;        // query length of the sequence
@@ -63,7 +69,8 @@ static_assert(sizeof(WorkItem) == 64, "WorkItem layout");
 // A unit split into KV chunks, merged by the combine kernel: chunk s wrote
 // rows [0, n_q * nh) starting at partial slot slot0 + s * slot_stride.
 struct CombineItem {
-  int32_t b;            // sequence (its query rows start at cu_seqlens_q[b]; split units hold all of them)
+  int32_t b;            // sequence
+  int32_t q_row0;       // its first query row when rows are packed (else cu_seqlens_q[b])
   int32_t n_q;
   int32_t hk;
   int32_t nsplit;
@@ -71,8 +78,9 @@ struct CombineItem {
   int32_t slot_stride;  // 16-row slots per chunk: ceil(n_q * nh / 16)
   int32_t h0;
   int32_t nh;
+  int32_t pad[3];
 };
-static_assert(sizeof(CombineItem) == 32, "CombineItem layout");
+static_assert(sizeof(CombineItem) == 48, "CombineItem layout");
 
 // Byte offsets of the sections of the caller's workspace.
 struct WorkspaceLayout {

@@ -34,7 +34,7 @@ struct AppendParams {
 
 struct CombineParams {
   const CombineItem* items;
-  const int32_t* cu_q;     // query row offsets of the sequences
+  const int32_t* q_offsets;  // nullable: query row offsets of the sequences (rows placed by the caller)
   const float* partial_o;
   const float* partial_lse;
   __nv_bfloat16* out;
@@ -52,7 +52,7 @@ struct AttnParams {
   int32_t out_v8;      // every output row starts on 32 bytes: prefill rows are written 32 bytes per store
   float* lse;
   int32_t total_q;     // rows of q / out / lse
-  const int32_t* cu_q; // query row offsets of the sequences (read for every work item)
+  const int32_t* q_offsets;  // nullable: query row offsets of the sequences (rows placed by the caller)
   const int32_t* block_table;
   int32_t bt_stride;
   const int32_t* page_indptr;  // nullable: ragged page list offsets
@@ -101,6 +101,6 @@ cudaError_t launch_combine(const CombineParams& p, int num_items, int head_dim, 
                            cudaStream_t stream);
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                              const CUtensorMap& tm_q, int num_ctas, int head_dim, bool fp8, bool has_prefill,
-                             bool overlap_prev, cudaStream_t stream);
+                             bool has_decode, bool overlap_prev, cudaStream_t stream);
 
 }  // namespace pkv

@@ -49,8 +49,8 @@ pkv_status validate_problem(const pkv_problem* p) {
   // any group size: groups of more than 128 heads are cut into head sub-groups
   if (p->cache_dtype != PKV_BF16 && p->cache_dtype != PKV_FP8_E4M3)
     return fail(PKV_ERR_INVALID_ARG, "cache_dtype %d unknown", p->cache_dtype);
-  if (p->head_dim != 64 && p->head_dim != 128)
-    return fail(PKV_ERR_UNSUPPORTED, "head_dim %d not in {64, 128}", p->head_dim);
+  if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 256)
+    return fail(PKV_ERR_UNSUPPORTED, "head_dim %d not in {64, 128, 256}", p->head_dim);
   if (p->page_size < 0 || p->page_size > 256 ||
       (p->page_size >= kBoxRows && p->page_size % kBoxRows != 0) ||
       (p->page_size > 0 && p->page_size < kBoxRows && (p->page_size & (p->page_size - 1)) != 0))
@@ -99,7 +99,8 @@ pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const 
   // tile) if its rows fit 16, else tensor-core tiles; units whose queries fit
   // one tile (decode steps of wide groups, short query runs) can be split
   // along the keys like decode units.
-  auto is_decode = [&](int lq) { return (int64_t)lq * G <= kDecodeRows; };
+  const int dec_rows = decode_rows(D);  // rows of a warp-MMA decode tile (8 at D = 256)
+  auto is_decode = [&](int lq) { return (int64_t)lq * G <= dec_rows; };
   auto splittable = [&](int lq) { return is_decode(lq) || lq <= tq_prefill; };
 
   int64_t total_q = 0, total_new = 0, total_split_keys = 0;
@@ -114,7 +115,7 @@ pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const 
     if (dynamic && lq > 0 && !splittable(lq))
       return fail(PKV_ERR_UNSUPPORTED,
                   "dynamic plans take requests whose queries fit one tile (sequence %d: %d query tokens > %d)", b, lq,
-                  std::max(tq_prefill, kDecodeRows / G));
+                  std::max(tq_prefill, dec_rows / G));
     if (lq > 0 && splittable(lq))
       total_split_keys += (int64_t)(lc + ln) * p.num_heads_kv * (is_decode(lq) ? 1 : n_sub);
   }
@@ -183,6 +184,7 @@ pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const 
           if (nchunks > 1) {
             CombineItem ci{};
             ci.b = b;
+            ci.q_row0 = (int32_t)q_row;
             ci.n_q = lq;
             ci.hk = hk;
             ci.nsplit = nchunks;

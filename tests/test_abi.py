@@ -48,6 +48,7 @@ def _problem(pkv, **kw):
 @pytest.mark.parametrize("kw,status", [
     (dict(num_heads_q=6, num_heads_kv=4), 1),
     (dict(head_dim=96), 2),
+    (dict(head_dim=512), 2),
     (dict(page_size=3), 2),
     (dict(page_size=12), 2),
     (dict(page_size=512), 2),

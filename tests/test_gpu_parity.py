@@ -77,6 +77,38 @@ def test_fp8_head_dim_64(P, q8):
     assert g.plan.stats()["num_split_units"] > 0
 
 
+@pytest.mark.parametrize("dtype,P,hq,hkv,q8", [("bf16", 16, 16, 4, False), ("bf16", 0, 16, 4, False),
+                                               ("bf16", 256, 32, 4, False), ("bf16", 1, 8, 1, False),
+                                               ("fp8", 16, 16, 4, False), ("fp8", 0, 32, 2, False),
+                                               ("fp8", 8, 16, 4, True), ("bf16", 16, 64, 2, False)])
+def test_head_dim_256(dtype, P, hq, hkv, q8):
+    """head_dim 256 (64-key tiles: three 64-column S buffers beside a
+    256-column O in tensor memory, 32 KB stages): a mixed batch of decode steps
+    (split along the keys), a short query run and prefills on cached prefixes,
+    GQA groups of 4 and 8 (decode tiles of at most 8 rows) and wider groups
+    (tensor-core tiles), bf16 and fp8 caches, with and without q_scale."""
+    import dataclasses
+    spec = synth.Spec(batch=5, hq=hq, hkv=hkv, d=256, page_size=P, causal=True,
+                      softmax_scale=float(np.float32(1.0 / np.sqrt(256))), cache_dtype=dtype,
+                      q_lens=np.array([1, 200, 1, 3, 90], np.int32), cache_lens=np.array([2500, 100, 600, 0, 41], np.int32),
+                      new_lens=np.array([1, 200, 1, 3, 90], np.int32), capacity=2560, name="d256")
+    case = synth.make_case(spec, np.random.default_rng(2560 + P + hq))
+    if q8:
+        amax = float(np.abs(synth.bf16_bits_to_f32(case.q)).max())
+        case = dataclasses.replace(case, q_scale=float(np.float32(amax / 448.0)))
+    g, _ = run_full(case, num_sms=24)
+    assert g.plan.stats()["num_split_units"] > 0
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_head_dim_256(seed):
+    """Random batches at head_dim 256 (both cache dtypes, causal or not, the
+    page sizes of the random cases)."""
+    case = H.gpu_random_case(2600 + seed, d=256, cache_dtype="fp8" if seed % 2 else "bf16",
+                             sentinel="nan" if seed % 3 == 0 else "finite")
+    run_full(case)
+
+
 @pytest.mark.parametrize("layout", ["head_pad", "base_offset"])
 @pytest.mark.parametrize("cache_dtype", ["bf16", "fp8"])
 def test_output_rows_not_32_byte_aligned(layout, cache_dtype):
