@@ -76,10 +76,18 @@ struct Layout {
   static constexpr bool kStageRegs = FP8 && !PF && D <= 128;
   static constexpr int kDecGroups = 1;
   static constexpr int kDecWarps = kConsumerWarps * kDecGroups;  // decode consumer warps
-  static constexpr int kVProducerWarp = PF ? 2 + kSoftmaxWarps : 1;
-  static constexpr int kConvWarp0 = 2 + kSoftmaxWarps + 1;
+  // fp8 cache with prefill tiles: the roles are grouped by warpgroup (0..3
+  // softmax, 4..7 converters, 8 K/Q producer, 9 S issuer, 10 V producer, 11
+  // P V issuer) so that setmaxnreg can move registers from the converters and
+  // the single-thread roles to the softmax warps
+  static constexpr bool kSplitRegs = FP8 && PF;
+  static constexpr int kCons0 = kSplitRegs ? 0 : 2;  // first consumer (softmax / decode) warp
+  static constexpr int kKProdWarp = kSplitRegs ? 8 : 0;
+  static constexpr int kSWarp = kSplitRegs ? 9 : 1;
+  static constexpr int kVProducerWarp = kSplitRegs ? 10 : (PF ? 2 + kSoftmaxWarps : 1);
+  static constexpr int kConvWarp0 = kSplitRegs ? 4 : 2 + kSoftmaxWarps + 1;
   static constexpr int kConvWarps = (FP8 && PF) ? 4 : 0;
-  static constexpr int kPvWarp = kConvWarp0 + kConvWarps;
+  static constexpr int kPvWarp = kSplitRegs ? 11 : kConvWarp0 + kConvWarps;
   static constexpr int kThreads = PF ? 32 * (3 + kSoftmaxWarps + kConvWarps + 1) : 32 * (2 + kDecWarps);
   static constexpr int kEsize = FP8 ? 1 : 2;
   // keys per K/V tile (one pipeline stage): 128, or 64 at D = 256 (stages of
@@ -754,7 +762,10 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
   using L = Layout<D, FP8, PF>;
   constexpr int kTile = L::kTile;
   constexpr uint32_t kTmemO = L::kTmemO;
-  constexpr int kPass = (FP8 ? 64 : 128) < kTile ? (FP8 ? 64 : 128) : kTile;  // S columns held in registers at a time
+  // S columns held in registers at a time (all of a tile's but in the fp8
+  // block without its register split)
+  constexpr int kPass = (FP8 && !L::kSplitRegs ? 64 : 128) < kTile ? (FP8 && !L::kSplitRegs ? 64 : 128) : kTile;
+  constexpr bool kTwoPass = kPass < kTile;  // S read twice (max, then probabilities)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qw = warp & 3;                   // TMEM lane quarter this warp may access
   const int r = qw * 32 + lane;              // tile row == TMEM lane
@@ -825,8 +836,8 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
     uint64_t sum2[2] = {0ull, 0ull};
 #pragma unroll
     for (int h = 0; h < kTile / kPass; ++h) {
-      if (FP8) {
-        // second pass: read this half of S again
+      if constexpr (kTwoPass) {
+        // second pass: read this part of S again
 #pragma unroll
         for (int c = 0; c < kPass / 32; ++c) tmem_ld32(t_lane + s_col + h * kPass + c * 32, s + c * 32);
         tmem_wait_ld();
@@ -881,9 +892,8 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
       }
     }
     // the previous item's O is written out before P V of this item's first tile
-    // may replace it (bf16 cache; with an fp8 cache the register budget of the
-    // larger block keeps the epilogue at the end of its own item)
-    if (!FP8 && j == 0 && pend.has) {
+    // may replace it
+    if (j == 0 && pend.has) {
       if (!epi_run<D, L::kTmemO>(p, B, pend, t_lane, abort_flag)) return false;
       pend.has = false;
     }
@@ -919,11 +929,6 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
     pend.lse = lse;
     pend.dst = valid ? dst : nullptr;
     pend.lse_dst = lse_dst;
-    if constexpr (FP8) {
-      if (!epi_run<D, L::kTmemO>(p, B, pend, t_lane, abort_flag)) return false;
-      tc_fence_before();
-      pend.has = false;
-    }
   } else {
     if (valid && part) {
 #pragma unroll
@@ -978,9 +983,9 @@ __device__ bool run_decode(const AttnParams& p, const WorkItem& w, uint8_t* smem
   constexpr int RB = L::kRowBytes;
   constexpr int kFin = D + 4;                    // row stride (floats) of the merged O in shared memory
   const int lane = threadIdx.x & 31;
-  const int cw = (threadIdx.x >> 5) - 2;         // 0 .. W-1
+  const int cw = (threadIdx.x >> 5) - L::kCons0;  // 0 .. W-1
   const int gi = cw / kConsumerWarps;            // consumer group: it runs the tiles with dtc % groups == gi
-  const int ctid = threadIdx.x - 64;
+  const int ctid = threadIdx.x - 32 * L::kCons0;
   const int g = lane >> 2, t = lane & 3;
   const int mi = lane >> 3;                      // ldmatrix: the 8x8 matrix this lane addresses
   const int kw0 = (cw % kConsumerWarps) * KPW;   // this warp's keys of each of its group's tiles
@@ -1473,7 +1478,7 @@ template <int D, bool FP8, bool PF, bool QF8, bool DEC>
 __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, volatile int* abort_flag, uint32_t tmem,
                          int it0, int it1) {
   using L = Layout<D, FP8, PF>;
-  const int ctid = threadIdx.x - 64;
+  const int ctid = threadIdx.x - 32 * L::kCons0;
   const bool mma_consumer = ctid < 32 * L::kDecWarps;  // the decode consumer warps
   if (blockIdx.x == 0 && mma_consumer) {
     for (int b = ctid; b < p.batch; b += 32 * L::kDecWarps) {
@@ -1526,7 +1531,7 @@ __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
       return false;
     }
   }
-  if constexpr (PF && !FP8) {
+  if constexpr (PF) {
     if (pend.has) {
       // the last prefill item's epilogue
       const int qw = (threadIdx.x >> 5) & 3;
@@ -1611,7 +1616,7 @@ __global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
     *abort_flag = 0;
     fence_mbarrier_init();
   }
-  if (L::kTc && warp == 1) {
+  if (L::kTc && warp == L::kSWarp) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -1621,7 +1626,53 @@ __global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
   const uint32_t tmem = L::kTc ? *tmem_slot : 0u;
   grid_dep_launch();  // the combine kernel may be scheduled; it waits for this grid to finish
   const int it0 = p.cta_begin[blockIdx.x], it1 = p.cta_begin[blockIdx.x + 1];
-  if (warp == 0) {
+  if constexpr (L::kSplitRegs) {
+    // 240 (softmax) + 152 (converters) + 112 (producers, issuers) registers a
+    // thread, one warpgroup each: exactly the 168 x 384 the block was launched
+    // with.  Each warpgroup runs one setmaxnreg at the head of its branch.
+    static_assert((240 + 152 + 112) * 128 == 168 * L::kThreads, "register split");
+    if (warp >= 8) {
+      reg_dealloc<112>();
+      if (warp == L::kKProdWarp) {
+        producer<D, FP8, PF, false>(p, &tm_k, &tm_q, smem, B, abort_flag, it0, it1);
+        return;
+      }
+      if (warp == L::kVProducerWarp) {
+        producer<D, FP8, PF, true>(p, &tm_v, &tm_q, smem, B, abort_flag, it0, it1);
+        return;
+      }
+      if (lane == 0) {
+        const bool pv = warp == L::kPvWarp;
+        if (!(pv ? pv_issuer<D, FP8, PF>(p, smem, B, abort_flag, tmem, it0, it1)
+                 : s_issuer<D, FP8, PF, QF8>(p, smem, B, abort_flag, tmem, it0, it1))) {
+          record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, pv ? -3 : -1);
+          *abort_flag = 1;
+          int zero = 0;
+          umma_commit(pv ? B.drain_pv : B.drain);
+          mbar_wait(pv ? B.drain_pv : B.drain, 0, &zero);
+        }
+      }
+      __syncwarp();
+    } else if (warp >= 4) {
+      reg_dealloc<152>();
+      if (!converter<D, PF, QF8>(p, smem, B, abort_flag, it0, it1)) {
+        if (lane == 0) record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, -2);
+        *abort_flag = 1;
+      }
+      return;
+    } else {
+      reg_alloc<240>();
+      consumer<D, FP8, PF, QF8, DEC>(p, smem, B, abort_flag, tmem, it0, it1);
+    }
+    // the S issuer, the consumers and the P V warp: every tensor-memory access
+    // is done before the S issuer's warp frees it
+    tc_fence_before();
+    named_bar_sync(2, 32 * (2 + L::kSoftmaxWarps));
+    tc_fence_after();
+    if (warp == L::kSWarp) tmem_dealloc(tmem, kTmemCols);
+    return;
+  }
+  if (warp == L::kKProdWarp) {
     producer<D, FP8, PF, false>(p, &tm_k, &tm_q, smem, B, abort_flag, it0, it1);
     return;
   }
@@ -1638,7 +1689,7 @@ __global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
       return;
     }
   }
-  if (L::kTc && (warp == 1 || warp == L::kPvWarp)) {
+  if (L::kTc && (warp == L::kSWarp || warp == L::kPvWarp)) {
     if constexpr (L::kTc) {
       if (lane == 0) {
         const bool pv = warp == L::kPvWarp;
@@ -1658,11 +1709,12 @@ __global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
     consumer<D, FP8, PF, QF8, DEC>(p, smem, B, abort_flag, tmem, it0, it1);
   }
   if constexpr (L::kTc) {
-    // warps 1..5 and the P V warp: every tensor-memory access is done before warp 1 frees it
+    // the S issuer, the consumers and the P V warp: every tensor-memory access
+    // is done before the S issuer's warp frees it
     tc_fence_before();
     named_bar_sync(2, 32 * (2 + L::kSoftmaxWarps));
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    if (warp == L::kSWarp) tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -1681,6 +1733,15 @@ cudaError_t launch_t(const AttnParams& p, const CUtensorMap& tk, const CUtensorM
     e = cudaFuncSetAttribute(attn_kernel<D, FP8, PF, QF8, DEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::kAlloc);
     if (e != cudaSuccess) return e;
+    if constexpr (L::kSplitRegs) {
+      // the register split adds up to exactly 168 registers a thread at launch:
+      // a build with any other count could leave the softmax warpgroup's
+      // increase waiting, so it is refused before it runs
+      cudaFuncAttributes fa{};
+      e = cudaFuncGetAttributes(&fa, attn_kernel<D, FP8, PF, QF8, DEC>);
+      if (e != cudaSuccess) return e;
+      if (fa.numRegs != 168) return cudaErrorInvalidConfiguration;
+    }
     configured.fetch_or(bit);
   }
   cudaLaunchAttribute attr[1];
