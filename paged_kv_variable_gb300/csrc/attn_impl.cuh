@@ -549,21 +549,35 @@ __device__ bool pv_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, vol
 // exactly (every e4m3 value is an f16 value), zeroing V rows past the
 // sequence; and the bf16 Q tile of each item into f16 in place.  Converted
 // tiles are double-buffered (T % 2); raw stages are released after conversion.
+//
+// Unit u of the 16-byte raw chunks (ct + 128 k) maps to row (u % 8) + 8 m and
+// chunk column (u / 8) % kCpr, m = u / (8 kCpr): the eight threads of a
+// quarter-warp (which one 16-byte shared access serves at a time) take eight
+// consecutive rows at one column, so under either swizzle (chunk XOR row % 8,
+// or the 64-byte one) their loads and each of their two stores fall on eight
+// distinct 16-byte bank groups.  (Eight chunks of one row would put chunks
+// 2c and 2c + 8 of the f16 row on the same group.)
+template <int kCpr>
+__device__ __forceinline__ void conv_unit(int u, int& r, int& c) {
+  c = (u >> 3) % kCpr;
+  r = (u & 7) + 8 * ((u >> 3) / kCpr);
+}
+
 template <int D, int TILE>
 __device__ __forceinline__ void convert_tile(const uint8_t* raw, uint8_t* conv, int ct, int zero_from) {
   constexpr int kCpr = D / 16;       // raw 16-byte chunks per row (e4m3 rows of D bytes)
   constexpr int RB = D < 128 ? D : 128;
 #pragma unroll
   for (int k = 0; k < TILE * kCpr / 128; ++k) {
-    const int u = ct + 128 * k;
-    const int r = u / kCpr, c = u % kCpr;  // raw 16-byte chunk c of row r: d = 16c .. 16c+15
+    int r, c;  // raw 16-byte chunk c of row r: d = 16c .. 16c+15
+    conv_unit<kCpr>(ct + 128 * k, r, c);
     uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
     if (r < zero_from) {
       const uint4 w = *reinterpret_cast<const uint4*>(raw + raw_off<RB, TILE>(r, c));
-      lo = make_uint4(e4m3x2_to_f16x2(w.x), e4m3x2_to_f16x2(w.x >> 16), e4m3x2_to_f16x2(w.y),
-                      e4m3x2_to_f16x2(w.y >> 16));
-      hi = make_uint4(e4m3x2_to_f16x2(w.z), e4m3x2_to_f16x2(w.z >> 16), e4m3x2_to_f16x2(w.w),
-                      e4m3x2_to_f16x2(w.w >> 16));
+      e4m3x4_to_f16x4(w.x, lo.x, lo.y);
+      e4m3x4_to_f16x4(w.y, lo.z, lo.w);
+      e4m3x4_to_f16x4(w.z, hi.x, hi.y);
+      e4m3x4_to_f16x4(w.w, hi.z, hi.w);
     }
     *reinterpret_cast<uint4*>(conv + tile_off<TILE>(r, 2 * c)) = lo;
     *reinterpret_cast<uint4*>(conv + tile_off<TILE>(r, 2 * c + 1)) = hi;
@@ -606,8 +620,8 @@ __device__ bool converter(const AttnParams& p, uint8_t* smem, const Bars& B, vol
       constexpr int kCpr = D / 16;  // e4m3 16-byte chunks per row
 #pragma unroll 2
       for (int k = 0; k < kCpr; ++k) {
-        const int u = ct + 128 * k;
-        const int r = u / kCpr, c = u % kCpr;
+        int r, c;
+        conv_unit<kCpr>(ct + 128 * k, r, c);
         const uint4 a = *reinterpret_cast<const uint4*>(qb + tile_off<kPrefillRowsTc>(r, 2 * c));
         const uint4 b = *reinterpret_cast<const uint4*>(qb + tile_off<kPrefillRowsTc>(r, 2 * c + 1));
         *reinterpret_cast<uint4*>(q8 + raw_off<L::kRowBytes, kPrefillRowsTc>(r, c)) =

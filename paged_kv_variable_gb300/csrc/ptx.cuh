@@ -287,6 +287,14 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
   return h2;
 }
 
+// four e4m3 codes -> two f16x2 (bytes 0, 1 -> lo; bytes 2, 3 -> hi), the word
+// split into its 16-bit halves once
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t v, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(v));
+}
+
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
