@@ -780,6 +780,11 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
   // block without its register split)
   constexpr int kPass = (FP8 && !L::kSplitRegs ? 64 : 128) < kTile ? (FP8 && !L::kSplitRegs ? 64 : 128) : kTile;
   constexpr bool kTwoPass = kPass < kTile;  // S read twice (max, then probabilities)
+  // fp8 cache: both passes walk the tile 32 columns at a time in loops that
+  // are not unrolled, reading S from tensor memory twice; the warps then
+  // share their SM sub-partitions with the converters' code in a small
+  // instruction footprint
+  constexpr bool kRolled = FP8 && L::kSplitRegs;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qw = warp & 3;                   // TMEM lane quarter this warp may access
   const int r = qw * 32 + lane;              // tile row == TMEM lane
@@ -805,14 +810,30 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
     if (!warp_wait(&B.s_full[sb], (T / kSBufs) & 1, abort_flag)) return false;
     tc_fence_after();
     const bool need_mask = __any_sync(0xffffffffu, t0 + kTile > lim);
-    uint32_t s[kPass];
+    uint32_t s[kPass];  // (unused when rolled)
 
     // row max as a tree, masked by select (rows past the sequence see nothing)
     float mx8[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+    if constexpr (kRolled) {
+#pragma unroll 1
+      for (int h = 0; h < kTile / 32; ++h) {
+        uint32_t c32[32];
+        tmem_ld32(t_lane + s_col + h * 32, c32);
+        tmem_wait_ld();
+        if (need_mask) {
 #pragma unroll
-    for (int h = 0; h < kTile / kPass; ++h) {
+          for (int c = 0; c < 32; ++c)
+            if (t0 + h * 32 + c >= lim) c32[c] = __float_as_uint(-INFINITY);
+        }
+#pragma unroll
+        for (int c = 0; c < 32; c += 2)
+          mx8[(c >> 1) & 7] = fmax3(mx8[(c >> 1) & 7], __uint_as_float(c32[c]), __uint_as_float(c32[c + 1]));
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < (kRolled ? 0 : kTile / kPass); ++h) {
 #pragma unroll
       for (int c = 0; c < kPass / 32; ++c) tmem_ld32(t_lane + s_col + h * kPass + c * 32, s + c * 32);
       tmem_wait_ld();
@@ -848,8 +869,34 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
     // packed add into the row sum
     const uint64_t sl2x2 = f32x2(sl2, sl2), nmu2 = f32x2(-mu, -mu);
     uint64_t sum2[2] = {0ull, 0ull};
+    if constexpr (kRolled) {
+      // P of columns 32h .. 32h+31 goes to packed columns 16h .. 16h+15, whose
+      // S has been read already
+#pragma unroll 1
+      for (int h = 0; h < kTile / 32; ++h) {
+        uint32_t c32[32];
+        tmem_ld32(t_lane + s_col + h * 32, c32);
+        tmem_wait_ld();
+        if (need_mask) {
 #pragma unroll
-    for (int h = 0; h < kTile / kPass; ++h) {
+          for (int c = 0; c < 32; ++c)
+            if (t0 + h * 32 + c >= lim) c32[c] = __float_as_uint(-INFINITY);
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          float y0, y1;
+          f32x2_split(fma_f32x2(f32x2(__uint_as_float(c32[2 * c]), __uint_as_float(c32[2 * c + 1])), sl2x2, nmu2), y0,
+                      y1);
+          const float p0 = ex2(y0), p1 = ex2(y1);
+          sum2[c & 1] = add_f32x2(sum2[c & 1], f32x2(p0, p1));
+          pk[c] = pack_f16(p0, p1);
+        }
+        tmem_st16(t_lane + s_col + h * 16, pk);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < (kRolled ? 0 : kTile / kPass); ++h) {
       if constexpr (kTwoPass) {
         // second pass: read this part of S again
 #pragma unroll
