@@ -571,14 +571,16 @@ __device__ __forceinline__ void convert_tile(const uint8_t* raw, uint8_t* conv, 
   for (int k = 0; k < TILE * kCpr / 128; ++k) {
     int r, c;  // raw 16-byte chunk c of row r: d = 16c .. 16c+15
     conv_unit<kCpr>(ct + 128 * k, r, c);
-    uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-    if (r < zero_from) {
-      const uint4 w = *reinterpret_cast<const uint4*>(raw + raw_off<RB, TILE>(r, c));
-      e4m3x4_to_f16x4(w.x, lo.x, lo.y);
-      e4m3x4_to_f16x4(w.y, lo.z, lo.w);
-      e4m3x4_to_f16x4(w.z, hi.x, hi.y);
-      e4m3x4_to_f16x4(w.w, hi.z, hi.w);
-    }
+    // every row is read and converted (the loads are not behind a branch, so
+    // they can all be in flight at once); rows at or past zero_from then
+    // become zeros by select
+    uint4 lo, hi;
+    const uint4 w = *reinterpret_cast<const uint4*>(raw + raw_off<RB, TILE>(r, c));
+    e4m3x4_to_f16x4(w.x, lo.x, lo.y);
+    e4m3x4_to_f16x4(w.y, lo.z, lo.w);
+    e4m3x4_to_f16x4(w.z, hi.x, hi.y);
+    e4m3x4_to_f16x4(w.w, hi.z, hi.w);
+    if (r >= zero_from) lo = hi = make_uint4(0, 0, 0, 0);
     *reinterpret_cast<uint4*>(conv + tile_off<TILE>(r, 2 * c)) = lo;
     *reinterpret_cast<uint4*>(conv + tile_off<TILE>(r, 2 * c + 1)) = hi;
   }
@@ -780,10 +782,12 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
   // block without its register split)
   constexpr int kPass = (FP8 && !L::kSplitRegs ? 64 : 128) < kTile ? (FP8 && !L::kSplitRegs ? 64 : 128) : kTile;
   constexpr bool kTwoPass = kPass < kTile;  // S read twice (max, then probabilities)
-  // fp8 cache: both passes walk the tile 32 columns at a time in loops that
-  // are not unrolled, reading S from tensor memory twice; the warps then
-  // share their SM sub-partitions with the converters' code in a small
-  // instruction footprint
+  // fp8 cache: S is read from tensor memory twice, the max pass at once (or,
+  // on tiles that need the mask, 32 columns at a time) and the probability
+  // pass 32 columns at a time in a loop that is not unrolled: the warps share
+  // their SM sub-partitions with the converters, and the smaller instruction
+  // footprint measured faster than the unrolled one-pass form (and than
+  // 64-column steps, or a second register buffer loading ahead)
   constexpr bool kRolled = FP8 && L::kSplitRegs;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qw = warp & 3;                   // TMEM lane quarter this warp may access
@@ -817,19 +821,28 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
 #pragma unroll
     for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
     if constexpr (kRolled) {
-#pragma unroll 1
-      for (int h = 0; h < kTile / 32; ++h) {
-        uint32_t c32[32];
-        tmem_ld32(t_lane + s_col + h * 32, c32);
+      if (!need_mask) {
+        // the whole tile at once: every load in flight, one wait
+        uint32_t st[kTile];
+#pragma unroll
+        for (int c = 0; c < kTile / 32; ++c) tmem_ld32(t_lane + s_col + c * 32, st + c * 32);
         tmem_wait_ld();
-        if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < kTile; c += 2)
+          mx8[(c >> 1) & 7] = fmax3(mx8[(c >> 1) & 7], __uint_as_float(st[c]), __uint_as_float(st[c + 1]));
+      } else {
+#pragma unroll 1
+        for (int h = 0; h < kTile / 32; ++h) {
+          uint32_t c32[32];
+          tmem_ld32(t_lane + s_col + h * 32, c32);
+          tmem_wait_ld();
 #pragma unroll
           for (int c = 0; c < 32; ++c)
             if (t0 + h * 32 + c >= lim) c32[c] = __float_as_uint(-INFINITY);
-        }
 #pragma unroll
-        for (int c = 0; c < 32; c += 2)
-          mx8[(c >> 1) & 7] = fmax3(mx8[(c >> 1) & 7], __uint_as_float(c32[c]), __uint_as_float(c32[c + 1]));
+          for (int c = 0; c < 32; c += 2)
+            mx8[(c >> 1) & 7] = fmax3(mx8[(c >> 1) & 7], __uint_as_float(c32[c]), __uint_as_float(c32[c + 1]));
+        }
       }
     }
 #pragma unroll
