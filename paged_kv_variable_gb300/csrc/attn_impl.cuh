@@ -787,7 +787,8 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
   // pass 32 columns at a time in a loop that is not unrolled: the warps share
   // their SM sub-partitions with the converters, and the smaller instruction
   // footprint measured faster than the unrolled one-pass form (and than
-  // 64-column steps, or a second register buffer loading ahead)
+  // 64-column steps, or a second register buffer loading ahead); the bf16
+  // tile, without the converters, measured faster unrolled
   constexpr bool kRolled = FP8 && L::kSplitRegs;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qw = warp & 3;                   // TMEM lane quarter this warp may access
@@ -1206,8 +1207,9 @@ __device__ bool run_decode(const AttnParams& p, const WorkItem& w, uint8_t* smem
           } else {
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              const uint32_t a0 = e4m3x2_to_f16x2(wa[u]), a1 = e4m3x2_to_f16x2(wc[u]);
-              const uint32_t a2 = e4m3x2_to_f16x2(wa[u] >> 16), a3 = e4m3x2_to_f16x2(wc[u] >> 16);
+              uint32_t a0, a1, a2, a3;
+              e4m3x4_to_f16x4(wa[u], a0, a2);
+              e4m3x4_to_f16x4(wc[u], a1, a3);
 #pragma unroll
               for (int j = 0; j < NQ; ++j) mma_f16(s[j][i], a0, a1, a2, a3, qb[j][4 * c + u][0], qb[j][4 * c + u][1]);
             }
@@ -1305,10 +1307,10 @@ __device__ bool run_decode(const AttnParams& p, const WorkItem& w, uint8_t* smem
           }
 #pragma unroll
           for (int h = 0; h < 2; ++h) {  // chunk 2cp + h: O^T m-tile 2cp + h
-            uint32_t a0 = e4m3x2_to_f16x2(prmt(v[2 * h], 0u, 0x0020u));
-            uint32_t a1 = e4m3x2_to_f16x2(prmt(v[2 * h], 0u, 0x0031u));
-            uint32_t a2 = e4m3x2_to_f16x2(prmt(v[2 * h + 1], 0u, 0x0020u));
-            uint32_t a3 = e4m3x2_to_f16x2(prmt(v[2 * h + 1], 0u, 0x0031u));
+            // bytes (0, 2) and (1, 3) of each word: one permute, then its halves
+            uint32_t a0, a1, a2, a3;
+            e4m3x4_to_f16x4(prmt(v[2 * h], 0u, 0x3120u), a0, a1);
+            e4m3x4_to_f16x4(prmt(v[2 * h + 1], 0u, 0x3120u), a2, a3);
             if (vmask) {
               a0 &= mlo;
               a1 &= mlo;
