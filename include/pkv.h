@@ -262,8 +262,7 @@ pkv_status pkv_attn_varlen_kvcache_fwd(const pkv_problem* problem, const pkv_fwd
  * exits; the entry point allocates nothing and frees nothing.  It uploads the
  * plan into that array and then runs the call on `stream`.
  *  - The first call on a device resolves the array's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *    (cudaGetSymbolAddress, checked) with that device current, once.
  *  - A plan needing more than 32 MiB of workspace is rejected with
  *    PKV_ERR_WORKSPACE_TOO_SMALL before anything is launched.
  *  - Every host-side check (problem, plan, cache, q / out, new tokens, size)
