@@ -50,24 +50,36 @@ namespace {
 constexpr int kConsumerWarps = 4;                  // warp-MMA consumers (decode, fp8 prefill): warps 2..5
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr float kLn2 = 0.693147180559945309f;
-// Tensor memory: three S buffers of one tile's keys each (fp32), then O (D fp32
-// columns): [0,128), [128,256), [256,384), O [384, 384+D) with 128-key tiles;
-// [0,64), [64,128), [128,192), O [192, 448) with the 64-key tiles of D = 256.
-// P of a tile (bf16 or f16 pairs: a tile's keys in half as many columns)
-// overwrites the first columns of its own S buffer once the softmax has read
-// S, so a buffer is free again when P V of its tile has completed.
+// Tensor memory: at D <= 128 (two query tiles per prefill item) query tile q
+// has one S buffer of a tile's keys (fp32) at 256q and its O (D fp32 columns)
+// at 256q + 128; at D = 256 three S buffers [0,64), [64,128), [128,192) of the
+// 64-key tiles, then O [192, 448).  P of a tile (bf16 or f16 pairs: a tile's
+// keys in half as many columns) overwrites the first columns of its own S
+// buffer once the softmax has read S, so a buffer is free again when P V of
+// its tile has completed.
 constexpr uint32_t kTmemCols = 512;
-constexpr int kSBufs = 3;             // S of tile T+3 waits only for P V of tile T
+constexpr int kSBufsMax = 3;          // S buffers (barrier slots); S of tile T+kSBufs waits only for P V of tile T
 
 template <int D, bool FP8, bool PF>
 struct Layout {
-  // Warp roles with prefill tiles (tcgen05): 0 K/Q producer, 1 S = Q K^T
-  // issuer, 2..5 consumers (softmax of prefill tiles, warp-MMA decode tiles),
-  // 6 V producer, for an fp8 cache 7..10 converters (e4m3 K/V tiles and the
-  // bf16 Q tile to f16 MMA operands), and a last warp issuing O += P V.
+  // Warp roles with prefill tiles (tcgen05) at D = 256 over a bf16 cache: 0
+  // K/Q producer, 1 S = Q K^T issuer, 2..5 consumers (softmax of prefill
+  // tiles, warp-MMA decode tiles), 6 V producer, 7 O += P V issuer.
   // Decode-only plans: 0 K producer, 1 V producer, 2.. decode consumers.
+  // Otherwise (prefill tiles at D <= 128, or an fp8 cache) the roles are
+  // grouped by warpgroup so that setmaxnreg can move registers between them:
+  // softmax warps first (one warpgroup per query tile of an item), then the
+  // four converters of an fp8 cache (e4m3 K/V tiles and the bf16 Q tiles to
+  // f16 MMA operands), then K/Q producer, S issuer, V producer, P V issuer.
+  static constexpr int kD = D;
   static constexpr bool kTc = PF;                           // prefill tiles (on tcgen05) in the plan
-  static constexpr int kSoftmaxWarps = kConsumerWarps;      // one per TMEM lane quarter
+  // query tiles of a prefill item: two over an fp8 cache at D <= 128, sharing
+  // every K/V tile (each with one S buffer and its O in tensor memory, and a
+  // softmax warpgroup of its own: the two tiles' MMAs run while the other's
+  // softmax does, and each converted K/V tile serves both); one otherwise
+  static constexpr int kQTiles = PF ? prefill_q_tiles(D, FP8) : 1;
+  static constexpr bool kQQ = kQTiles == 2;
+  static constexpr int kSoftmaxWarps = kConsumerWarps * kQTiles;  // one per TMEM lane quarter and query tile
   // Decode-only plans over an fp8 cache, whose tiles carry half the bytes of a
   // bf16 tile for the same arithmetic: each consumer warp copies its share of
   // a K and a V tile into registers and releases both stages at once (a stage
@@ -76,28 +88,36 @@ struct Layout {
   static constexpr bool kStageRegs = FP8 && !PF && D <= 128;
   static constexpr int kDecGroups = 1;
   static constexpr int kDecWarps = kConsumerWarps * kDecGroups;  // decode consumer warps
-  // fp8 cache with prefill tiles: the roles are grouped by warpgroup (0..3
-  // softmax, 4..7 converters, 8 K/Q producer, 9 S issuer, 10 V producer, 11
-  // P V issuer) so that setmaxnreg can move registers from the converters and
-  // the single-thread roles to the softmax warps
-  static constexpr bool kSplitRegs = FP8 && PF;
-  static constexpr int kCons0 = kSplitRegs ? 0 : 2;  // first consumer (softmax / decode) warp
-  static constexpr int kKProdWarp = kSplitRegs ? 8 : 0;
-  static constexpr int kSWarp = kSplitRegs ? 9 : 1;
-  static constexpr int kVProducerWarp = kSplitRegs ? 10 : (PF ? 2 + kSoftmaxWarps : 1);
-  static constexpr int kConvWarp0 = kSplitRegs ? 4 : 2 + kSoftmaxWarps + 1;
+  static constexpr bool kSplitRegs = PF && (FP8 || kQQ);
   static constexpr int kConvWarps = (FP8 && PF) ? 4 : 0;
-  static constexpr int kPvWarp = kSplitRegs ? 11 : kConvWarp0 + kConvWarps;
+  static constexpr int kCons0 = kSplitRegs ? 0 : 2;  // first consumer (softmax / decode) warp
+  static constexpr int kSingle0 = kSoftmaxWarps + kConvWarps;  // (split) first single-role warp
+  static constexpr int kKProdWarp = kSplitRegs ? kSingle0 : 0;
+  static constexpr int kSWarp = kSplitRegs ? kSingle0 + 1 : 1;
+  static constexpr int kVProducerWarp = kSplitRegs ? kSingle0 + 2 : (PF ? 2 + kSoftmaxWarps : 1);
+  static constexpr int kConvWarp0 = kSplitRegs ? kSoftmaxWarps : 2 + kSoftmaxWarps + 1;
+  static constexpr int kPvWarp = kSplitRegs ? kSingle0 + 3 : kConvWarp0 + kConvWarps;
   static constexpr int kThreads = PF ? 32 * (3 + kSoftmaxWarps + kConvWarps + 1) : 32 * (2 + kDecWarps);
+  // registers a thread at launch (one block per SM) and, with the split, after
+  // each warpgroup's setmaxnreg: softmax, converters, single-role warps
+  static constexpr int kLaunchRegs = kThreads > 384 ? 128 : 168;
+  static constexpr int kRegsSoftmax = kThreads > 384 ? 144 : (kQQ ? 216 : 240);
+  static constexpr int kRegsConv = 152;
+  static constexpr int kRegsSingle = kQQ ? 72 : 112;
   static constexpr int kEsize = FP8 ? 1 : 2;
   // keys per K/V tile (one pipeline stage): 128, or 64 at D = 256 (stages of
   // 32 KB, and TMEM for three 64-column S buffers beside a 256-column O)
   static constexpr int kTile = D == 256 ? 64 : kKvTile;
+  // S buffers (per query tile); tensor memory of query tile q starts at
+  // q * kQCols: its S buffers, then its O
+  static constexpr int kSBufs = kQQ ? 1 : 3;
+  static constexpr uint32_t kQCols = kQQ ? 256 : 0;
   static constexpr uint32_t kTmemO = kSBufs * kTile;
-  static_assert(kTmemO + D <= kTmemCols, "tensor memory budget");
+  static_assert((kQQ ? kQCols * kQTiles : kTmemO + D) <= kTmemCols && (!kQQ || kTmemO + D <= kQCols),
+                "tensor memory budget");
   // decode-only plans give all shared memory to the rings
-  static constexpr int kStagesK = PF ? (FP8 ? 2 : (D == 64 ? 4 : 3)) : (FP8 || D == 64 ? 6 : 4);
-  static constexpr int kStagesV = PF ? (FP8 ? 2 : (D == 64 ? 4 : D == 256 ? 2 : 3)) : (FP8 || D == 64 ? 6 : 3);
+  static constexpr int kStagesK = PF ? (FP8 ? 2 : (D == 64 ? 4 : kQQ ? 2 : 3)) : (FP8 || D == 64 ? 6 : 4);
+  static constexpr int kStagesV = PF ? (FP8 ? 2 : (D == 64 ? 4 : D == 256 || kQQ ? 2 : 3)) : (FP8 || D == 64 ? 6 : 3);
   static constexpr int kTileBytes = kTile * D * kEsize;     // one raw K (or V) tile
   // A raw tile is [column chunks][128 rows][kRowBytes]: 128-byte chunks with
   // the 128-byte swizzle, or (an fp8 cache at D = 64) one chunk of 64-byte
@@ -106,10 +126,11 @@ struct Layout {
   static constexpr int kChunks = D * kEsize / kRowBytes;      // column chunks per cache row
   static constexpr int kKOff = 0;                             // K ring
   static constexpr int kVOff = kStagesK * kTileBytes;         // V ring
-  static constexpr int kQOff = kVOff + kStagesV * kTileBytes; // Q tile (128 x D, bf16; f16 after conversion)
+  static constexpr int kQOff = kVOff + kStagesV * kTileBytes; // Q tiles (128 x D, bf16; f16 after conversion)
+  static constexpr int kQBytes = kPrefillRowsTc * D * 2;      // one Q tile
   static constexpr int kConvTile = kTile * D * 2;             // one converted (f16) K or V tile
-  static constexpr int kConvBufs = D == 256 ? 1 : 2;          // converted tiles per operand
-  static constexpr int kKcOff = kQOff + (PF ? kPrefillRowsTc * D * 2 : 0);  // fp8: converted K tiles
+  static constexpr int kConvBufs = (D == 256 || (kQQ && D == 128)) ? 1 : 2;  // converted tiles per operand
+  static constexpr int kKcOff = kQOff + (PF ? kQTiles * kQBytes : 0);  // fp8: converted K tiles
   static constexpr int kVcOff = kKcOff + (kConvWarps ? kConvBufs * kConvTile : 0);  // fp8: converted V tiles
   // decode merge scratch: the item's last V stage, borrowed before it is
   // released, or (tiles staged in registers, every stage released at once)
@@ -120,7 +141,7 @@ struct Layout {
   static constexpr int kMergeBytes = kStageRegs ? kDecWarps * (D / 16) * 32 * 16 : 0;
   static constexpr int kMlOff = kMergeOff + kMergeBytes;     // float[kDecWarps][16][2] (m, l), int[kDecWarps]
   static constexpr int kBarOff = kMlOff + kDecWarps * kDecodeRows * 2 * 4 + kDecWarps * 4;  // + failed-wait flags
-  static constexpr int kNumBars = 2 * kStagesK + 2 * kStagesV + 3 + 3 * kSBufs + 9 + 1;
+  static constexpr int kNumBars = 2 * kStagesK + 2 * kStagesV + 3 + 3 * kSBufsMax + 9 + 1 + 3;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;     // tmem base, abort flag
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kAlloc = kBytes;                       // base is 1024-aligned (checked in the kernel)
@@ -145,6 +166,13 @@ struct Bars {
   uint64_t* vc_full;   // [2] converted V tile ready
   uint64_t* vc_empty;  // [2] P V of the tile using it has completed
   uint64_t* drain_pv;  // P V MMA completion before tensor memory is freed after an abort
+  // the second query tile of an item (two query tiles per item)
+  uint64_t* q_full_b;
+  uint64_t* q_empty_b;
+  uint64_t* qc_full_b;
+  __device__ __forceinline__ uint64_t* qfull(int q) const { return q ? q_full_b : q_full; }
+  __device__ __forceinline__ uint64_t* qempty(int q) const { return q ? q_empty_b : q_empty; }
+  __device__ __forceinline__ uint64_t* qcfull(int q) const { return q ? qc_full_b : qc_full; }
 };
 
 // Byte offset of 16-byte chunk c of row r in a tile of ROWS rows stored as
@@ -195,6 +223,22 @@ __device__ __forceinline__ WorkItem load_item(const AttnParams& p, int it) {
 template <int TILE>
 __device__ __forceinline__ int num_tiles(const WorkItem& w) {
   return w.kv_end > w.kv_begin ? (w.kv_end - w.kv_begin + TILE - 1) / TILE : 0;
+}
+
+// Query tile q (0 or 1) of a prefill item as an item of its own: its tokens
+// (none if the item has fewer) and, causal, the keys up to its last token's.
+// Every role derives the tiles of each query tile through here.
+__device__ __forceinline__ WorkItem q_tile(const WorkItem& w, int q, bool causal) {
+  WorkItem v = w;
+  const int tq = kPrefillRowsTc / w.nh;  // query tokens of a tile
+  v.q_i0 = w.q_i0 + q * tq;
+  v.q_row0 = w.q_row0 + q * tq;
+  v.n_q = max(0, min(tq, w.n_q - q * tq));
+  if (v.n_q == 0)
+    v.kv_end = v.kv_begin;
+  else if (causal)
+    v.kv_end = max(v.kv_begin, min(w.kv_end, v.q_i0 + v.n_q + w.lk - w.lq));
+  return v;
 }
 
 struct Ring {
@@ -294,7 +338,7 @@ __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CU
 
   Ring ring;
   int issued = 0;
-  uint32_t pi = 0;  // prefill items with at least one tile
+  uint32_t pi[2] = {0, 0};  // Q tiles loaded, per query tile of an item
   bool ok = true;
   bool dep_done = false;  // waited for the append kernel (rows at or past the old cache length)
 
@@ -316,21 +360,27 @@ __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CU
         mark_full(pend);
         pend = -1;
       }
-      if (!warp_wait(B.q_empty, (pi & 1) ^ 1, abort_flag)) {
-        ok = false;
-        break;
+      // each query tile of the item that has keys to attend, into its own buffer
+      for (int q = 0; q < L::kQTiles; ++q) {
+        const WorkItem wq = L::kQQ ? q_tile(w, q, p.causal) : w;
+        if (num_tiles<L::kTile>(wq) == 0) continue;
+        if (!warp_wait(B.qempty(q), (pi[q] & 1) ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          if (pi[0] + pi[1] == 0) tma_prefetch_desc(tm_q);
+          // the box: nh_tc heads x (128 / nh_tc) tokens, every byte credited (zero fill included)
+          const int nh_tc = tc_group_heads(p.G);
+          mbar_arrive_expect_tx(B.qfull(q), (uint32_t)((D / 64) * nh_tc * (kPrefillRowsTc / nh_tc) * 128));
+        }
+        __syncwarp();
+        if (lane < D / 64)
+          tma_load_3d(smem + L::kQOff + q * L::kQBytes + lane * (kPrefillRowsTc * 128), tm_q, B.qfull(q), lane * 64,
+                      w.hk * p.G + w.h0, wq.q_row0);
+        ++pi[q];
       }
-      if (lane == 0) {
-        if (pi == 0) tma_prefetch_desc(tm_q);
-        // the box: nh_tc heads x (128 / nh_tc) tokens, every byte credited (zero fill included)
-        const int nh_tc = tc_group_heads(p.G);
-        mbar_arrive_expect_tx(B.q_full, (uint32_t)((D / 64) * nh_tc * (kPrefillRowsTc / nh_tc) * 128));
-      }
-      __syncwarp();
-      if (lane < D / 64)
-        tma_load_3d(smem + L::kQOff + lane * (kPrefillRowsTc * 128), tm_q, B.q_full, lane * 64, w.hk * p.G + w.h0,
-                    w.q_row0);
-      ++pi;
+      if (!ok) break;
     }
     int q = 0;  // tile of the current page group
     for (int t0 = w.kv_begin; t0 < w.kv_end; t0 += kTile) {
@@ -438,7 +488,7 @@ __device__ bool s_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
     if (n == 0) continue;
     if (!mbar_wait(FP8 ? B.qc_full : B.q_full, pi & 1, abort_flag)) return false;
     for (int j = 0; j < n; ++j) {
-      const uint32_t T = pt + j, b = T % kSBufs, use = T / kSBufs;
+      const uint32_t T = pt + j, b = T % L::kSBufs, use = T / L::kSBufs;
       uint32_t k_base;
       if constexpr (FP8 && !QF8) {
         constexpr int NB = L::kConvBufs;
@@ -509,8 +559,8 @@ __device__ bool pv_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, vol
       continue;
     }
     for (int j = 0; j < n; ++j) {
-      const uint32_t T = pt + j, b = T % kSBufs;
-      if (!mbar_wait(&B.p_full[b], (T / kSBufs) & 1, abort_flag)) return false;
+      const uint32_t T = pt + j, b = T % L::kSBufs;
+      if (!mbar_wait(&B.p_full[b], (T / L::kSBufs) & 1, abort_flag)) return false;
       uint32_t v_base;
       if constexpr (FP8) {
         constexpr int NB = L::kConvBufs;
@@ -539,6 +589,168 @@ __device__ bool pv_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, vol
       rv.advance<L::kStagesV>();
     }
     pt += n;
+  }
+  return true;
+}
+
+// The same two queues with two query tiles per item (D <= 128): query tile q
+// has one S buffer (at q * 256 in tensor memory) and its O, and barriers
+// s_full / p_full / o_done [q].  For K tile j the S issuer runs S_q = Q_q K_j^T
+// for each query tile whose keys reach tile j (once P V of that tile's
+// previous K/V tile has freed its S buffer) and then releases the K tile; the
+// P V issuer runs O_q += P_q V_j as each tile's P is written, except that on a
+// tile whose V rows past the sequence a softmax warpgroup zeroes (bf16 cache;
+// the second tile's, which always reaches the item's last K/V tile) both P
+// are waited for first.  So one query tile's MMAs run while the other's
+// softmax does.
+template <int D, bool FP8, bool PF, bool QF8>
+__device__ bool s_issuer_qq(const AttnParams& p, uint8_t* smem, const Bars& B, volatile int* abort_flag, uint32_t tmem,
+                            int it0, int it1) {
+  using L = Layout<D, FP8, PF>;
+  constexpr int kAB = FP8 ? 0 : 1;
+  constexpr int kTile = L::kTile;
+  constexpr uint32_t kIdescQK = idesc_f16(kAB, 0, 128, kTile);
+  constexpr int NB = L::kConvBufs;
+  Ring rk;
+  uint32_t pt[2] = {0, 0}, pi[2] = {0, 0}, ck = 0;  // S tiles and items per query tile; K tiles (converted)
+  for (int it = it0; it < it1; ++it) {
+    const WorkItem w = load_item(p, it);
+    const int n = num_tiles<kTile>(w);
+    if (w.kind != kPrefill) {
+      rk.advance<L::kStagesK>(n);
+      continue;
+    }
+    if (n == 0) continue;
+    int nq[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) nq[q] = num_tiles<kTile>(q_tile(w, q, p.causal));
+    // the item's Q tiles first (the producer loads them after every K tile
+    // of the items before)
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      if (nq[q] > 0 && !mbar_wait(FP8 ? B.qcfull(q) : B.qfull(q), pi[q] & 1, abort_flag)) return false;
+    for (int j = 0; j < n; ++j) {
+      uint32_t k_base;
+      if constexpr (FP8 && !QF8) {
+        if (!mbar_wait(&B.kc_full[ck % NB], (ck / NB) & 1, abort_flag)) return false;
+        k_base = smem_u32(smem + L::kKcOff + (ck % NB) * L::kConvTile);
+      } else {
+        if (!mbar_wait(&B.full_k[rk.stage], rk.phase, abort_flag)) return false;
+        k_base = smem_u32(smem + L::kKOff + rk.stage * L::kTileBytes);
+      }
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        if (j >= nq[q]) continue;
+        // the S buffer last held S and P of this query tile's previous tile
+        if (pt[q] >= 1 && !mbar_wait(&B.o_done[q], (pt[q] - 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t s_tmem = tmem + q * L::kQCols;
+        if constexpr (QF8) {
+          const uint32_t q_base = smem_u32(smem + L::kKcOff + q * (kPrefillRowsTc * D));
+#pragma unroll
+          for (int k = 0; k < D / 32; ++k) {
+            if constexpr (D >= 128)
+              umma_ss_e4m3(s_tmem, sdesc_sw128(q_base + (k >> 2) * (kPrefillRowsTc * 128) + (k & 3) * 32, 16, 1024),
+                           sdesc_sw128(k_base + (k >> 2) * (kTile * 128) + (k & 3) * 32, 16, 1024), kIdescQK,
+                           k > 0 ? 1u : 0u);
+            else
+              umma_ss_e4m3(s_tmem, sdesc_sw64(q_base + k * 32, 16, 512), sdesc_sw64(k_base + k * 32, 16, 512),
+                           kIdescQK, k > 0 ? 1u : 0u);
+          }
+        } else {
+          const uint32_t q_base = smem_u32(smem + L::kQOff + q * L::kQBytes);
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t qoff = (k >> 2) * (kPrefillRowsTc * 128) + (k & 3) * 32;
+            const uint32_t koff = (k >> 2) * (kTile * 128) + (k & 3) * 32;
+            umma_ss(s_tmem, sdesc_sw128(q_base + qoff, 16, 1024), sdesc_sw128(k_base + koff, 16, 1024), kIdescQK,
+                    k > 0 ? 1u : 0u);
+          }
+        }
+        umma_commit(&B.s_full[q]);
+        ++pt[q];
+      }
+      // the K tile is free once these MMAs have completed (the raw-stage
+      // barrier expects one arrival per consumer warp: all but one now)
+      if constexpr (FP8 && !QF8) {
+        umma_commit(&B.kc_empty[ck % NB]);
+        ++ck;
+      } else {
+        mbar_arrive_cnt(&B.empty_k[rk.stage], kConsumerWarps - 1);
+        umma_commit(&B.empty_k[rk.stage]);
+      }
+      rk.advance<L::kStagesK>();
+    }
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      if (nq[q] == 0) continue;
+      umma_commit(B.qempty(q));
+      ++pi[q];
+    }
+  }
+  return true;
+}
+
+template <int D, bool FP8, bool PF>
+__device__ bool pv_issuer_qq(const AttnParams& p, uint8_t* smem, const Bars& B, volatile int* abort_flag,
+                             uint32_t tmem, int it0, int it1) {
+  using L = Layout<D, FP8, PF>;
+  constexpr int kAB = FP8 ? 0 : 1;
+  constexpr int kTile = L::kTile;
+  constexpr uint32_t kIdescPV = idesc_f16(kAB, 1, 128, D);
+  constexpr int NB = L::kConvBufs;
+  Ring rv;
+  uint32_t pt[2] = {0, 0}, cv = 0;  // P V tiles per query tile; V tiles (converted)
+  for (int it = it0; it < it1; ++it) {
+    const WorkItem w = load_item(p, it);
+    const int n = num_tiles<kTile>(w);
+    if (w.kind != kPrefill) {
+      rv.advance<L::kStagesV>(n);
+      continue;
+    }
+    int nq[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) nq[q] = num_tiles<kTile>(q_tile(w, q, p.causal));
+    for (int j = 0; j < n; ++j) {
+      // bf16: V rows past the sequence are zeroed by the second query tile's
+      // warps when both reach this tile: the first tile's P V waits for them
+      const bool both = !FP8 && w.kv_begin + (j + 1) * kTile > w.lk && j < nq[0] && j < nq[1];
+      // P of the first query tile reaching this tile before its V (the
+      // softmax has then seen S of the tile, so every fill before it is in)
+      const int q0 = j < nq[0] ? 0 : 1;
+      if (!mbar_wait(&B.p_full[q0], pt[q0] & 1, abort_flag)) return false;
+      if (both && !mbar_wait(&B.p_full[1], pt[1] & 1, abort_flag)) return false;
+      uint32_t v_base;
+      if constexpr (FP8) {
+        if (!mbar_wait(&B.vc_full[cv % NB], (cv / NB) & 1, abort_flag)) return false;
+        v_base = smem_u32(smem + L::kVcOff + (cv % NB) * L::kConvTile);
+      } else {
+        if (!mbar_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
+        v_base = smem_u32(smem + L::kVOff + rv.stage * L::kTileBytes);
+      }
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        if (j >= nq[q]) continue;
+        if (q != q0 && !(both && q == 1) && !mbar_wait(&B.p_full[q], pt[q] & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t p_tmem = tmem + q * L::kQCols;  // P over the first columns of the S buffer
+#pragma unroll
+        for (int k = 0; k < kTile / 16; ++k) {
+          const uint64_t bd = sdesc_sw128(v_base + k * 16 * 128, kTile * 128, 1024);
+          umma_ts(p_tmem + L::kTmemO, p_tmem + k * 8, bd, kIdescPV, (j == 0 && k == 0) ? 0u : 1u);
+        }
+        umma_commit(&B.o_done[q]);
+        ++pt[q];
+      }
+      if constexpr (FP8) {
+        umma_commit(&B.vc_empty[cv % NB]);
+        ++cv;
+      } else {
+        mbar_arrive_cnt(&B.empty_v[rv.stage], kConsumerWarps - 1);
+        umma_commit(&B.empty_v[rv.stage]);
+      }
+      rv.advance<L::kStagesV>();
+    }
   }
   return true;
 }
@@ -593,7 +805,7 @@ __device__ bool converter(const AttnParams& p, uint8_t* smem, const Bars& B, vol
   const int lane = threadIdx.x & 31;
   const int ct = threadIdx.x - 32 * L::kConvWarp0;  // 0..127
   Ring rk, rv;
-  uint32_t pt = 0, pi = 0;
+  uint32_t pt = 0, pi[2] = {0, 0};
   for (int it = it0; it < it1; ++it) {
     const WorkItem w = load_item(p, it);
     const int n = num_tiles<L::kTile>(w);
@@ -603,46 +815,51 @@ __device__ bool converter(const AttnParams& p, uint8_t* smem, const Bars& B, vol
       continue;
     }
     if (n == 0) continue;
-    if (!warp_wait(B.q_full, pi & 1, abort_flag)) return false;
-    if constexpr (QF8) {
-      // Q: bf16 -> e4m3 with the cache's encode (one IEEE reciprocal of q_scale,
-      // an RN multiply per value, RN satfinite), into the first converted-K
-      // buffer as [128 rows][128 B] swizzled: the 16 values of e4m3 chunk c of
-      // row r come from bf16 chunks 2c and 2c+1 of that row
-      const float inv_q = __frcp_rn(__ldg(p.q_scale));
-      auto quant4 = [&](uint32_t w0, uint32_t w1) -> uint32_t {
-        auto lo = [](uint32_t v) { return __uint_as_float(v << 16); };
-        auto hi = [](uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); };
-        const uint32_t a = f32x2_to_e4m3x2(__fmul_rn(lo(w0), inv_q), __fmul_rn(hi(w0), inv_q));
-        const uint32_t b = f32x2_to_e4m3x2(__fmul_rn(lo(w1), inv_q), __fmul_rn(hi(w1), inv_q));
-        return a | (b << 16);
-      };
-      const uint8_t* qb = smem + L::kQOff;
-      uint8_t* q8 = smem + L::kKcOff;
-      constexpr int kCpr = D / 16;  // e4m3 16-byte chunks per row
+    // each query tile of the item that has keys to attend
+    for (int qt = 0; qt < L::kQTiles; ++qt) {
+      if (L::kQQ && num_tiles<L::kTile>(q_tile(w, qt, p.causal)) == 0) continue;
+      if (!warp_wait(B.qfull(qt), pi[qt] & 1, abort_flag)) return false;
+      if constexpr (QF8) {
+        // Q: bf16 -> e4m3 with the cache's encode (one IEEE reciprocal of
+        // q_scale, an RN multiply per value, RN satfinite), into the converted-K
+        // area (query tile q at q x 128 x D bytes) as [128 rows][128 B]
+        // swizzled: the 16 values of e4m3 chunk c of row r come from bf16
+        // chunks 2c and 2c+1 of that row
+        const float inv_q = __frcp_rn(__ldg(p.q_scale));
+        auto quant4 = [&](uint32_t w0, uint32_t w1) -> uint32_t {
+          auto lo = [](uint32_t v) { return __uint_as_float(v << 16); };
+          auto hi = [](uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); };
+          const uint32_t a = f32x2_to_e4m3x2(__fmul_rn(lo(w0), inv_q), __fmul_rn(hi(w0), inv_q));
+          const uint32_t b = f32x2_to_e4m3x2(__fmul_rn(lo(w1), inv_q), __fmul_rn(hi(w1), inv_q));
+          return a | (b << 16);
+        };
+        const uint8_t* qb = smem + L::kQOff + qt * L::kQBytes;
+        uint8_t* q8 = smem + L::kKcOff + qt * (kPrefillRowsTc * D);
+        constexpr int kCpr = D / 16;  // e4m3 16-byte chunks per row
 #pragma unroll 2
-      for (int k = 0; k < kCpr; ++k) {
-        int r, c;
-        conv_unit<kCpr>(ct + 128 * k, r, c);
-        const uint4 a = *reinterpret_cast<const uint4*>(qb + tile_off<kPrefillRowsTc>(r, 2 * c));
-        const uint4 b = *reinterpret_cast<const uint4*>(qb + tile_off<kPrefillRowsTc>(r, 2 * c + 1));
-        *reinterpret_cast<uint4*>(q8 + raw_off<L::kRowBytes, kPrefillRowsTc>(r, c)) =
-            make_uint4(quant4(a.x, a.y), quant4(a.z, a.w), quant4(b.x, b.y), quant4(b.z, b.w));
-      }
-    } else {
-      // Q: bf16 -> f16 in place (elementwise, so the swizzle does not matter)
-      uint4* q = reinterpret_cast<uint4*>(smem + L::kQOff);
+        for (int k = 0; k < kCpr; ++k) {
+          int r, c;
+          conv_unit<kCpr>(ct + 128 * k, r, c);
+          const uint4 a = *reinterpret_cast<const uint4*>(qb + tile_off<kPrefillRowsTc>(r, 2 * c));
+          const uint4 b = *reinterpret_cast<const uint4*>(qb + tile_off<kPrefillRowsTc>(r, 2 * c + 1));
+          *reinterpret_cast<uint4*>(q8 + raw_off<L::kRowBytes, kPrefillRowsTc>(r, c)) =
+              make_uint4(quant4(a.x, a.y), quant4(a.z, a.w), quant4(b.x, b.y), quant4(b.z, b.w));
+        }
+      } else {
+        // Q: bf16 -> f16 in place (elementwise, so the swizzle does not matter)
+        uint4* q = reinterpret_cast<uint4*>(smem + L::kQOff + qt * L::kQBytes);
 #pragma unroll 4
-      for (int k = 0; k < kPrefillRowsTc * D * 2 / 16 / 128; ++k) {
-        uint4 v = q[ct + 128 * k];
-        v = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
-        q[ct + 128 * k] = v;
+        for (int k = 0; k < kPrefillRowsTc * D * 2 / 16 / 128; ++k) {
+          uint4 v = q[ct + 128 * k];
+          v = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+          q[ct + 128 * k] = v;
+        }
       }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(B.qcfull(qt));
+      ++pi[qt];
     }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(B.qc_full);
-    ++pi;
     constexpr int NB = L::kConvBufs;
     for (int j = 0; j < n; ++j) {
       const uint32_t T = pt + j;
@@ -695,15 +912,18 @@ struct PendingEpi {
 };
 
 // Writes the pending item's rows (waits for its last P V), 32 columns at a time
-template <int D, uint32_t kTmemO>
+// (query tile qt of the item: its O and its P V barrier)
+template <class L>
 __device__ __forceinline__ bool epi_run(const AttnParams& p, const Bars& B, const PendingEpi& e, uint32_t t_lane,
-                                        volatile int* abort_flag) {
-  if (!warp_wait(&B.o_done[e.T % kSBufs], (e.T / kSBufs) & 1, abort_flag)) return false;
+                                        int qt, volatile int* abort_flag) {
+  constexpr int D = L::kD;
+  if (!warp_wait(&B.o_done[L::kQQ ? qt : e.T % L::kSBufs], (e.T / L::kSBufs) & 1, abort_flag)) return false;
   tc_fence_after();
+  const uint32_t o_col = qt * L::kQCols + L::kTmemO;
 #pragma unroll
   for (int c = 0; c < D / 32; ++c) {
     uint32_t o[32];
-    tmem_ld32(t_lane + kTmemO + c * 32, o);
+    tmem_ld32(t_lane + o_col + c * 32, o);
     tmem_wait_ld();
     if (e.dst != nullptr) {
       uint4 v[4];
@@ -734,15 +954,17 @@ __device__ __forceinline__ bool epi_run(const AttnParams& p, const Bars& B, cons
 // item: waits for its last P V, then writes the normalised fp32 row and the
 // log2 LSE into the item's partial slots, so that the deferred epilogue of
 // the common case carries no state for it.
-template <int D, uint32_t kTmemO>
-__device__ __forceinline__ bool epi_partial(const Bars& B, uint32_t T, float inv, float lse2, float* pdst,
-                                         float* lse_dst, uint32_t t_lane, volatile int* abort_flag) {
-  if (!warp_wait(&B.o_done[T % kSBufs], (T / kSBufs) & 1, abort_flag)) return false;
+template <class L>
+__device__ __forceinline__ bool epi_partial(const Bars& B, uint32_t T, int qt, float inv, float lse2, float* pdst,
+                                            float* lse_dst, uint32_t t_lane, volatile int* abort_flag) {
+  constexpr int D = L::kD;
+  if (!warp_wait(&B.o_done[L::kQQ ? qt : T % L::kSBufs], (T / L::kSBufs) & 1, abort_flag)) return false;
   tc_fence_after();
+  const uint32_t o_col = qt * L::kQCols + L::kTmemO;
 #pragma unroll
   for (int c = 0; c < D / 32; ++c) {
     uint32_t o[32];
-    tmem_ld32(t_lane + kTmemO + c * 32, o);
+    tmem_ld32(t_lane + o_col + c * 32, o);
     tmem_wait_ld();
     if (pdst != nullptr) {
 #pragma unroll
@@ -774,10 +996,13 @@ __device__ __forceinline__ bool epi_partial(const Bars& B, uint32_t T, float inv
 template <int D, bool FP8, bool PF>
 __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* smem, const Bars& B,
                              volatile int* abort_flag, uint32_t tmem, Ring& rk, Ring& rv, uint32_t& pt, float sl2,
-                             float vscale, PendingEpi& pend) {
+                             float vscale, PendingEpi& pend, int qt_, int n_ring, bool zero_owner) {
   using L = Layout<D, FP8, PF>;
   constexpr int kTile = L::kTile;
-  constexpr uint32_t kTmemO = L::kTmemO;
+  const int qt = L::kQQ ? qt_ : 0;  // (compile-time 0 with one query tile per item)
+  // (two query tiles per item: w is query tile qt of the item, whose K/V tiles
+  // number n_ring; its S buffer, O and barriers are its own)
+  const uint32_t o_col = qt * L::kQCols + L::kTmemO;
   // S columns held in registers at a time (all of a tile's but in the fp8
   // block without its register split)
   constexpr int kPass = (FP8 && !L::kSplitRegs ? 64 : 128) < kTile ? (FP8 && !L::kSplitRegs ? 64 : 128) : kTile;
@@ -810,9 +1035,9 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
   for (int j = 0; j < n; ++j) {
     const uint32_t T = pt + j;
     const int t0 = w.kv_begin + j * kTile;
-    const uint32_t sb = T % kSBufs;
-    const uint32_t s_col = sb * kTile;
-    if (!warp_wait(&B.s_full[sb], (T / kSBufs) & 1, abort_flag)) return false;
+    const uint32_t sb = L::kQQ ? qt : T % L::kSBufs;
+    const uint32_t s_col = L::kQQ ? qt * L::kQCols : sb * kTile;
+    if (!warp_wait(&B.s_full[sb], (T / L::kSBufs) & 1, abort_flag)) return false;
     tc_fence_after();
     const bool need_mask = __any_sync(0xffffffffu, t0 + kTile > lim);
     uint32_t s[kPass];  // (unused when rolled)
@@ -851,8 +1076,9 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
 #pragma unroll
       for (int c = 0; c < kPass / 32; ++c) tmem_ld32(t_lane + s_col + h * kPass + c * 32, s + c * 32);
       tmem_wait_ld();
-      if constexpr (!FP8) {
-        // S of this tile is complete: its K stage is free
+      if constexpr (!FP8 && !L::kQQ) {
+        // S of this tile is complete: its K stage is free (with two query
+        // tiles the S issuer releases it)
         __syncwarp();
         if (lane == 0) mbar_arrive(&B.empty_k[rk.stage]);
       }
@@ -940,7 +1166,7 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
     f32x2_split(sum2[1], q2, q3);
     l = l * alpha + ((q0 + q2) + (q1 + q3));
 
-    const bool zero_v = !FP8 && t0 + kTile > w.lk;
+    const bool zero_v = !FP8 && (!L::kQQ || zero_owner) && t0 + kTile > w.lk;
     if (zero_v) {
       // rows past the sequence may hold anything (even NaN): zero them in V
       if (!warp_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
@@ -954,22 +1180,23 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
     }
     if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
       // O must hold P V of tile T-1 before it is rescaled
-      if (!warp_wait(&B.o_done[(T - 1) % kSBufs], ((T - 1) / kSBufs) & 1, abort_flag)) return false;
+      if (!warp_wait(&B.o_done[L::kQQ ? qt : (T - 1) % L::kSBufs], ((T - 1) / L::kSBufs) & 1, abort_flag))
+        return false;
       tc_fence_after();
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
-        tmem_ld32(t_lane + kTmemO + c * 32, o);
+        tmem_ld32(t_lane + o_col + c * 32, o);
         tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-        tmem_st32(t_lane + kTmemO + c * 32, o);
+        tmem_st32(t_lane + o_col + c * 32, o);
       }
     }
     // the previous item's O is written out before P V of this item's first tile
     // may replace it
     if (j == 0 && pend.has) {
-      if (!epi_run<D, L::kTmemO>(p, B, pend, t_lane, abort_flag)) return false;
+      if (!epi_run<L>(p, B, pend, t_lane, qt, abort_flag)) return false;
       pend.has = false;
     }
     tmem_wait_st();
@@ -979,6 +1206,11 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
     if (lane == 0) mbar_arrive(&B.p_full[sb]);
     rk.advance<L::kStagesK>();
     rv.advance<L::kStagesV>();
+  }
+  // (the item's K/V tiles past this query tile's keys)
+  if (L::kQQ && n_ring > n) {
+    rk.advance<L::kStagesK>(n_ring - n);
+    rv.advance<L::kStagesV>(n_ring - n);
   }
 
   // epilogue: O / l -> bf16 rows and the natural-log LSE (or, for a split-KV
@@ -994,8 +1226,8 @@ __device__ bool softmax_item(const AttnParams& p, const WorkItem& w, uint8_t* sm
   if (n > 0 && part) {
     // a split-KV chunk: its partial rows at once (the previous item's deferred
     // epilogue ran in this item's first tile)
-    if (!epi_partial<D, kTmemO>(B, pt + n - 1, l > 0.f ? vscale / l : 0.f, lse, valid ? pdst : nullptr, lse_dst,
-                                t_lane, abort_flag))
+    if (!epi_partial<L>(B, pt + n - 1, qt, l > 0.f ? vscale / l : 0.f, lse, valid ? pdst : nullptr, lse_dst, t_lane,
+                        abort_flag))
       return false;
   } else if (n > 0) {
     pend.has = true;
@@ -1064,6 +1296,13 @@ __device__ bool run_decode(const AttnParams& p, const WorkItem& w, uint8_t* smem
   const int g = lane >> 2, t = lane & 3;
   const int mi = lane >> 3;                      // ldmatrix: the 8x8 matrix this lane addresses
   const int kw0 = (cw % kConsumerWarps) * KPW;   // this warp's keys of each of its group's tiles
+  // Key of row x (0..7, and x + 8) of a 16-key m-tile: x, or (fp8 cache with
+  // 128-byte rows, swizzled chunk XOR row % 8) the interleaving 0 4 1 5 2 6 3 7,
+  // so that the two key rows a quarter-warp's 16-byte K reads span (rows of g
+  // and g + 1, four chunks each) fall on different bank groups; V and the
+  // masks follow the same order.
+  constexpr bool kPerm = FP8 && RB == 128;
+  auto krow = [](int x) { return kPerm ? (((x & 1) << 2) | (x >> 1)) : x; };
   const int R = w.n_q * p.G;
 
   // this thread's query rows (N columns of S^T and O^T): 8j + 2t + e
@@ -1160,7 +1399,7 @@ __device__ bool run_decode(const AttnParams& p, const WorkItem& w, uint8_t* smem
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int c = 0; c < D / 64; ++c)
-            kreg[i][h][c] = lds_u128(kb + raw_off<RB, kTile>(kw0 + 16 * i + 8 * h + g, 4 * c + t));
+            kreg[i][h][c] = lds_u128(kb + raw_off<RB, kTile>(kw0 + 16 * i + 8 * h + krow(g), 4 * c + t));
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.empty_k[rk.stage]);
       if (!warp_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) {
@@ -1171,7 +1410,7 @@ __device__ bool run_decode(const AttnParams& p, const WorkItem& w, uint8_t* smem
       for (int i = 0; i < MT; ++i)
 #pragma unroll
         for (int cp = 0; cp < D / 32; ++cp)
-          ldsm_x4_t(vb + raw_off<RB, kTile>(kw0 + 16 * i + (mi & 1) * 8 + (lane & 7), 2 * cp + (mi >> 1)), vreg[i][cp][0],
+          ldsm_x4_t(vb + raw_off<RB, kTile>(kw0 + 16 * i + (mi & 1) * 8 + krow(lane & 7), 2 * cp + (mi >> 1)), vreg[i][cp][0],
                     vreg[i][cp][1], vreg[i][cp][2], vreg[i][cp][3]);
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.empty_v[rv.stage]);
@@ -1193,8 +1432,8 @@ __device__ bool run_decode(const AttnParams& p, const WorkItem& w, uint8_t* smem
             ka = kreg[i][0][c];
             kc = kreg[i][1][c];
           } else {
-            ka = lds_u128(kb + raw_off<RB, kTile>(kw0 + 16 * i + g, 4 * c + t));
-            kc = lds_u128(kb + raw_off<RB, kTile>(kw0 + 16 * i + 8 + g, 4 * c + t));
+            ka = lds_u128(kb + raw_off<RB, kTile>(kw0 + 16 * i + krow(g), 4 * c + t));
+            kc = lds_u128(kb + raw_off<RB, kTile>(kw0 + 16 * i + 8 + krow(g), 4 * c + t));
           }
           const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w}, wc[4] = {kc.x, kc.y, kc.z, kc.w};
           if constexpr (QF8) {
@@ -1238,7 +1477,7 @@ __device__ bool run_decode(const AttnParams& p, const WorkItem& w, uint8_t* smem
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
       for (int i = 0; i < MT; ++i) {
-        const int ka = t0 + kw0 + 16 * i + g, kc = ka + 8;
+        const int ka = t0 + kw0 + 16 * i + krow(g), kc = ka + 8;
         s[j][i][0] = ka < lim[j][0] ? s[j][i][0] * sl2 : -INFINITY;
         s[j][i][1] = ka < lim[j][1] ? s[j][i][1] * sl2 : -INFINITY;
         s[j][i][2] = kc < lim[j][0] ? s[j][i][2] * sl2 : -INFINITY;
@@ -1292,9 +1531,9 @@ __device__ bool run_decode(const AttnParams& p, const WorkItem& w, uint8_t* smem
         pb[j][0] = movm_t(FP8 ? pack_f16(s[j][i][0], s[j][i][1]) : pack_bf16(s[j][i][0], s[j][i][1]));
         pb[j][1] = movm_t(FP8 ? pack_f16(s[j][i][2], s[j][i][3]) : pack_bf16(s[j][i][2], s[j][i][3]));
       }
-      const int k0 = t0 + kw0 + 16 * i + 2 * t;
-      const uint32_t mlo = (k0 < w.lk ? 0x0000FFFFu : 0u) | (k0 + 1 < w.lk ? 0xFFFF0000u : 0u);
-      const uint32_t mhi = (k0 + 8 < w.lk ? 0x0000FFFFu : 0u) | (k0 + 9 < w.lk ? 0xFFFF0000u : 0u);
+      const int k0 = t0 + kw0 + 16 * i + krow(2 * t), k1 = t0 + kw0 + 16 * i + krow(2 * t + 1);
+      const uint32_t mlo = (k0 < w.lk ? 0x0000FFFFu : 0u) | (k1 < w.lk ? 0xFFFF0000u : 0u);
+      const uint32_t mhi = (k0 + 8 < w.lk ? 0x0000FFFFu : 0u) | (k1 + 8 < w.lk ? 0xFFFF0000u : 0u);
       if constexpr (FP8) {
 #pragma unroll
         for (int cp = 0; cp < D / 32; ++cp) {
@@ -1302,7 +1541,7 @@ __device__ bool run_decode(const AttnParams& p, const WorkItem& w, uint8_t* smem
           if constexpr (kRegs) {
             v[0] = vreg[i][cp][0], v[1] = vreg[i][cp][1], v[2] = vreg[i][cp][2], v[3] = vreg[i][cp][3];
           } else {
-            ldsm_x4_t(vb + raw_off<RB, kTile>(kw0 + 16 * i + (mi & 1) * 8 + (lane & 7), 2 * cp + (mi >> 1)), v[0], v[1],
+            ldsm_x4_t(vb + raw_off<RB, kTile>(kw0 + 16 * i + (mi & 1) * 8 + krow(lane & 7), 2 * cp + (mi >> 1)), v[0], v[1],
                       v[2], v[3]);
           }
 #pragma unroll
@@ -1597,7 +1836,13 @@ __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
         rv.advance<L::kStagesV>(num_tiles<L::kTile>(w));
       }
     } else if constexpr (PF) {
-      ok = softmax_item<D, FP8, PF>(p, w, smem, B, abort_flag, tmem, rk, rv, pt, QF8 ? sl2q : sl2, vscale, pend);
+      // (two query tiles per item: warpgroup qt takes tile qt; the second
+      // tile's warps zero V rows past the sequence whenever it has keys)
+      const int qt = L::kQQ ? ((threadIdx.x >> 5) - L::kCons0) >> 2 : 0;
+      const WorkItem wq = L::kQQ ? q_tile(w, qt, p.causal) : w;
+      const bool zero_owner = !L::kQQ || qt == 1 || num_tiles<L::kTile>(q_tile(w, 1, p.causal)) == 0;
+      ok = softmax_item<D, FP8, PF>(p, wq, smem, B, abort_flag, tmem, rk, rv, pt, QF8 ? sl2q : sl2, vscale, pend, qt,
+                                    num_tiles<L::kTile>(w), zero_owner);
     } else {
       ok = false;  // a decode-only launch never receives prefill tiles
     }
@@ -1611,7 +1856,8 @@ __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
     if (pend.has) {
       // the last prefill item's epilogue
       const int qw = (threadIdx.x >> 5) & 3;
-      if (!epi_run<D, L::kTmemO>(p, B, pend, tmem + ((uint32_t)(qw * 32) << 16), abort_flag)) {
+      const int qt = L::kQQ ? ((threadIdx.x >> 5) - L::kCons0) >> 2 : 0;
+      if (!epi_run<L>(p, B, pend, tmem + ((uint32_t)(qw * 32) << 16), qt, abort_flag)) {
         record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, it1);
         *abort_flag = 1;
         return false;
@@ -1648,14 +1894,17 @@ __global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
   B.q_empty = B.q_full + 1;
   B.drain = B.q_full + 2;
   B.s_full = B.q_full + 3;
-  B.p_full = B.s_full + kSBufs;
-  B.o_done = B.p_full + kSBufs;
-  B.qc_full = B.o_done + kSBufs;
+  B.p_full = B.s_full + kSBufsMax;
+  B.o_done = B.p_full + kSBufsMax;
+  B.qc_full = B.o_done + kSBufsMax;
   B.kc_full = B.qc_full + 1;
   B.kc_empty = B.kc_full + 2;
   B.vc_full = B.kc_empty + 2;
   B.vc_empty = B.vc_full + 2;
   B.drain_pv = B.vc_empty + 2;
+  B.q_full_b = B.drain_pv + 1;
+  B.q_empty_b = B.drain_pv + 2;
+  B.qc_full_b = B.drain_pv + 3;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1673,13 +1922,17 @@ __global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
     }
     mbar_init(B.q_full, 1);
     mbar_init(B.q_empty, 1);
-    for (int i = 0; i < kSBufs; ++i) {
+    mbar_init(B.q_full_b, 1);
+    mbar_init(B.q_empty_b, 1);
+    for (int i = 0; i < kSBufsMax; ++i) {
       mbar_init(&B.s_full[i], 1);
-      mbar_init(&B.p_full[i], L::kSoftmaxWarps);
+      // one arrival per softmax warp of the query tile the buffer serves
+      mbar_init(&B.p_full[i], L::kQQ ? kConsumerWarps : L::kSoftmaxWarps);
       mbar_init(&B.o_done[i], 1);
     }
     if (L::kConvWarps > 0) {
       mbar_init(B.qc_full, L::kConvWarps);
+      mbar_init(B.qc_full_b, L::kConvWarps);
       for (int i = 0; i < 2; ++i) {
         mbar_init(&B.kc_full[i], L::kConvWarps);
         mbar_init(&B.kc_empty[i], 1);
@@ -1703,12 +1956,17 @@ __global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
   grid_dep_launch();  // the combine kernel may be scheduled; it waits for this grid to finish
   const int it0 = p.cta_begin[blockIdx.x], it1 = p.cta_begin[blockIdx.x + 1];
   if constexpr (L::kSplitRegs) {
-    // 240 (softmax) + 152 (converters) + 112 (producers, issuers) registers a
-    // thread, one warpgroup each: exactly the 168 x 384 the block was launched
-    // with.  Each warpgroup runs one setmaxnreg at the head of its branch.
-    static_assert((240 + 152 + 112) * 128 == 168 * L::kThreads, "register split");
-    if (warp >= 8) {
-      reg_dealloc<112>();
+    // softmax (one warpgroup per query tile), converters (fp8 cache),
+    // producers and issuers: the registers of the warpgroups add up to exactly
+    // what the block was launched with (fp8, two query tiles: 2 x 144 + 152 +
+    // 72 of 4 x 128; bf16, two query tiles: 2 x 216 + 72 of 3 x 168; fp8 at
+    // D = 256: 240 + 152 + 112 of 3 x 168).  Each warpgroup runs one setmaxnreg
+    // at the head of its branch.
+    static_assert((L::kSoftmaxWarps * L::kRegsSoftmax + L::kConvWarps * L::kRegsConv + 4 * L::kRegsSingle) * 32 ==
+                      L::kLaunchRegs * L::kThreads,
+                  "register split");
+    if (warp >= L::kSingle0) {
+      reg_dealloc<L::kRegsSingle>();
       if (warp == L::kKProdWarp) {
         producer<D, FP8, PF, false>(p, &tm_k, &tm_q, smem, B, abort_flag, it0, it1);
         return;
@@ -1719,8 +1977,14 @@ __global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
       }
       if (lane == 0) {
         const bool pv = warp == L::kPvWarp;
-        if (!(pv ? pv_issuer<D, FP8, PF>(p, smem, B, abort_flag, tmem, it0, it1)
-                 : s_issuer<D, FP8, PF, QF8>(p, smem, B, abort_flag, tmem, it0, it1))) {
+        bool ok;
+        if constexpr (L::kQQ)
+          ok = pv ? pv_issuer_qq<D, FP8, PF>(p, smem, B, abort_flag, tmem, it0, it1)
+                  : s_issuer_qq<D, FP8, PF, QF8>(p, smem, B, abort_flag, tmem, it0, it1);
+        else
+          ok = pv ? pv_issuer<D, FP8, PF>(p, smem, B, abort_flag, tmem, it0, it1)
+                  : s_issuer<D, FP8, PF, QF8>(p, smem, B, abort_flag, tmem, it0, it1);
+        if (!ok) {
           record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, pv ? -3 : -1);
           *abort_flag = 1;
           int zero = 0;
@@ -1729,15 +1993,18 @@ __global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
         }
       }
       __syncwarp();
-    } else if (warp >= 4) {
-      reg_dealloc<152>();
-      if (!converter<D, PF, QF8>(p, smem, B, abort_flag, it0, it1)) {
-        if (lane == 0) record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, -2);
-        *abort_flag = 1;
+    } else if (L::kConvWarps > 0 && warp >= L::kConvWarp0) {
+      if constexpr (L::kConvWarps > 0) {
+        if constexpr (L::kRegsConv > L::kLaunchRegs) reg_alloc<L::kRegsConv>();
+        else reg_dealloc<L::kRegsConv>();
+        if (!converter<D, PF, QF8>(p, smem, B, abort_flag, it0, it1)) {
+          if (lane == 0) record_status(p.status, PKV_ERR_DEVICE_TIMEOUT, blockIdx.x, -2);
+          *abort_flag = 1;
+        }
       }
       return;
     } else {
-      reg_alloc<240>();
+      reg_alloc<L::kRegsSoftmax>();
       consumer<D, FP8, PF, QF8, DEC>(p, smem, B, abort_flag, tmem, it0, it1);
     }
     // the S issuer, the consumers and the P V warp: every tensor-memory access
@@ -1810,13 +2077,13 @@ cudaError_t launch_t(const AttnParams& p, const CUtensorMap& tk, const CUtensorM
                              L::kAlloc);
     if (e != cudaSuccess) return e;
     if constexpr (L::kSplitRegs) {
-      // the register split adds up to exactly 168 registers a thread at launch:
-      // a build with any other count could leave the softmax warpgroup's
-      // increase waiting, so it is refused before it runs
+      // the register split adds up to exactly the registers a thread has at
+      // launch: a build with any other count could leave a warpgroup's increase
+      // waiting, so it is refused before it runs
       cudaFuncAttributes fa{};
       e = cudaFuncGetAttributes(&fa, attn_kernel<D, FP8, PF, QF8, DEC>);
       if (e != cudaSuccess) return e;
-      if (fa.numRegs != 168) return cudaErrorInvalidConfiguration;
+      if (fa.numRegs != L::kLaunchRegs) return cudaErrorInvalidConfiguration;
     }
     configured.fetch_or(bit);
   }

@@ -44,6 +44,13 @@ enum ItemKind : int32_t { kDecode = 0, kPrefill = 1 };
 #endif
 PKV_HOST_DEVICE inline int tc_group_heads(int G) { return G < kPrefillRowsTc ? G : kPrefillRowsTc; }
 
+// Query tiles of 128 rows a tensor-core prefill item may hold: two over an
+// fp8 cache at head_dim <= 128, whose K/V tiles (converted to f16 once) then
+// serve both, each with its own S and O in tensor memory and its own softmax
+// warpgroup; one otherwise (a bf16 cache measured slower with two).  The plan
+// pairs tiles only in plans without decode tiles.
+PKV_HOST_DEVICE constexpr int prefill_q_tiles(int head_dim, bool fp8) { return fp8 && head_dim <= 128 ? 2 : 1; }
+
 // One tile of work for one persistent CTA.  Rows of the tile are
 // (query token, head of the tile's head sub-group) pairs: row r = token * nh + g,
 // query head = hk * G + h0 + g.

@@ -102,6 +102,11 @@ pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const 
   const int dec_rows = decode_rows(D);  // rows of a warp-MMA decode tile (8 at D = 256)
   auto is_decode = [&](int lq) { return (int64_t)lq * G <= dec_rows; };
   auto splittable = [&](int lq) { return is_decode(lq) || lq <= tq_prefill; };
+  // an item of a long query run holds up to two consecutive tiles (fp8 cache,
+  // head dims up to 128; plans without decode tiles), which share its K/V tiles
+  bool any_decode = false;
+  for (int b = 0; b < B; ++b) any_decode |= h_q_lens[b] > 0 && is_decode(h_q_lens[b]);
+  const int tq_item = tq_prefill * (any_decode ? 1 : prefill_q_tiles(D, p.cache_dtype == PKV_FP8_E4M3));
 
   int64_t total_q = 0, total_new = 0, total_split_keys = 0;
   for (int b = 0; b < B; ++b) {
@@ -137,7 +142,7 @@ pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const 
     if (lq == 0) continue;
     num_tiles_est += (int64_t)p.num_heads_kv * (is_decode(lq) ? nchunks_of(lk)
                                                 : (int64_t)n_sub * (splittable(lq) ? nchunks_of(lk)
-                                                                                   : (lq + tq_prefill - 1) / tq_prefill));
+                                                                                   : (lq + tq_item - 1) / tq_item));
   }
   std::vector<Tile> tiles;
   tiles.reserve((size_t)num_tiles_est);
@@ -196,9 +201,9 @@ pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const 
             num_slots += (int64_t)nchunks * stride;
           }
         } else {
-          for (int i0 = 0; i0 < lq; i0 += tq_prefill) {
-            int n = std::min(tq_prefill, lq - i0);
-            int kv_end = lk;
+          for (int i0 = 0; i0 < lq; i0 += tq_item) {
+            int n = std::min(tq_item, lq - i0);
+            int kv_end = lk;  // the keys of the item's last query token
             if (p.causal) kv_end = std::max(0, std::min(lk, i0 + n + lk - lq));
             Tile t{};
             t.item.b = b;
@@ -214,7 +219,13 @@ pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const 
             t.item.partial = -1;
             t.item.h0 = h0;
             t.item.nh = nh;
-            t.cost = prefill_cost(kv_end, prefill_rows, D);
+            // each query tile of the item attends the keys of its own last token
+            t.cost = 0.0;
+            for (int s = i0; s < i0 + n; s += tq_prefill) {
+              const int ns = std::min(tq_prefill, i0 + n - s);
+              const int ke = p.causal ? std::max(0, std::min(lk, s + ns + lk - lq)) : lk;
+              t.cost += prefill_cost(ke, prefill_rows, D);
+            }
             tiles.push_back(t);
             ++n_pre;
           }

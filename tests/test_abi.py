@@ -90,7 +90,12 @@ def _coverage(spec, items, num_sms):
         if it["kind"] == 0:
             assert rows <= 16 and it["num_heads"] == G
         else:
-            assert rows <= 128 and it["num_heads"] == min(128, G - it["head0"])
+            # a tensor-core item holds two 128-row query tiles over an fp8 cache
+            # at head_dim <= 128 in a plan without decode tiles (one when it is a
+            # split-KV chunk), else one
+            pairs = spec.d <= 128 and spec.cache_dtype == "fp8" and not any(x["kind"] == 0 for x in items)
+            q_tiles = 2 if pairs and it["partial_slot"] < 0 else 1
+            assert rows <= 128 * q_tiles and it["num_heads"] == min(128, G - it["head0"])
     for b in range(spec.batch):
         lq, lk = int(spec.q_lens[b]), int(spec.kv_lens[b])
         for hq in range(spec.hq):
