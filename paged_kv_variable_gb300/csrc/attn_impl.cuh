@@ -129,13 +129,17 @@ struct Layout {
   static constexpr int kQOff = kVOff + kStagesV * kTileBytes; // Q tiles (128 x D, bf16; f16 after conversion)
   static constexpr int kQBytes = kPrefillRowsTc * D * 2;      // one Q tile
   static constexpr int kConvTile = kTile * D * 2;             // one converted (f16) K or V tile
-  static constexpr int kConvBufs = (D == 256 || (kQQ && D == 128)) ? 1 : 2;  // converted tiles per operand
+  // converted K and V tiles: two each, or one each at D = 256 and (two query
+  // tiles per item, D = 128) where shared memory is short (one more converted
+  // K or V tile there measured slower)
+  static constexpr int kConvBufsK = (D == 256 || (kQQ && D == 128)) ? 1 : 2;
+  static constexpr int kConvBufsV = kConvBufsK;
   static constexpr int kKcOff = kQOff + (PF ? kQTiles * kQBytes : 0);  // fp8: converted K tiles
-  static constexpr int kVcOff = kKcOff + (kConvWarps ? kConvBufs * kConvTile : 0);  // fp8: converted V tiles
+  static constexpr int kVcOff = kKcOff + (kConvWarps ? kConvBufsK * kConvTile : 0);  // fp8: converted V tiles
   // decode merge scratch: the item's last V stage, borrowed before it is
   // released, or (tiles staged in registers, every stage released at once)
   // its own area
-  static constexpr int kMergeOff = kVcOff + (kConvWarps ? kConvBufs * kConvTile : 0);
+  static constexpr int kMergeOff = kVcOff + (kConvWarps ? kConvBufsV * kConvTile : 0);
   // (tiles staged in registers: every warp's O^T of one 8-column tile, or the
   // tree's slots of two column tiles)
   static constexpr int kMergeBytes = kStageRegs ? kDecWarps * (D / 16) * 32 * 16 : 0;
@@ -491,7 +495,7 @@ __device__ bool s_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
       const uint32_t T = pt + j, b = T % L::kSBufs, use = T / L::kSBufs;
       uint32_t k_base;
       if constexpr (FP8 && !QF8) {
-        constexpr int NB = L::kConvBufs;
+        constexpr int NB = L::kConvBufsK;
         if (!mbar_wait(&B.kc_full[T % NB], (T / NB) & 1, abort_flag)) return false;
         k_base = smem_u32(smem + L::kKcOff + (T % NB) * L::kConvTile);
       } else {
@@ -531,7 +535,7 @@ __device__ bool s_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
         mbar_arrive_cnt(&B.empty_k[rk.stage], kConsumerWarps - 1);
         umma_commit(&B.empty_k[rk.stage]);
       } else if constexpr (FP8) {
-        umma_commit(&B.kc_empty[T % L::kConvBufs]);
+        umma_commit(&B.kc_empty[T % L::kConvBufsK]);
       }
       rk.advance<L::kStagesK>();
     }
@@ -563,7 +567,7 @@ __device__ bool pv_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, vol
       if (!mbar_wait(&B.p_full[b], (T / L::kSBufs) & 1, abort_flag)) return false;
       uint32_t v_base;
       if constexpr (FP8) {
-        constexpr int NB = L::kConvBufs;
+        constexpr int NB = L::kConvBufsV;
         if (!mbar_wait(&B.vc_full[T % NB], (T / NB) & 1, abort_flag)) return false;
         v_base = smem_u32(smem + L::kVcOff + (T % NB) * L::kConvTile);
       } else {
@@ -579,7 +583,7 @@ __device__ bool pv_issuer(const AttnParams& p, uint8_t* smem, const Bars& B, vol
       }
       umma_commit(&B.o_done[b]);
       if constexpr (FP8) {
-        umma_commit(&B.vc_empty[T % L::kConvBufs]);
+        umma_commit(&B.vc_empty[T % L::kConvBufsV]);
       } else {
         // the V stage barrier expects one arrival per consumer warp (as the decode
         // warps give): all but one now, the last when these MMAs complete
@@ -610,7 +614,7 @@ __device__ bool s_issuer_qq(const AttnParams& p, uint8_t* smem, const Bars& B, v
   constexpr int kAB = FP8 ? 0 : 1;
   constexpr int kTile = L::kTile;
   constexpr uint32_t kIdescQK = idesc_f16(kAB, 0, 128, kTile);
-  constexpr int NB = L::kConvBufs;
+  constexpr int NB = L::kConvBufsK;
   Ring rk;
   uint32_t pt[2] = {0, 0}, pi[2] = {0, 0}, ck = 0;  // S tiles and items per query tile; K tiles (converted)
   for (int it = it0; it < it1; ++it) {
@@ -698,7 +702,7 @@ __device__ bool pv_issuer_qq(const AttnParams& p, uint8_t* smem, const Bars& B, 
   constexpr int kAB = FP8 ? 0 : 1;
   constexpr int kTile = L::kTile;
   constexpr uint32_t kIdescPV = idesc_f16(kAB, 1, 128, D);
-  constexpr int NB = L::kConvBufs;
+  constexpr int NB = L::kConvBufsV;
   Ring rv;
   uint32_t pt[2] = {0, 0}, cv = 0;  // P V tiles per query tile; V tiles (converted)
   for (int it = it0; it < it1; ++it) {
@@ -860,7 +864,7 @@ __device__ bool converter(const AttnParams& p, uint8_t* smem, const Bars& B, vol
       if (lane == 0) mbar_arrive(B.qcfull(qt));
       ++pi[qt];
     }
-    constexpr int NB = L::kConvBufs;
+    constexpr int NB = L::kConvBufsK, NV = L::kConvBufsV;
     for (int j = 0; j < n; ++j) {
       const uint32_t T = pt + j;
       const int t0 = w.kv_begin + j * L::kTile;
@@ -877,14 +881,14 @@ __device__ bool converter(const AttnParams& p, uint8_t* smem, const Bars& B, vol
         }
       }
       if (!warp_wait(&B.full_v[rv.stage], rv.phase, abort_flag)) return false;
-      if (T >= NB && !warp_wait(&B.vc_empty[T % NB], ((T / NB) - 1) & 1, abort_flag)) return false;
+      if (T >= NV && !warp_wait(&B.vc_empty[T % NV], ((T / NV) - 1) & 1, abort_flag)) return false;
       // rows past the sequence may hold anything (even NaN): they become zeros
-      convert_tile<D, L::kTile>(smem + L::kVOff + rv.stage * L::kTileBytes, smem + L::kVcOff + (T % NB) * L::kConvTile,
+      convert_tile<D, L::kTile>(smem + L::kVOff + rv.stage * L::kTileBytes, smem + L::kVcOff + (T % NV) * L::kConvTile,
                                 ct, w.lk - t0);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&B.vc_full[T % NB]);
+        mbar_arrive(&B.vc_full[T % NV]);
         mbar_arrive(&B.empty_v[rv.stage]);
       }
       rk.advance<L::kStagesK>();
