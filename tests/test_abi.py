@@ -352,3 +352,23 @@ def test_wide_groups_plan(pkv, hq, hkv):
     assert dyn.items() == items
     with pytest.raises(pkv.PkvError):   # more query tokens than one tile holds: not a dynamic-plan request
         pkv.plan_decode_dynamic(prob, np.full(B, 200, np.int32), lc, np.full(B, 200, np.int32), num_sms=152)
+
+
+def test_two_query_tile_items_only_for_fp8_prefill_plans(pkv):
+    """Items of two 128-row query tiles (sharing each K/V tile) appear for an
+    fp8 cache at head_dim <= 128 in plans without decode tiles, and nowhere
+    else: not for a bf16 cache, not at head_dim 256, not beside a decode unit."""
+    def items(dtype, d, q_lens):
+        prob = pkv.make_problem(batch=len(q_lens), num_heads_q=8, num_heads_kv=2, head_dim=d, page_size=16,
+                                cache_capacity=4096, num_pages=1024, cache_dtype=dtype, causal=True,
+                                softmax_scale=0.125)
+        lc = [100] * len(q_lens)
+        return pkv.plan(prob, q_lens, lc, q_lens, num_sms=13).items()
+    tq = 128 // 4
+    pairs = [it for it in items("fp8", 128, [300, 70]) if it["n_q"] > tq]
+    assert pairs and all(it["n_q"] <= 2 * tq for it in pairs)
+    assert any(it["n_q"] > tq for it in items("fp8", 64, [300, 70]))
+    assert not any(it["n_q"] > tq for it in items("bf16", 128, [300, 70]))
+    assert not any(it["n_q"] > tq for it in items("fp8", 256, [300, 70]))
+    mixed = items("fp8", 128, [300, 1])
+    assert any(it["kind"] == 0 for it in mixed) and not any(it["n_q"] > tq for it in mixed)

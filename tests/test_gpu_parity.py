@@ -738,6 +738,40 @@ def test_fp8_quantised_queries_decode(P, G, split):
     H.compare_lse(g.lse, ref["lse"])
 
 
+@pytest.mark.parametrize("d,G,causal,P,q8", [(128, 4, True, 16, False), (64, 8, False, 0, False),
+                                              (128, 1, True, 32, True), (128, 16, True, 16, False),
+                                              (64, 2, True, 16, True), (128, 4, False, 1, False)])
+def test_fp8_two_query_tile_items(d, G, causal, P, q8):
+    """Prefill-only batches over an fp8 cache, whose items hold two query tiles
+    sharing each K/V tile: ragged query runs leave single-tile items and tiles
+    with fewer rows, the first tile of a causal item attending fewer key tiles
+    than the second; every row against the oracle."""
+    import dataclasses
+    rng = np.random.default_rng(700 + d + G + P + int(causal) + int(q8))
+    tq = 128 // G
+    lq = np.array([2 * tq + 5, 3 * tq + tq // 2, tq + 1, 4 * tq], np.int32)
+    lc = np.array([0, 130, 7, 300], np.int32)
+    spec = synth.Spec(batch=4, hq=2 * G, hkv=2, d=d, page_size=P, causal=causal,
+                      softmax_scale=float(np.float32(1.0 / np.sqrt(d))), cache_dtype="fp8",
+                      q_lens=lq, cache_lens=lc, new_lens=lq.copy(),
+                      capacity=int(((lc + lq).max() + 15) // 16 * 16 + 16), name="fp8-two-query-tiles")
+    case = synth.make_case(spec, rng)
+    if q8:
+        amax = float(np.abs(synth.bf16_bits_to_f32(case.q)).max())
+        case = dataclasses.replace(case, q_scale=float(np.float32(amax / 448.0)))
+    g = H.GpuCase(case)
+    items = g.plan.items()
+    assert all(it["kind"] == 1 for it in items)
+    assert any(it["n_q"] > tq for it in items), "no item holds two query tiles"
+    g.write_prefix()
+    g.run()
+    assert g.status() == 0, g.pkv.last_error()
+    ref = oracle.forward(case)
+    H.compare_out(g.out, ref["out"], H.FP8_TOL)
+    H.compare_lse(g.lse, ref["lse"])
+    assert np.array_equal(H.to_numpy_bits(g.k_cache), ref["k_cache"]), "k cache differs"
+
+
 @pytest.mark.parametrize("P,G,causal,mixed", [(16, 4, True, False), (0, 4, False, False), (16, 8, True, True),
                                               (32, 2, True, False)])
 def test_fp8_quantised_queries_prefill(P, G, causal, mixed):
