@@ -115,9 +115,15 @@ struct Layout {
   static constexpr uint32_t kTmemO = kSBufs * kTile;
   static_assert((kQQ ? kQCols * kQTiles : kTmemO + D) <= kTmemCols && (!kQQ || kTmemO + D <= kQCols),
                 "tensor memory budget");
-  // decode-only plans give all shared memory to the rings
-  static constexpr int kStagesK = PF ? (FP8 ? 2 : (D == 64 ? 4 : kQQ ? 2 : 3)) : (FP8 || D == 64 ? 6 : 4);
-  static constexpr int kStagesV = PF ? (FP8 ? 2 : (D == 64 ? 4 : D == 256 || kQQ ? 2 : 3)) : (FP8 || D == 64 ? 6 : 3);
+  // decode-only plans give all shared memory to the rings; over an fp8 cache
+  // at D <= 128 two CTAs share an SM (each with 3 + 3 stages of 16 KB, the
+  // same bytes in flight as one CTA with 6 + 6): twice the decode warps to
+  // hide the per-tile chain of conversions, warp MMAs and softmax
+  static constexpr int kCtasPerSm = (FP8 && !PF && D <= 128) ? 2 : 1;
+  static constexpr int kStagesK =
+      PF ? (FP8 ? 2 : (D == 64 ? 4 : kQQ ? 2 : 3)) : (kCtasPerSm == 2 ? 3 : (FP8 || D == 64 ? 6 : 4));
+  static constexpr int kStagesV =
+      PF ? (FP8 ? 2 : (D == 64 ? 4 : D == 256 || kQQ ? 2 : 3)) : (kCtasPerSm == 2 ? 3 : (FP8 || D == 64 ? 6 : 3));
   static constexpr int kTileBytes = kTile * D * kEsize;     // one raw K (or V) tile
   // A raw tile is [column chunks][128 rows][kRowBytes]: 128-byte chunks with
   // the 128-byte swizzle, or (an fp8 cache at D = 64) one chunk of 64-byte
@@ -1877,7 +1883,7 @@ __device__ bool consumer(const AttnParams& p, uint8_t* smem, const Bars& B, vola
 // otherwise weigh on the softmax path (measured: 133 -> 123 us on the
 // cached-prefix prefill batch).
 template <int D, bool FP8, bool PF, bool QF8, bool DEC>
-__global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, 1)
+__global__ void __launch_bounds__(Layout<D, FP8, PF>::kThreads, Layout<D, FP8, PF>::kCtasPerSm)
     attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q) {
   using L = Layout<D, FP8, PF>;
@@ -2070,6 +2076,8 @@ cudaError_t launch_t(const AttnParams& p, const CUtensorMap& tk, const CUtensorM
                      int num_ctas, bool overlap_prev, cudaStream_t s) {
   using L = Layout<D, FP8, PF>;
   static_assert(L::kAlloc <= 232448, "shared memory budget");
+  // (two CTAs an SM: both fit the SM's 228 KB with the 1 KB each reserves)
+  static_assert(L::kCtasPerSm == 1 || L::kCtasPerSm * (L::kAlloc + 1024) <= 233472, "two CTAs an SM");
   // once per device (kept out of the launch path, so the call can be captured in a graph)
   static std::atomic<uint64_t> configured{0};
   int dev = 0;

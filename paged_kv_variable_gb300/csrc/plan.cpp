@@ -241,7 +241,10 @@ pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const 
   // CTA index), found with a tournament tree over the CTAs' (load, index)
   // pairs; each CTA keeps its items in the order they were assigned
   const int num_items = (int)tiles.size();
-  const int num_ctas = std::max(1, std::min(num_sms, num_items));
+  // (decode-only plans over an fp8 cache at head dims up to 128 run two CTAs
+  // an SM)
+  const int cps = (p.cache_dtype == PKV_FP8_E4M3 && D <= 128 && n_pre == 0) ? 2 : 1;
+  const int num_ctas = std::max(1, std::min(num_sms * cps, num_items));
   std::vector<double> costs(num_items);
   for (int i = 0; i < num_items; ++i) costs[i] = tiles[i].cost;
   std::vector<int> order(num_items);
