@@ -364,17 +364,36 @@ def e2e_decode(case, steps, warmup, device, mode="graph"):
     import paged_kv_variable_gb300 as pkv
     g = H.GpuCase(case, device=device)
     spec = case.spec
-    host = {
-        "q": torch.from_numpy(case.q.view(np.int16)).view(torch.bfloat16).pin_memory(),
-        "k_new": torch.from_numpy(case.k_new.view(np.int16)).view(torch.bfloat16).pin_memory(),
-        "v_new": torch.from_numpy(case.v_new.view(np.int16)).view(torch.bfloat16).pin_memory(),
-        "cu_q": torch.from_numpy(spec.cu_q).pin_memory(),
-        "cu_new": torch.from_numpy(spec.cu_new).pin_memory(),
-        "lens": torch.from_numpy(spec.cache_lens).pin_memory(),
+    # the step's inputs (q, new K/V, cu_seqlens, lengths) sit in one pinned host
+    # buffer and one device buffer, 256-byte aligned segments of each: one
+    # host -> device copy a step, the call's arguments pointing into the device
+    # buffer
+    src = {
+        "q": torch.from_numpy(case.q.view(np.int16)).view(torch.bfloat16),
+        "k_new": torch.from_numpy(case.k_new.view(np.int16)).view(torch.bfloat16),
+        "v_new": torch.from_numpy(case.v_new.view(np.int16)).view(torch.bfloat16),
+        "cu_q": torch.from_numpy(np.ascontiguousarray(spec.cu_q, dtype=np.int32)),
+        "cu_new": torch.from_numpy(np.ascontiguousarray(spec.cu_new, dtype=np.int32)),
+        "lens": torch.from_numpy(np.ascontiguousarray(spec.cache_lens, dtype=np.int32)),
     }
+    offs, off = {}, 0
+    for k, t in src.items():
+        offs[k] = off
+        off += (t.numel() * t.element_size() + 255) // 256 * 256
+    hpack = torch.empty(off, dtype=torch.uint8).pin_memory()
+    dpack = torch.empty(off, dtype=torch.uint8, device=device)
+
+    def seg(buf, k):
+        t = src[k]
+        return buf[offs[k]:offs[k] + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+
+    for k, t in src.items():
+        seg(hpack, k).copy_(t)
+    g.q, g.k_new, g.v_new = seg(dpack, "q"), seg(dpack, "k_new"), seg(dpack, "v_new")
+    g.cu_q, g.cu_new, g.cache_lens = seg(dpack, "cu_q"), seg(dpack, "cu_new"), seg(dpack, "lens")
+    dpack.copy_(hpack)
     out_h = torch.empty(g.out.shape, dtype=torch.bfloat16).pin_memory()
-    dev = {"q": g.q, "k_new": g.k_new, "v_new": g.v_new, "cu_q": g.cu_q, "cu_new": g.cu_new, "lens": g.cache_lens}
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = hpack.numel()
     d2h = out_h.numel() * out_h.element_size()
     nsms = torch.cuda.get_device_properties(device).multi_processor_count
     stream = torch.cuda.current_stream()
@@ -398,16 +417,14 @@ def e2e_decode(case, steps, warmup, device, mode="graph"):
         torch.cuda.synchronize()
 
         def one():
-            for k in host:
-                dev[k].copy_(host[k], non_blocking=True)
+            dpack.copy_(hpack, non_blocking=True)
             graph.replay()
             out_h.copy_(g.out, non_blocking=True)
             stream.synchronize()
     else:
         def one():
             pl = pkv.plan(g.problem, spec.q_lens, spec.cache_lens, spec.new_lens, nsms)
-            for k in host:
-                dev[k].copy_(host[k], non_blocking=True)
+            dpack.copy_(hpack, non_blocking=True)
             pl.upload(g.workspace)
             pkv.attn_varlen_kvcache_fwd(g.problem, g.args(), pl, g.workspace)
             out_h.copy_(g.out, non_blocking=True)
