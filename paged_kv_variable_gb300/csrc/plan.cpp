@@ -107,9 +107,14 @@ pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const 
   auto splittable = [&](int lq) { return is_decode(lq) || lq <= tq_prefill; };
   // an item of a long query run holds up to two consecutive tiles (fp8 cache,
   // head dims up to 128; plans without decode tiles), which share its K/V tiles
-  bool any_decode = false;
-  for (int b = 0; b < B; ++b) any_decode |= h_q_lens[b] > 0 && is_decode(h_q_lens[b]);
+  bool any_decode = false, any_prefill = false;
+  for (int b = 0; b < B; ++b) {
+    any_decode |= h_q_lens[b] > 0 && is_decode(h_q_lens[b]);
+    any_prefill |= h_q_lens[b] > 0 && !is_decode(h_q_lens[b]);
+  }
   const int tq_item = tq_prefill * (any_decode ? 1 : prefill_q_tiles(D, p.cache_dtype == PKV_FP8_E4M3));
+  // decode-only plans over an fp8 cache at head dims up to 128 run two CTAs an SM
+  const bool two_ctas = p.cache_dtype == PKV_FP8_E4M3 && D <= 128 && !any_prefill;
 
   int64_t total_q = 0, total_new = 0, total_split_keys = 0;
   for (int b = 0; b < B; ++b) {
@@ -130,10 +135,13 @@ pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const 
   if (total_q > INT32_MAX / 2 || total_new > INT32_MAX / 2)
     return fail(PKV_ERR_UNSUPPORTED, "total tokens too large");
 
-  // split-KV chunk: at least 4 splittable items per CTA, chunks >= 512 keys
+  // split-KV chunk: at least 4 splittable items per SM (2 where two CTAs share
+  // an SM: their items share its bandwidth, and fewer splits measured faster
+  // there -- 59.1 against 60.9 us on the fp8 decode batch, 61.7 against 64.9
+  // on one of random lengths), chunks >= 512 keys
   int64_t chunk = 1 << 30;
   if (total_split_keys > 0) {
-    int64_t target = 4LL * num_sms;
+    int64_t target = (two_ctas ? 2LL : 4LL) * num_sms;
     chunk = (total_split_keys + target - 1) / target;
     chunk = std::max<int64_t>(512, (chunk + kKvTile - 1) / kKvTile * kKvTile);
   }
@@ -244,9 +252,7 @@ pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const 
   // CTA index), found with a tournament tree over the CTAs' (load, index)
   // pairs; each CTA keeps its items in the order they were assigned
   const int num_items = (int)tiles.size();
-  // (decode-only plans over an fp8 cache at head dims up to 128 run two CTAs
-  // an SM)
-  const int cps = (p.cache_dtype == PKV_FP8_E4M3 && D <= 128 && n_pre == 0) ? 2 : 1;
+  const int cps = two_ctas ? 2 : 1;
   const int num_ctas = std::max(1, std::min(num_sms * cps, num_items));
   std::vector<double> costs(num_items);
   for (int i = 0; i < num_items; ++i) costs[i] = tiles[i].cost;

@@ -707,7 +707,8 @@ def test_small_pages_decode(P, cache_dtype):
     spec = synth.uniform_spec("small-page-decode", 6, 1, 2500, hq=16, hkv=4, d=128, page_size=P,
                               cache_dtype=cache_dtype)
     case = synth.make_case(spec, rng)
-    g = H.GpuCase(case, num_sms=8)
+    # (decode-only fp8 plans aim at half the items an SM: more SMs to split)
+    g = H.GpuCase(case, num_sms=16 if cache_dtype == "fp8" else 8)
     assert g.plan.stats()["num_split_units"] > 0
     g.write_prefix()
     g.run()
@@ -728,7 +729,7 @@ def test_fp8_quantised_queries_decode(P, G, split):
     case = synth.make_case(spec, rng)
     amax = float(np.abs(synth.bf16_bits_to_f32(case.q)).max())
     case = dataclasses.replace(case, q_scale=float(np.float32(amax / 448.0)))
-    g = H.GpuCase(case, num_sms=4 if split else 152)
+    g = H.GpuCase(case, num_sms=8 if split else 152)
     assert (g.plan.stats()["num_split_units"] > 0) == split
     g.write_prefix()
     g.run()                                          # q_scale goes in with the other arguments
