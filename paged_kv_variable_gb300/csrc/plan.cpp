@@ -135,13 +135,15 @@ pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const 
   if (total_q > INT32_MAX / 2 || total_new > INT32_MAX / 2)
     return fail(PKV_ERR_UNSUPPORTED, "total tokens too large");
 
-  // split-KV chunk: at least 4 splittable items per SM (2 where two CTAs share
-  // an SM: their items share its bandwidth, and fewer splits measured faster
-  // there -- 59.1 against 60.9 us on the fp8 decode batch, 61.7 against 64.9
-  // on one of random lengths), chunks >= 512 keys
+  // split-KV chunk: at least 2 splittable items per SM in decode-only plans, 4
+  // when prefill tiles share the launch (their gaps want finer decode items),
+  // chunks >= 512 keys.  Measured: the fp8 decode batch (two CTAs an SM) 59.1
+  // against 60.9 us at 4, one of random lengths 61.7 against 64.9; the bf16
+  // decode batch the same attention kernel and 100.4 against 101.8 us a call
+  // (fewer partials to combine); the mixed batch 0.417 against 0.430 ms at 4.
   int64_t chunk = 1 << 30;
   if (total_split_keys > 0) {
-    int64_t target = (two_ctas ? 2LL : 4LL) * num_sms;
+    int64_t target = (any_prefill ? 4LL : 2LL) * num_sms;
     chunk = (total_split_keys + target - 1) / target;
     chunk = std::max<int64_t>(512, (chunk + kKvTile - 1) / kKvTile * kKvTile);
   }

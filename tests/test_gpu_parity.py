@@ -707,8 +707,8 @@ def test_small_pages_decode(P, cache_dtype):
     spec = synth.uniform_spec("small-page-decode", 6, 1, 2500, hq=16, hkv=4, d=128, page_size=P,
                               cache_dtype=cache_dtype)
     case = synth.make_case(spec, rng)
-    # (decode-only fp8 plans aim at half the items an SM: more SMs to split)
-    g = H.GpuCase(case, num_sms=16 if cache_dtype == "fp8" else 8)
+    # (decode-only plans aim at two items an SM: 16 SMs to have them split)
+    g = H.GpuCase(case, num_sms=16)
     assert g.plan.stats()["num_split_units"] > 0
     g.write_prefix()
     g.run()
