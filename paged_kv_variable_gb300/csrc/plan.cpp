@@ -115,6 +115,7 @@ pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const 
   const int tq_item = tq_prefill * (any_decode ? 1 : prefill_q_tiles(D, p.cache_dtype == PKV_FP8_E4M3));
   // decode-only plans over an fp8 cache at head dims up to 128 run two CTAs an SM
   const bool two_ctas = p.cache_dtype == PKV_FP8_E4M3 && D <= 128 && !any_prefill;
+  const int cps = two_ctas ? 2 : 1;
 
   int64_t total_q = 0, total_new = 0, total_split_keys = 0;
   for (int b = 0; b < B; ++b) {
@@ -141,11 +142,42 @@ pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const 
   // against 60.9 us at 4, one of random lengths 61.7 against 64.9; the bf16
   // decode batch the same attention kernel and 100.4 against 101.8 us a call
   // (fewer partials to combine); the mixed batch 0.417 against 0.430 ms at 4.
+  auto chunk_for = [&](int64_t items_per_sm) {
+    const int64_t target = items_per_sm * num_sms;
+    const int64_t c = (total_split_keys + target - 1) / target;
+    return std::max<int64_t>(512, (c + kKvTile - 1) / kKvTile * kKvTile);
+  };
   int64_t chunk = 1 << 30;
-  if (total_split_keys > 0) {
-    int64_t target = (any_prefill ? 4LL : 2LL) * num_sms;
-    chunk = (total_split_keys + target - 1) / target;
-    chunk = std::max<int64_t>(512, (chunk + kKvTile - 1) / kKvTile * kKvTile);
+  if (total_split_keys > 0) chunk = chunk_for(any_prefill ? 4 : 2);
+  // A decode-only plan whose units are placed as evenly whole (one item an SM
+  // as the target) as in chunks of the half is not split at all: no partials
+  // and no combine kernel (the bf16 decode batch: 98.1 against 100.3 us a
+  // call, the same attention kernel).  Judged on the model costs of a
+  // longest-first placement; batches with a few long sequences stay split.
+  if (!any_prefill && total_split_keys > 0) {
+    const int ctas = num_sms * cps;
+    auto busiest = [&](int64_t ch) {  // the longest-first placement's largest CTA cost
+      std::vector<double> c;
+      for (int b = 0; b < B; ++b) {
+        if (h_q_lens[b] == 0) continue;
+        const int lk = h_cache_lens[b] + (h_new_lens ? h_new_lens[b] : 0);
+        const int n = lk <= ch ? 1 : (int)((lk + ch - 1) / ch);
+        for (int k = 0; k < n; ++k) {
+          const int keys = (int)(std::min<int64_t>((int64_t)(k + 1) * ch, lk) - std::min<int64_t>((int64_t)k * ch, lk));
+          for (int hk = 0; hk < p.num_heads_kv; ++hk) c.push_back(decode_cost(keys, D, esize));
+        }
+      }
+      std::sort(c.begin(), c.end(), std::greater<double>());
+      std::vector<double> load(ctas, 0.0);  // a min-heap over the CTA loads
+      for (double x : c) {
+        std::pop_heap(load.begin(), load.end(), std::greater<double>());
+        load.back() += x;
+        std::push_heap(load.begin(), load.end(), std::greater<double>());
+      }
+      return *std::max_element(load.begin(), load.end());
+    };
+    const int64_t whole = chunk_for(1);
+    if (whole != chunk && busiest(whole) <= 1.02 * busiest(chunk)) chunk = whole;
   }
   auto nchunks_of = [&](int lk) { return lk <= chunk ? 1 : (int)((lk + chunk - 1) / chunk); };
 
@@ -254,7 +286,6 @@ pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const 
   // CTA index), found with a tournament tree over the CTAs' (load, index)
   // pairs; each CTA keeps its items in the order they were assigned
   const int num_items = (int)tiles.size();
-  const int cps = two_ctas ? 2 : 1;
   const int num_ctas = std::max(1, std::min(num_sms * cps, num_items));
   std::vector<double> costs(num_items);
   for (int i = 0; i < num_items; ++i) costs[i] = tiles[i].cost;
