@@ -374,3 +374,30 @@ def test_two_query_tile_items_only_for_fp8_prefill_plans(pkv):
     assert not any(it["n_q"] > tq for it in items("fp8", 256, [300, 70]))
     mixed = items("fp8", 128, [300, 1])
     assert any(it["kind"] == 0 for it in mixed) and not any(it["n_q"] > tq for it in mixed)
+
+
+def test_decode_only_split_policy(pkv):
+    """Decode-only plans: units that balance as well placed whole (within 2%
+    of the split placement, on the planner's costs) are not split, so no
+    combine runs; a batch with a few long sequences is still split; a plan
+    with prefill tiles splits its decode units finer (four items an SM); an
+    fp8 cache at head_dim <= 128 runs two CTAs an SM."""
+    def plan(dtype, q_lens, lc):
+        B = len(lc)
+        prob = pkv.make_problem(batch=B, num_heads_q=32, num_heads_kv=8, head_dim=128, page_size=16,
+                                cache_capacity=65552, num_pages=200000, cache_dtype=dtype, causal=True,
+                                softmax_scale=0.088)
+        q = np.asarray(q_lens, np.int32)
+        return pkv.plan(prob, q, np.asarray(lc, np.int32), q, num_sms=152).stats()
+    rng = np.random.default_rng(5)
+    lc = rng.integers(512, 4097, 64)
+    even = plan("bf16", [1] * 64, lc)
+    assert even["num_split_units"] == 0 and even["num_items"] == 64 * 8 and even["num_ctas"] == 152
+    skewed = plan("bf16", [1] * 64, [65536] * 8 + [1024] * 56)
+    assert skewed["num_split_units"] > 0
+    assert skewed["max_cta_cost"] <= 1.1 * skewed["mean_cta_cost"]
+    fp8 = plan("fp8", [1] * 64, [2048] * 64)
+    assert fp8["num_ctas"] == 2 * 152 and fp8["num_split_units"] == 0
+    # one prefill request in the batch: the decode units are cut for four items an SM
+    mixed = plan("bf16", [1] * 63 + [512], list(lc[:63]) + [1000])
+    assert mixed["num_prefill_items"] > 0 and mixed["num_split_units"] > 0 and mixed["num_ctas"] == 152
