@@ -802,3 +802,29 @@ def test_fp8_quantised_queries_prefill(P, G, causal, mixed):
     H.compare_lse(g.lse, ref["lse"])
     assert np.array_equal(H.to_numpy_bits(g.k_cache), ref["k_cache"]), "k cache differs"
 
+
+
+@pytest.mark.parametrize("dtype,sms,q8", [("fp8", 152, False), ("fp8", 12, False), ("fp8", 152, True),
+                                          ("bf16", 152, False), ("bf16", 8, False)])
+def test_decode_random_lengths_whole_and_split(dtype, sms, q8):
+    """Decode batches of random lengths U[512, 4096] with the full GQA shape
+    (Hq=32, Hkv=8, D=128, pages of 16, poisoned unused slots): at a few SMs
+    the planner places the 192 units whole (no partials, no combine), at 152
+    SMs (two CTAs an SM over an fp8 cache) it splits them to fill the CTAs;
+    every row against the oracle, the cache byte for byte."""
+    import dataclasses
+    rng = np.random.default_rng(7100 + sms + (1 if q8 else 0))
+    B = 24
+    lc = rng.integers(512, 4097, B).astype(np.int32)
+    ones = np.ones(B, np.int32)
+    spec = synth.Spec(batch=B, hq=32, hkv=8, d=128, page_size=16, causal=True,
+                      softmax_scale=float(np.float32(1.0 / np.sqrt(128))), cache_dtype=dtype, q_lens=ones,
+                      cache_lens=lc, new_lens=ones.copy(), capacity=4112, name="decode-rand")
+    case = synth.make_case(spec, rng, sentinel="nan")
+    if q8:
+        amax = float(np.abs(synth.bf16_bits_to_f32(case.q)).max())
+        case = dataclasses.replace(case, q_scale=float(np.float32(amax / 448.0)))
+    g, _ = run_full(case, num_sms=sms)
+    st = g.plan.stats()
+    assert (st["num_split_units"] > 0) == (sms == 152)
+    assert st["num_ctas"] == sms * (2 if dtype == "fp8" else 1)
