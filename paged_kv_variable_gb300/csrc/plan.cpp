@@ -156,24 +156,26 @@ pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const 
   // longest-first placement; batches with a few long sequences stay split.
   if (!any_prefill && total_split_keys > 0) {
     const int ctas = num_sms * cps;
+    std::vector<double> c, load;
+    c.reserve((size_t)B * 4);
+    load.reserve((size_t)ctas);
     auto busiest = [&](int64_t ch) {  // the longest-first placement's largest CTA cost
-      std::vector<double> c;
-      for (int b = 0; b < B; ++b) {
+      c.clear();
+      for (int b = 0; b < B; ++b) {  // one cost per chunk; every kv head has the same
         if (h_q_lens[b] == 0) continue;
         const int lk = h_cache_lens[b] + (h_new_lens ? h_new_lens[b] : 0);
         const int n = lk <= ch ? 1 : (int)((lk + ch - 1) / ch);
-        for (int k = 0; k < n; ++k) {
-          const int keys = (int)(std::min<int64_t>((int64_t)(k + 1) * ch, lk) - std::min<int64_t>((int64_t)k * ch, lk));
-          for (int hk = 0; hk < p.num_heads_kv; ++hk) c.push_back(decode_cost(keys, D, esize));
-        }
+        for (int k = 0; k < n; ++k)
+          c.push_back(decode_cost((int)(std::min<int64_t>((int64_t)(k + 1) * ch, lk) - (int64_t)k * ch), D, esize));
       }
       std::sort(c.begin(), c.end(), std::greater<double>());
-      std::vector<double> load(ctas, 0.0);  // a min-heap over the CTA loads
-      for (double x : c) {
-        std::pop_heap(load.begin(), load.end(), std::greater<double>());
-        load.back() += x;
-        std::push_heap(load.begin(), load.end(), std::greater<double>());
-      }
+      load.assign((size_t)ctas, 0.0);  // a min-heap over the CTA loads
+      for (double x : c)
+        for (int hk = 0; hk < p.num_heads_kv; ++hk) {
+          std::pop_heap(load.begin(), load.end(), std::greater<double>());
+          load.back() += x;
+          std::push_heap(load.begin(), load.end(), std::greater<double>());
+        }
       return *std::max_element(load.begin(), load.end());
     };
     const int64_t whole = chunk_for(1);
