@@ -519,6 +519,48 @@ def cpu_oracle_leg(budget_s=12.0):
                               "sample": f"{one['sequences']} sequences in {one['seconds']:.1f} s, median of 3"}}
 
 
+def decode_variant(d=128, page_size=16):
+    """The decode batch (B=64, one query and one appended token each, Hq=32,
+    Hkv=8, cache lengths U[512,4096], the same seed, so the same lengths) at
+    another head dim or page size."""
+    import math
+    rng = np.random.Generator(np.random.PCG64(1002))
+    B = 64
+    lc = rng.integers(512, 4096, size=B, endpoint=True).astype(np.int32)
+    ones = np.ones(B, np.int32)
+    width = (4097 + page_size - 1) // page_size
+    spec = synth.Spec(batch=B, hq=32, hkv=8, d=d, page_size=page_size, causal=True,
+                      softmax_scale=float(np.float32(1.0 / math.sqrt(d))), cache_dtype="bf16", q_lens=ones,
+                      cache_lens=lc, new_lens=ones.copy(), capacity=width * page_size,
+                      name=f"decode-d{d}-p{page_size}")
+    return synth.make_case(spec, rng, block_table_width=width)
+
+
+def use_ragged_page_list(wl):
+    """Address the workload's paged cache through a ragged page list (each
+    sequence's used pages concatenated, page_indptr offsets) in place of the
+    padded block table."""
+    import torch
+    case, g = wl.case, wl.g
+    spec = case.spec
+    P = spec.page_size
+    counts = [(int(n) + P - 1) // P for n in spec.kv_lens]
+    flat = np.concatenate([case.block_table[b, :counts[b]] for b in range(spec.batch)]).astype(np.int32)
+    indptr = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    flat_t = torch.from_numpy(flat).to(g.q.device)
+    indptr_t = torch.from_numpy(indptr).to(g.q.device)
+
+    def args(with_new=True):
+        return g.pkv.make_args(q=g.q, out=g.out, lse=g.lse, cu_seqlens_q=g.cu_q,
+                               max_seqlen_q=int(spec.q_lens.max()), k_cache=g.k_cache, v_cache=g.v_cache,
+                               cache_seqlens=g.cache_lens, k_new=g.k_new if with_new else None,
+                               v_new=g.v_new if with_new else None,
+                               cu_seqlens_knew=g.cu_new if with_new else None, block_table=flat_t,
+                               page_indptr=indptr_t)
+    g.args = args
+    return wl
+
+
 def with_q_scale(case):
     """The fp8 workload with quantised queries: per-tensor q_scale = amax(|q|)/448
     (fp32), the same rule as the cache scales."""
@@ -607,11 +649,17 @@ def gpu_arm(args):
                      ("mixed_prefill_decode", synth.config4, "mixed"),
                      ("fp8_prefill", lambda: synth.config5()[0], "tensor"),
                      ("fp8_prefill_quantised_q", lambda: with_q_scale(synth.config5()[0]), "fp8tensor"),
-                     ("fp8_decode", lambda: synth.config5()[1], "hbm")]
+                     ("fp8_decode", lambda: synth.config5()[1], "hbm"),
+                     ("decode_head_dim_64", lambda: decode_variant(d=64), "hbm"),
+                     ("decode_head_dim_256", lambda: decode_variant(d=256), "hbm"),
+                     ("decode_page_size_4", lambda: decode_variant(page_size=4), "hbm"),
+                     ("decode_ragged_page_list", synth.config2, "hbm")]
         n_sec = max(30, args.steps)
         for name, mk, bound in secondary:
             case = mk()
             wl = Workload(name, case, device)
+            if name == "decode_ragged_page_list":
+                use_ragged_page_list(wl)
             if name == "fp8_decode":
                 pre = Workload("fp8_prefill_for_decode", synth.config5()[0], device)
                 pre.step()
