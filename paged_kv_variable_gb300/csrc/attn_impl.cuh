@@ -265,28 +265,21 @@ struct Ring {
   }
 };
 
-// ------------------------------------------------------------------ producers
-// Two producer warps, one per ring: warp 0 loads Q tiles and K tiles, the V
-// producer warp loads V tiles, each as soon as a stage of its own ring is
-// free.  The whole warp issues: lane l owns box (l % boxes) of 128-byte column
-// chunk (l / boxes) of every tile, where a tile of 128 keys is `boxes` boxes
-// of box_rows cache rows (128 for a contiguous cache, the largest power of two
-// dividing the page size for a paged one).
-//
-// Within an item no global load sits between a free stage and its copy:
-// block_table entries are read one warp-wide load per group of 32 / boxes
-// tiles (lane l: box l % boxes of tile l / boxes of the group), a group ahead
-// of its use.  (Loading the next item's descriptor ahead as well measured
-// slower on prefill plans.)
 // Row gather of one tile (pages of P = 1, 2 or 4 tokens): lane l copies rows
 // l, l+32, l+64, l+96 in 16-byte cp.async pieces into the swizzled layout
 // (rows past the key range become zeros).  Row r's page is entry r / P of the
 // tile, held by lane (r / P) % 32 in ent[(r / P) / 32] = ent[i / P]; pages of
 // one token: each lane loads its rows' entries itself (those loads are
-// coalesced already; the shuffled form measured slower there).
+// coalesced already; the shuffled form measured slower).  Decode-only
+// instances: the producers of instances with prefill tiles run on few
+// registers and keep a simpler form.
+template <int N>
+struct PageEntries {
+  int v[N];
+};
 template <class L, bool kIsV, int P>
 __device__ __forceinline__ void gather_rows(const AttnParams& p, const WorkItem& w, int t0, uint8_t* stage,
-                                            const int (&ent)[L::kTile / 32]) {
+                                            PageEntries<L::kTile / 32> ent) {
   constexpr int kTile = L::kTile;
   constexpr int kPieces = L::kD * L::kEsize / 16;  // 16-byte pieces of a cache row
   const int lane = threadIdx.x & 31;
@@ -300,7 +293,7 @@ __device__ __forceinline__ void gather_rows(const AttnParams& p, const WorkItem&
       const int32_t* pages = seq_pages(p.block_table, p.bt_stride, p.page_indptr, w.b, &npages);
       pg = (j >= w.kv_end || (npages >= 0 && j >= npages)) ? -1 : __ldg(pages + j);
     } else {
-      pg = __shfl_sync(0xffffffffu, ent[i / P], (r / P) & 31);
+      pg = __shfl_sync(0xffffffffu, ent.v[i / P], (r / P) & 31);
     }
     const uint8_t* src = base;
     uint32_t bytes = 0;
@@ -320,6 +313,19 @@ __device__ __forceinline__ void gather_rows(const AttnParams& p, const WorkItem&
   cp_async_commit();
 }
 
+// ------------------------------------------------------------------ producers
+// Two producer warps, one per ring: warp 0 loads Q tiles and K tiles, the V
+// producer warp loads V tiles, each as soon as a stage of its own ring is
+// free.  The whole warp issues: lane l owns box (l % boxes) of 128-byte column
+// chunk (l / boxes) of every tile, where a tile of 128 keys is `boxes` boxes
+// of box_rows cache rows (128 for a contiguous cache, the largest power of two
+// dividing the page size for a paged one).
+//
+// Within an item no global load sits between a free stage and its copy:
+// block_table entries are read one warp-wide load per group of 32 / boxes
+// tiles (lane l: box l % boxes of tile l / boxes of the group), a group ahead
+// of its use.  (Loading the next item's descriptor ahead as well measured
+// slower on prefill plans.)
 template <int D, bool FP8, bool PF, bool kIsV>
 __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CUtensorMap* tm_q, uint8_t* smem,
                          const Bars& B, volatile int* abort_flag, int it0, int it1) {
@@ -351,13 +357,17 @@ __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CU
     return (npages >= 0 && pgi >= npages) ? -1 : __ldg(pages + pgi);
   };
 
+  // (decode-only instances; instances with prefill tiles, whose producers run
+  // on few registers, look the pages up row by row)
+  constexpr bool kEnt = !PF;
   // Row gather (pages of 1, 2 or 4 tokens): the tile's page numbers, one a
   // page (kTile / page_size of them), come from one coalesced load, lane e
   // holding entries e, e + 32, ... (-1 past the sequence's page list), taken
   // a tile ahead of the copies that use them (pages of 2 and 4 tokens: 0.25 ->
   // 0.20 ms on the decode batch, where each lane had loaded its rows' entries
   // as it copied them).
-  auto load_entries = [&](const WorkItem& w, int t0, int (&ent)[kTile / 32]) {
+  auto load_entries = [&](const WorkItem& w, int t0) {
+    PageEntries<kTile / 32> ent;
     int npages;
     const int32_t* pages = seq_pages(p.block_table, p.bt_stride, p.page_indptr, w.b, &npages);
     const int E = kTile / p.page_size;
@@ -365,11 +375,42 @@ __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CU
     for (int k = 0; k < kTile / 32; ++k) {
       const int e = lane + 32 * k;
       const int pgi = t0 / p.page_size + e;
-      ent[k] = (e < E && pgi * p.page_size < w.kv_end && !(npages >= 0 && pgi >= npages)) ? __ldg(pages + pgi) : -1;
+      ent.v[k] = (e < E && pgi * p.page_size < w.kv_end && !(npages >= 0 && pgi >= npages)) ? __ldg(pages + pgi) : -1;
     }
+    return ent;
   };
-  // A gathered tile is marked full once its copies have landed, which is
-  // checked when the next tile has been issued (or at the end).
+  // Row gather in instances with prefill tiles: lane l copies rows l, l+32,
+  // l+64, l+96 of a tile in 16-byte cp.async pieces into the swizzled layout
+  // (rows past the key range become zeros), looking each row's page up as it
+  // goes.  A gathered tile is marked full once its copies have landed, which
+  // is checked when the next tile has been issued (or at the end).
+  auto gather_tile = [&](const WorkItem& w, int t0, uint8_t* stage) {
+    const uint8_t* base = static_cast<const uint8_t*>(kIsV ? p.vc : p.kc);
+    constexpr int kPieces = D * L::kEsize / 16;  // 16-byte pieces of a cache row
+#pragma unroll
+    for (int i = 0; i < kTile / 32; ++i) {
+      const int r = lane + 32 * i, j = t0 + r;
+      const uint8_t* src = base;
+      uint32_t bytes = 0;
+      if (j < w.kv_end) {
+        int npages;
+        const int32_t* pages = seq_pages(p.block_table, p.bt_stride, p.page_indptr, w.b, &npages);
+        const int pgi = j / p.page_size;
+        const int pg = (npages >= 0 && pgi >= npages) ? -1 : __ldg(pages + pgi);
+        if (pg < 0 || pg >= p.num_pages) {
+          if (!kIsV) record_status(p.status, PKV_ERR_DEVICE_BOUNDS, w.b, pg);
+        } else {
+          src = base + ((int64_t)pg * p.c_stride_page + (int64_t)(j % p.page_size) * p.c_stride_tok +
+                        (int64_t)w.hk * p.c_stride_head) * L::kEsize;
+          bytes = 16;
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < kPieces; ++c)
+        cp_async_16(stage + raw_off<L::kRowBytes, kTile>(r, c), src + (bytes ? c * 16 : 0), bytes);
+    }
+    cp_async_commit();
+  };
   int pend = -1;  // row gather: stage whose copies are in flight, not yet marked full
   auto mark_full = [&](int stage) {
     fence_proxy_async_smem();  // the copies (generic proxy) before tensor-core reads of the stage
@@ -404,8 +445,8 @@ __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CU
     int gcur = load_pages(w, w.kv_begin);
     int t0g = w.kv_begin;
     int gnext = load_pages(w, t0g + per * kTile);
-    int ent[kTile / 32] = {};  // row gather: the page numbers of the next tile to copy
-    if (rows && p.page_size > 1) load_entries(w, w.kv_begin, ent);
+    PageEntries<kTile / 32> ent{};  // row gather: the page numbers of the next tile to copy
+    if (kEnt && rows && p.page_size > 1) ent = load_entries(w, w.kv_begin);
     if (!kIsV && L::kTc && w.kind == kPrefill && num_tiles<L::kTile>(w) > 0) {
       // Row gather: the last tile of the previous item is still unmarked (a
       // tile is marked once the next one has been issued), and the Q buffer
@@ -474,10 +515,12 @@ __device__ void producer(const AttnParams& p, const CUtensorMap* tm_kv, const CU
       }
       if (rows) {
         uint8_t* stage = ring_base + ring.stage * L::kTileBytes;
-        if (p.page_size == 1) gather_rows<L, kIsV, 1>(p, w, t0, stage, ent);
+        if constexpr (!kEnt) gather_tile(w, t0, stage);
+        else if (p.page_size == 1) gather_rows<L, kIsV, 1>(p, w, t0, stage, ent);
         else if (p.page_size == 2) gather_rows<L, kIsV, 2>(p, w, t0, stage, ent);
         else gather_rows<L, kIsV, 4>(p, w, t0, stage, ent);
-        if (p.page_size > 1 && t0 + kTile < w.kv_end) load_entries(w, t0 + kTile, ent);  // in flight during the wait below
+        if (kEnt && p.page_size > 1 && t0 + kTile < w.kv_end)
+          ent = load_entries(w, t0 + kTile);  // in flight during the wait below
         if (pend >= 0) {
           cp_async_wait_group<1>();  // all but the tile just issued have landed
           mark_full(pend);
