@@ -167,8 +167,8 @@ typedef struct {
  * query runs) into KV chunks (split-KV, flash-attention PR, Limitation), and
  * assigns all tiles to persistent CTAs longest first: num_sms of them (the
  * GPU's SM count), or 2 * num_sms for a plan of decode tiles only over an fp8
- * cache at head_dim <= 128, whose kernel runs two CTAs an SM (the plan's
- * stats report the count).
+ * cache at head_dim <= 128 or a bf16 cache at head_dim 64, whose kernel runs
+ * two CTAs an SM (the plan's stats report the count).
  * h_q_lens / h_cache_lens / h_new_lens: host int32 [B]; h_new_lens may be NULL
  * when the call appends nothing.  Zero lengths are accepted.  On success
  * *out_plan owns a host work list and *out_workspace_bytes is the device

@@ -116,10 +116,12 @@ struct Layout {
   static_assert((kQQ ? kQCols * kQTiles : kTmemO + D) <= kTmemCols && (!kQQ || kTmemO + D <= kQCols),
                 "tensor memory budget");
   // decode-only plans give all shared memory to the rings; over an fp8 cache
-  // at D <= 128 two CTAs share an SM (each with 3 + 3 stages of 16 KB, the
-  // same bytes in flight as one CTA with 6 + 6): twice the decode warps to
-  // hide the per-tile chain of conversions, warp MMAs and softmax
-  static constexpr int kCtasPerSm = (FP8 && !PF && D <= 128) ? 2 : 1;
+  // at D <= 128 and a bf16 one at D = 64 (tiles of 128-byte rows) two CTAs
+  // share an SM (each with 3 + 3 stages of 16 KB, the same bytes in flight as
+  // one CTA with 6 + 6): twice the decode warps to hide the per-tile chain of
+  // conversions, warp MMAs and softmax (bf16 at D = 64: 61.3 -> 55.0 us on the
+  // decode batch)
+  static constexpr int kCtasPerSm = (!PF && (FP8 ? D <= 128 : D == 64)) ? 2 : 1;
   static constexpr int kStagesK =
       PF ? (FP8 ? 2 : (D == 64 ? 4 : kQQ ? 2 : 3)) : (kCtasPerSm == 2 ? 3 : (FP8 || D == 64 ? 6 : 4));
   static constexpr int kStagesV =

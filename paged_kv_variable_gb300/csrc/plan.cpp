@@ -113,8 +113,9 @@ pkv_status make_plan(const pkv_problem* problem, const int32_t* h_q_lens, const 
     any_prefill |= h_q_lens[b] > 0 && !is_decode(h_q_lens[b]);
   }
   const int tq_item = tq_prefill * (any_decode ? 1 : prefill_q_tiles(D, p.cache_dtype == PKV_FP8_E4M3));
-  // decode-only plans over an fp8 cache at head dims up to 128 run two CTAs an SM
-  const bool two_ctas = p.cache_dtype == PKV_FP8_E4M3 && D <= 128 && !any_prefill;
+  // decode-only plans over an fp8 cache at head dims up to 128, or a bf16 one
+  // at head dim 64 (rows of 128 bytes), run two CTAs an SM
+  const bool two_ctas = (p.cache_dtype == PKV_FP8_E4M3 ? D <= 128 : D == 64) && !any_prefill;
   const int cps = two_ctas ? 2 : 1;
 
   int64_t total_q = 0, total_new = 0, total_split_keys = 0;

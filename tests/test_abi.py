@@ -80,7 +80,8 @@ def _coverage(spec, items, num_sms):
     for it in items:
         b, hk = it["seq"], it["kv_head"]
         # (decode-only plans over an fp8 cache at head_dim <= 128: two CTAs an SM)
-        cps = 2 if spec.cache_dtype == "fp8" and spec.d <= 128 and all(x["kind"] == 0 for x in items) else 1
+        two = spec.d <= 128 if spec.cache_dtype == "fp8" else spec.d == 64   # rows of 128 bytes or fewer
+        cps = 2 if two and all(x["kind"] == 0 for x in items) else 1
         assert 0 <= it["cta"] < num_sms * cps
         assert it["kv_begin"] % 128 == 0 or it["kv_begin"] == it["kv_end"]
         assert 0 <= it["head0"] and it["head0"] + it["num_heads"] <= G
