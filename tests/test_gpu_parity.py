@@ -804,21 +804,22 @@ def test_fp8_quantised_queries_prefill(P, G, causal, mixed):
 
 
 
-@pytest.mark.parametrize("dtype,sms,q8", [("fp8", 152, False), ("fp8", 12, False), ("fp8", 152, True),
-                                          ("bf16", 152, False), ("bf16", 8, False)])
-def test_decode_random_lengths_whole_and_split(dtype, sms, q8):
+@pytest.mark.parametrize("dtype,sms,q8,d", [("fp8", 152, False, 128), ("fp8", 12, False, 128), ("fp8", 152, True, 128),
+                                            ("bf16", 152, False, 128), ("bf16", 8, False, 128),
+                                            ("bf16", 152, False, 64), ("fp8", 152, False, 64)])
+def test_decode_random_lengths_whole_and_split(dtype, sms, q8, d):
     """Decode batches of random lengths U[512, 4096] with the full GQA shape
-    (Hq=32, Hkv=8, D=128, pages of 16, poisoned unused slots): at a few SMs
-    the planner places the 192 units whole (no partials, no combine), at 152
-    SMs (two CTAs an SM over an fp8 cache) it splits them to fill the CTAs;
-    every row against the oracle, the cache byte for byte."""
+    (Hq=32, Hkv=8, D=128 or 64, pages of 16, poisoned unused slots): at a few
+    SMs the planner places the 192 units whole (no partials, no combine), at
+    152 SMs (two CTAs an SM where rows are 128 bytes or fewer) it splits them
+    to fill the CTAs; every row against the oracle, the cache byte for byte."""
     import dataclasses
     rng = np.random.default_rng(7100 + sms + (1 if q8 else 0))
     B = 24
     lc = rng.integers(512, 4097, B).astype(np.int32)
     ones = np.ones(B, np.int32)
-    spec = synth.Spec(batch=B, hq=32, hkv=8, d=128, page_size=16, causal=True,
-                      softmax_scale=float(np.float32(1.0 / np.sqrt(128))), cache_dtype=dtype, q_lens=ones,
+    spec = synth.Spec(batch=B, hq=32, hkv=8, d=d, page_size=16, causal=True,
+                      softmax_scale=float(np.float32(1.0 / np.sqrt(d))), cache_dtype=dtype, q_lens=ones,
                       cache_lens=lc, new_lens=ones.copy(), capacity=4112, name="decode-rand")
     case = synth.make_case(spec, rng, sentinel="nan")
     if q8:
@@ -827,4 +828,5 @@ def test_decode_random_lengths_whole_and_split(dtype, sms, q8):
     g, _ = run_full(case, num_sms=sms)
     st = g.plan.stats()
     assert (st["num_split_units"] > 0) == (sms == 152)
-    assert st["num_ctas"] == sms * (2 if dtype == "fp8" else 1)
+    two = d <= 128 if dtype == "fp8" else d == 64   # rows of 128 bytes or fewer: two CTAs an SM
+    assert st["num_ctas"] == sms * (2 if two else 1)
