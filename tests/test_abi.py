@@ -382,7 +382,8 @@ def test_decode_only_split_policy(pkv):
     of the split placement, on the planner's costs) are not split, so no
     combine runs; a batch with a few long sequences is still split; a plan
     with prefill tiles splits its decode units finer (four items an SM); an
-    fp8 cache at head_dim <= 128 runs two CTAs an SM."""
+    fp8 cache at head_dim <= 128, or a bf16 one at head_dim 64, runs two
+    CTAs an SM."""
     def plan(dtype, q_lens, lc):
         B = len(lc)
         prob = pkv.make_problem(batch=B, num_heads_q=32, num_heads_kv=8, head_dim=128, page_size=16,
@@ -399,6 +400,12 @@ def test_decode_only_split_policy(pkv):
     assert skewed["max_cta_cost"] <= 1.1 * skewed["mean_cta_cost"]
     fp8 = plan("fp8", [1] * 64, [2048] * 64)
     assert fp8["num_ctas"] == 2 * 152 and fp8["num_split_units"] == 0
+    # rows of 128 bytes over a bf16 cache (head_dim 64) run two CTAs an SM too
+    prob64 = pkv.make_problem(batch=64, num_heads_q=32, num_heads_kv=8, head_dim=64, page_size=16,
+                              cache_capacity=65552, num_pages=200000, cache_dtype="bf16", causal=True,
+                              softmax_scale=0.125)
+    ones = np.ones(64, np.int32)
+    assert pkv.plan(prob64, ones, np.full(64, 2048, np.int32), ones, num_sms=152).stats()["num_ctas"] == 2 * 152
     # one prefill request in the batch: the decode units are cut for four items an SM
     mixed = plan("bf16", [1] * 63 + [512], list(lc[:63]) + [1000])
     assert mixed["num_prefill_items"] > 0 and mixed["num_split_units"] > 0 and mixed["num_ctas"] == 152
